@@ -1,0 +1,238 @@
+"""Pins of the oracle's whole-layer / whole-step composition.
+
+The parts are pinned in test_oracle_ops.py.  Here special cases reduce the
+layer to closed forms (zero projections, identity projections) so that a
+wiring mistake -- a wrong tensor fed forward, a wrong residual, a transposed
+operand, a missed cache write -- fails a check.  A float64 torch restatement
+of the layer on a random tiny case is an extra cross-check; beyond these the
+full-layer numbers are "parity unpinned" (no page prints a worked layer).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pdl_persistent_megakernel_gb300 import synth
+
+TINY = synth.DecodeConfig(
+    "tiny", hidden=128, inter=128, n_q_heads=1, n_kv_heads=1, head_dim=128,
+    n_layers=1, vocab=0, fp8=False, num_requests=2, tokens_per_request=3,
+    context=10, page_size=4, seed=99)
+
+
+def f64(b):
+    return oracle.bf16_to_double(np.asarray(b))
+
+
+def bf16t(a):
+    return torch.as_tensor(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def _weights(cfg, kind):
+    """kind: dict name -> 'zero' | 'eye' | 'rand'."""
+    w = synth.make_layer_weights(cfg, 0)
+    for name, k in kind.items():
+        shp = w[name].shape
+        if k == "zero":
+            w[name] = torch.zeros(shp, dtype=torch.bfloat16)
+        elif k == "eye":
+            n, kk = shp
+            w[name] = torch.cat([torch.eye(kk)] * (n // kk)).to(torch.bfloat16)
+    return w
+
+
+def _run(cfg, w, inputs=None):
+    inputs = inputs or synth.make_inputs(cfg)
+    res = oracle.decode_step(cfg, {"layers": [w] * cfg.n_layers,
+                                   "final_norm_w": None, "lm_head_w": None},
+                             inputs, trace=True)
+    return inputs, res
+
+
+def _np_cache(inputs):
+    return synth.as_u16(inputs["kv_pages"])
+
+
+def test_zero_projections_reduce_to_residual_and_mean_v():
+    cfg = TINY
+    w = _weights(cfg, {"w_qkv": "zero", "w_o": "zero", "w_gate_up": "zero",
+                       "w_down": "zero"})
+    inputs, r = _run(cfg, w)
+    x, res = synth.as_u16(inputs["x"]), synth.as_u16(inputs["residual"])
+    r1 = (torch.from_numpy(f64(x)) + torch.from_numpy(f64(res))).float().to(torch.bfloat16)
+    r1 = r1.view(torch.int16).numpy().view(np.uint16)
+    assert not f64(r["out"][0]).any()                  # y = 0
+    assert np.array_equal(r["out"][1], r1)             # r'' = r' = bf16(x + r)
+    assert np.array_equal(r["r2"], r1) and not f64(r["o2"]).any()
+    assert not f64(r["k_rot"]).any() and not f64(r["v"]).any()  # +-0
+    # new slots hold zeros, every other element of the cache is unchanged
+    before, after = _np_cache(inputs), r["kv_pages"].reshape(_np_cache(inputs).shape)
+    bt = inputs["block_table"].numpy()
+    pos = inputs["positions"].numpy()
+    mask = np.zeros(before.shape, bool)
+    for m in range(cfg.M):
+        rq = m // cfg.tokens_per_request
+        pg = bt[rq, pos[m] // cfg.page_size]
+        mask[0, pg, :, :, pos[m] % cfg.page_size, :] = True
+    assert not f64(after[mask]).any()
+    assert np.array_equal(after[~mask], before[~mask])
+    # q = 0 -> uniform softmax -> attention output = mean of V over [0, p]
+    for m in range(cfg.M):
+        rq = m // cfg.tokens_per_request
+        vs = np.stack([after[0, bt[rq, j // cfg.page_size], 1, 0, j % cfg.page_size]
+                       for j in range(pos[m] + 1)])
+        want = f64(vs).mean(axis=0)
+        # bf16 rounding of the exact mean: within half a bf16 ulp (2^-9 rel)
+        assert np.allclose(f64(r["attn"][m]), want, rtol=2 ** -8, atol=1e-30)
+
+
+def test_identity_projections_wire_each_stage():
+    # H = Hq d = I = 128: identity O, gate, up and down projections
+    cfg = TINY
+    w = _weights(cfg, {"w_qkv": "eye", "w_o": "eye", "w_gate_up": "eye",
+                       "w_down": "eye"})
+    inputs, r = _run(cfg, w)
+    # QKV = [I; I; I]: q = k = v = h1
+    h1 = f64(r["h1"])
+    assert np.array_equal(r["v"], r["h1"])
+    for m in range(cfg.M):
+        p = int(inputs["positions"][m])
+        for name, nw in (("q_rot", w["q_norm_w"]), ("k_rot", w["k_norm_w"])):
+            n = oracle.head_rmsnorm(h1[m], synth.as_u16(nw), cfg.eps)
+            n = f64(bf16t(n).view(torch.int16).numpy().view(np.uint16))
+            want = bf16t(oracle.rope(n, p, cfg.rope_theta))
+            assert np.array_equal(r[name][m], want.view(torch.int16).numpy().view(np.uint16))
+    # O = I: o2 = attn exactly; r2 = bf16(o2 + r1)
+    assert np.array_equal(r["o2"], r["attn"])
+    want_r2 = (torch.from_numpy(f64(r["o2"])) + torch.from_numpy(f64(r["r1"]))).float().to(torch.bfloat16)
+    assert np.array_equal(r["r2"], want_r2.view(torch.int16).numpy().view(np.uint16))
+    # gate = up = I: a = silu(h2) * h2; down = I: y = a
+    h2 = torch.from_numpy(f64(r["h2"]))
+    want_a = (torch.nn.functional.silu(h2) * h2).float().to(torch.bfloat16)
+    got_a = torch.from_numpy(r["act"].view(np.int16)).view(torch.bfloat16)
+    assert torch.equal(got_a, want_a) or (got_a.double() - want_a.double()).abs().max() <= 2 ** -7 * want_a.double().abs().max()
+    assert np.array_equal(r["y"], r["act"])
+    assert np.array_equal(r["out"][0], r["y"])
+
+
+def test_full_step_tail_and_layer_chaining():
+    cfg = TINY.replace(n_layers=3, vocab=300)
+    w = _weights(cfg, {"w_qkv": "zero", "w_o": "zero", "w_gate_up": "zero",
+                       "w_down": "zero"})
+    inputs = synth.make_inputs(cfg)
+    fn = synth.randn_bf16(cfg, "fn", (cfg.hidden,), 0.02, 1.0)
+    lm = synth.randn_bf16(cfg, "lm", (cfg.vocab, cfg.hidden), 0.02)
+    r = oracle.decode_step(cfg, {"layers": [w] * 3, "final_norm_w": fn,
+                                 "lm_head_w": lm}, inputs)
+    # zero layers: y = 0 and the residual stays bf16(x + r) through all layers
+    x, res = synth.as_u16(inputs["x"]), synth.as_u16(inputs["residual"])
+    r1 = (torch.from_numpy(f64(x)) + torch.from_numpy(f64(res))).float().to(torch.bfloat16)
+    r1 = r1.view(torch.int16).numpy().view(np.uint16)
+    _, hf_b, _ = oracle.add_rmsnorm(np.zeros_like(r1), r1, synth.as_u16(fn), cfg.eps)
+    want = f64(hf_b) @ f64(synth.as_u16(lm)).T
+    assert np.allclose(r["logits"], want.astype(np.float32), rtol=1e-6, atol=1e-6)
+    assert np.array_equal(r["ids"], want.argmax(axis=1))
+    # the cache of every layer got the step's writes
+    assert r["kv_pages"].size == _np_cache(inputs).size
+
+
+def test_fp8_layer_tracks_bf16_layer_within_tolerance():
+    cfg = TINY.replace(hidden=256, inter=256, n_q_heads=2, n_kv_heads=1)
+    w16 = synth.make_layer_weights(cfg, 0)
+    w8 = dict(w16)
+    for name in ("w_qkv", "w_o", "w_gate_up", "w_down"):
+        c, s = synth.quantize_blocks_e4m3(w16[name])
+        w8[name], w8[name + "_scale"] = c, s
+        # the bf16 reference uses the dequantized FP8 weights
+        deq = c.view(torch.float8_e4m3fn).float() * torch.kron(s, torch.ones(128, 128))
+        w16[name] = deq.to(torch.bfloat16)
+    inputs = synth.make_inputs(cfg)
+    r16 = oracle.decode_step(cfg, {"layers": [w16]}, inputs)
+    r8 = oracle.decode_step(cfg.replace(fp8=True), {"layers": [w8]}, inputs)
+    for i in range(2):
+        a, b = f64(r8["out"][i]), f64(r16["out"][i])
+        rel = np.sqrt(((a - b) ** 2).mean() / (b ** 2).mean())
+        # e4m3 activations (3 mantissa bits) give a few % RMS error; a wiring
+        # mistake (scales transposed or misplaced) gives O(1)
+        assert rel < 0.1, (i, rel)
+    # and the FP8 path really differs (activations are quantized)
+    assert not np.array_equal(r8["out"][0], r16["out"][0])
+
+
+def test_rejects_non_consecutive_positions():
+    cfg = TINY
+    inputs = synth.make_inputs(cfg)
+    inputs["positions"] = inputs["positions"].clone()
+    inputs["positions"][1] += 1
+    with pytest.raises(ValueError):
+        oracle.decode_step(cfg, {"layers": [synth.make_layer_weights(cfg, 0)]}, inputs)
+
+
+def _torch_layer(cfg, w, inputs):
+    """float64 torch restatement of the layer (extra cross-check)."""
+    bf = lambda t: t.to(torch.bfloat16).double()
+    d, G, P = cfg.head_dim, cfg.n_q_heads // cfg.n_kv_heads, cfg.page_size
+    x, res = inputs["x"].double(), inputs["residual"].double()
+    cache = inputs["kv_pages"].clone()
+
+    def rms(v, wt):
+        return v / torch.sqrt((v * v).mean(-1, keepdim=True) + cfg.eps) * wt.double()
+
+    r1 = bf(x + res)
+    h1 = bf(rms(r1, w["ln1_w"]))
+    qkv = bf(h1 @ w["w_qkv"].double().T)
+    M = cfg.M
+    heads = qkv.view(M, -1, d)
+    Hq, Hkv = cfg.n_q_heads, cfg.n_kv_heads
+    inv = torch.tensor([cfg.rope_theta ** (-2.0 * i / d) for i in range(d // 2)], dtype=torch.float64)
+    pos = inputs["positions"].double()
+    ang = pos[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rot(v):
+        a, b = v[..., :d // 2], v[..., d // 2:]
+        return torch.cat([a * cos[:, None] - b * sin[:, None], b * cos[:, None] + a * sin[:, None]], -1)
+
+    q = bf(rot(bf(rms(heads[:, :Hq], w["q_norm_w"]))))
+    k = bf(rot(bf(rms(heads[:, Hq:Hq + Hkv], w["k_norm_w"]))))
+    v = heads[:, Hq + Hkv:]
+    bt = inputs["block_table"]
+    for m in range(M):
+        rq, p = m // cfg.tokens_per_request, int(inputs["positions"][m])
+        pg = int(bt[rq, p // P])
+        cache[0, pg, 0, :, p % P] = k[m].to(torch.bfloat16)
+        cache[0, pg, 1, :, p % P] = v[m].to(torch.bfloat16)
+    attn = torch.zeros(M, Hq, d, dtype=torch.float64)
+    for m in range(M):
+        rq, p = m // cfg.tokens_per_request, int(inputs["positions"][m])
+        idx = [int(bt[rq, j // P]) for j in range(p + 1)]
+        sl = [j % P for j in range(p + 1)]
+        for hq in range(Hq):
+            K = torch.stack([cache[0, a, 0, hq // G, s] for a, s in zip(idx, sl)]).double()
+            V = torch.stack([cache[0, a, 1, hq // G, s] for a, s in zip(idx, sl)]).double()
+            attn[m, hq] = torch.softmax(q[m, hq] @ K.T / math.sqrt(d), 0) @ V
+    attn = bf(attn.view(M, -1))
+    o2 = bf(attn @ w["w_o"].double().T)
+    r2 = bf(o2 + r1)
+    h2 = bf(rms(r2, w["ln2_w"]))
+    gu = bf(h2 @ w["w_gate_up"].double().T)
+    I = cfg.inter
+    a = bf(torch.nn.functional.silu(gu[:, :I]) * gu[:, I:])
+    y = bf(a @ w["w_down"].double().T)
+    return y, r2
+
+
+def test_random_layer_matches_float64_torch_restatement():
+    cfg = TINY.replace(hidden=256, inter=384, n_q_heads=4, n_kv_heads=2)
+    w = synth.make_layer_weights(cfg, 0)
+    inputs = synth.make_inputs(cfg)
+    r = oracle.decode_step(cfg, {"layers": [w]}, inputs)
+    y, r2 = _torch_layer(cfg, w, inputs)
+    for got, want in ((r["out"][0], y), (r["out"][1], r2)):
+        g = f64(got)
+        diff = np.abs(g - want.numpy())
+        # identical up to a rare bf16 rounding flip of an intermediate
+        assert diff.max() <= 2 ** -6 * (1 + np.abs(want.numpy()).max())
+        assert (diff == 0).mean() > 0.95
