@@ -1,0 +1,208 @@
+/*
+ * dl.h -- C ABI of the GB300 (sm_103a) small-batch decode-step library.
+ *
+ * One memory-bound, Qwen3-shaped transformer decode step: fused residual
+ * add + RMSNorm (optionally with per-token FP8 quantisation), QKV projection,
+ * QK-norm + RoPE, paged KV-cache write, split-KV GQA attention with a
+ * log-sum-exp combine, O projection, a second add + RMSNorm, gate/up with
+ * SiLU*mul, down projection and, for full steps, the final norm, lm_head and
+ * greedy argmax.  The operation list follows the Qwen3 decode kernel list of
+ * the gap model on page "PDL and megakernel" (section on estimating the
+ * gaps); the fused Add + RMSNorm + Quant step is the first op of page
+ * "Kernel-Mega-PDL" (TLDR and section 1); the split-KV combine is page
+ * "kernel prologue/epilogue" section 4.2.
+ *
+ * The step runs under three schedules (page "Kernel-Mega-PDL"):
+ *   - serial single-stream kernels (section 1),
+ *   - CUDA Graph + multistream branches + programmatic dependent launch, each
+ *     consumer prefetching its weights before it waits on its producer
+ *     (sections 6 and 7),
+ *   - a persistent tile-instruction megakernel, one worker CTA per SM with
+ *     host-built per-SM queues and global event counters published with
+ *     release adds and awaited with acquire polls (section 4; page "PDL and
+ *     megakernel", megakernel section).
+ *
+ * Conventions.  All pointers passed to dl_decode_step are device pointers
+ * (16-byte aligned) unless the name says _host.  bf16 tensors are 16-bit
+ * bfloat16 bit patterns; FP8 weights are OCP e4m3 ("E4M3FN") codes with one
+ * fp32 scale per 128x128 block.  Weight matrices are [out, in] row-major.
+ * Errors: functions return a dl_status; dl_plan_create returns NULL; the
+ * message of the last failure on the calling thread is dl_last_error().
+ * A plan runs one step at a time: calls on one plan must be ordered by the
+ * caller (same stream, or synchronised).
+ */
+#ifndef DL_H
+#define DL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DL_OK = 0,
+  DL_ERR_INVALID_ARG = 1,   /* a host-visible argument check failed */
+  DL_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+  DL_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  DL_ERR_OOM = 4,           /* device allocation failed */
+  DL_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up */
+  DL_ERR_PLAN_INVALID = 6,  /* megakernel plan failed host validation */
+  DL_ERR_DEVICE_BOUNDS = 7  /* a device-side bounds check failed (bad block
+                               table entry or position) */
+} dl_status;
+
+typedef enum {
+  DL_MODE_SERIAL = 0,            /* one kernel per op, one stream, no PDL */
+  DL_MODE_PDL_GRAPH = 1,         /* graph, DAG branches, programmatic edges */
+  DL_MODE_MEGAKERNEL = 2,        /* persistent tile-instruction megakernel */
+  DL_MODE_GRAPH_LINEAR = 3,      /* graph, linear chain, full edges */
+  DL_MODE_GRAPH_LINEAR_PDL = 4,  /* graph, linear chain, programmatic edges */
+  DL_MODE_GRAPH_DAG = 5          /* graph, DAG branches, full edges */
+} dl_mode;
+
+typedef enum {
+  DL_WEIGHT_BF16 = 0,
+  DL_WEIGHT_FP8_E4M3_B128 = 1  /* e4m3 codes + fp32 scale per 128x128 block;
+                                  activations quantised per token per 128 */
+} dl_weight_dtype;
+
+/* Device pointers of one layer's weights.  Caller-owned; they must stay
+ * valid and unchanged for the plan's lifetime.  *_scale pointers are [N/128,
+ * K/128] fp32 for FP8 weights and NULL for bf16. */
+typedef struct {
+  const void* ln1_w;        /* bf16 [hidden] */
+  const void* w_qkv;        /* [(n_q_heads + 2 n_kv_heads) head_dim, hidden],
+                               rows = q heads | k heads | v heads */
+  const float* w_qkv_scale;
+  const void* q_norm_w;     /* bf16 [head_dim] */
+  const void* k_norm_w;     /* bf16 [head_dim] */
+  const void* w_o;          /* [hidden, n_q_heads head_dim] */
+  const float* w_o_scale;
+  const void* ln2_w;        /* bf16 [hidden] */
+  const void* w_gate_up;    /* [2 inter, hidden], rows = gate | up */
+  const float* w_gate_up_scale;
+  const void* w_down;       /* [hidden, inter] */
+  const float* w_down_scale;
+} dl_layer_weights;
+
+typedef struct {
+  int hidden, inter, n_q_heads, n_kv_heads, head_dim, n_layers;
+  int vocab;                /* 0: layer plan (no lm_head); else full step */
+  float eps;                /* RMSNorm epsilon (inside the square root) */
+  float rope_theta;         /* RoPE base; neox half-split pairing */
+  int weight_dtype;         /* dl_weight_dtype */
+  int num_requests;         /* R */
+  int tokens_per_request;   /* T; M = R * T tokens, request-major */
+  int page_size;            /* tokens per KV page */
+  int num_pages;            /* pages per layer in the cache */
+  int max_pages_per_request;/* block-table row length */
+  int max_context;          /* largest context (keys) a request may reach */
+  int num_sms;              /* worker CTAs; 0 = every SM of the device */
+  unsigned modes_mask;      /* bit m: prepare mode m (graphs, queues) */
+  const dl_layer_weights* layers;  /* [n_layers], read during create */
+  const void* final_norm_w; /* bf16 [hidden] (full steps) */
+  const void* lm_head_w;    /* bf16 [vocab, hidden] (full steps) */
+} dl_config;
+
+typedef struct dl_plan dl_plan;
+
+/* Build a plan on the current CUDA device: validates cfg, allocates the
+ * plan's workspace (activations, split-K/split-KV partials, counters,
+ * cos/sin table, TMA descriptors), records the per-mode launch lists,
+ * captures the graphs and packs the megakernel queues of modes_mask.
+ * Returns NULL on failure (see dl_last_error). */
+dl_plan* dl_plan_create(const dl_config* cfg);
+
+/* Message describing the last failure on this thread ("" if none). */
+const char* dl_last_error(void);
+
+/* One decode step, asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).
+ *   x, residual  bf16 [M, hidden], read only.
+ *   kv_pages     bf16 [n_layers][num_pages][2 (K,V)][n_kv_heads][page_size]
+ *                [head_dim]; the step writes K/V of its M tokens in place.
+ *   block_table  int32 [num_requests, max_pages_per_request]: logical page
+ *                i of request r lives in physical page block_table[r][i].
+ *   positions    int32 [M]: token m of request r = m / T sits at this
+ *                position; positions of a request are consecutive and its
+ *                context after the step is positions[last] + 1 keys.
+ *   out          layer plans: bf16 [2, M, hidden] = (layer output, new
+ *                residual); full plans: int32 [M] greedy token ids.
+ * Host-checkable errors return synchronously (DL_ERR_INVALID_ARG).
+ * Device-side failures (bounded wait expiry, bad block-table entry) are
+ * reported by dl_plan_status after the stream is synchronised. */
+dl_status dl_decode_step(dl_plan* plan, const void* x, const void* residual,
+                         void* kv_pages, const int32_t* block_table,
+                         const int32_t* positions, void* out, int mode,
+                         void* stream);
+
+/* End-to-end variant: x, residual, block_table, positions and out are HOST
+ * buffers (pinned memory makes the copies asynchronous); the step copies
+ * them to and from plan-owned device buffers on `stream`.  kv_pages is a
+ * device pointer.  The result is in out_host once the stream is done. */
+dl_status dl_decode_step_host(dl_plan* plan, const void* x_host,
+                              const void* residual_host, void* kv_pages,
+                              const int32_t* block_table_host,
+                              const int32_t* positions_host, void* out_host,
+                              int mode, void* stream);
+
+/* Device-side status of the last step(s); call after synchronising.  Reading
+ * it clears it. */
+dl_status dl_plan_status(dl_plan* plan);
+
+/* fp32 logits [M, vocab] of the last full step (device pointer), or NULL. */
+const float* dl_plan_logits(dl_plan* plan);
+
+/* Debug access to a plan-owned intermediate buffer of the last layer run:
+ *   0 r1 (bf16 [M,H])     1 h1 (bf16 [Mp,H] or e4m3 [Mp,H])  2 h1 scales
+ *   3 q (bf16 [M,Hq,d])   4 attn (bf16/e4m3 [Mp, Hq d])       5 attn scales
+ *   6 o2 (bf16 [M,H])     7 r2 (bf16 [M,H])                   8 h2
+ *   9 h2 scales           10 act (bf16/e4m3 [Mp, I])          11 act scales
+ *   12 y (bf16 [M,H])
+ * Returns DL_ERR_INVALID_ARG for an unknown index. */
+dl_status dl_plan_debug_buffer(dl_plan* plan, int which, void** ptr,
+                               size_t* bytes);
+
+/* Number of kernels one step of `mode` launches (for accounting). */
+int dl_plan_kernel_count(dl_plan* plan, int mode);
+
+/* Megakernel queue statistics: workers, queue length, events. */
+dl_status dl_plan_mega_info(dl_plan* plan, int* workers, int* qlen,
+                            int* events);
+
+/* Test hook for failure detection: with `delta` != 0 the megakernel plan's
+ * first wait threshold is raised by delta WITHOUT host validation, so the
+ * device wait must expire (bounded by budget_ns) and report DL_ERR_TIMEOUT.
+ * delta = 0 restores the validated plan.  Returns DL_ERR_PLAN_INVALID if the
+ * validator rejects the modified plan when validate != 0. */
+dl_status dl_plan_debug_perturb_wait(dl_plan* plan, unsigned delta,
+                                     unsigned long long budget_ns,
+                                     int validate);
+
+void dl_plan_destroy(dl_plan* plan);
+
+/* ------------------------------------------------------ test-only exports
+ * Bit-exact paged-KV indexing (the slot math of the QKV epilogue and the
+ * block-table gather of attention) as pure copies:
+ *   dl_test_kv_write: for each token m (request m / T, position positions[m])
+ *     copy src[m][kv][h][0..d) to kv_pages[layer][page][kv][h][slot][...]
+ *     with page = block_table[r][p / P], slot = p % P.
+ *   dl_test_kv_gather: dst[r][kv][h][j][0..d) = the cache row of key j of
+ *     request r, j < n_keys (same mapping).
+ * All pointers device; the calls are asynchronous on `stream`. */
+dl_status dl_test_kv_write(const void* src, void* kv_pages,
+                           const int32_t* block_table,
+                           const int32_t* positions, int layer, int M, int T,
+                           int n_kv_heads, int head_dim, int page_size,
+                           int num_pages, int max_pages, void* stream);
+dl_status dl_test_kv_gather(const void* kv_pages, const int32_t* block_table,
+                            void* dst, int layer, int R, int n_keys,
+                            int n_kv_heads, int head_dim, int page_size,
+                            int num_pages, int max_pages, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DL_H */

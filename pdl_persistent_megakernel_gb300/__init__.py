@@ -1,0 +1,264 @@
+"""GB300 (sm_103a) small-batch decode step, three schedules, behind a C ABI.
+
+The compute path is the CUDA library libdl.so (include/dl.h): every step of
+the decode step runs in its kernels.  This module only marshals arguments
+through ctypes; PyTorch supplies device memory and streams.  There is no CPU
+fallback: if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, List, Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(_ROOT, "include")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libdl.so")
+_SOURCES = ["dl_kernels.cu", "dl_host.cu"]
+_HEADERS = ["dl_internal.h", "dl_device.cuh", "dl_ops.cuh", "dl_kernels.h"]
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+MODE_SERIAL, MODE_PDL_GRAPH, MODE_MEGAKERNEL = 0, 1, 2
+MODE_GRAPH_LINEAR, MODE_GRAPH_LINEAR_PDL, MODE_GRAPH_DAG = 3, 4, 5
+MODE_NAMES = {0: "serial", 1: "pdl_graph", 2: "megakernel", 3: "graph_linear",
+              4: "graph_linear_pdl", 5: "graph_dag"}
+ALL_MODES = (1 << 6) - 1
+
+DEBUG_BUFFERS = {"r1": 0, "h1": 1, "h1_scales": 2, "q_rot": 3, "attn": 4,
+                 "attn_scales": 5, "o2": 6, "r2": 7, "h2": 8, "h2_scales": 9,
+                 "act": 10, "act_scales": 11, "y": 12}
+
+
+def _nvcc() -> str:
+    for cand in ("/usr/local/cuda/bin/nvcc", "nvcc"):
+        if cand == "nvcc" or os.path.exists(cand):
+            return cand
+    return "nvcc"
+
+
+def _cuda_lib_dir() -> str:
+    nv = _nvcc()
+    base = os.path.dirname(os.path.dirname(os.path.realpath(nv))) if os.path.sep in nv else "/usr/local/cuda"
+    return os.path.join(base, "lib64")
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libdl.so for sm_103a in-tree (two translation units in
+    parallel, then one link)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS]
+    deps.append(os.path.join(_INCLUDE, "dl.h"))
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= max(os.path.getmtime(d) for d in deps)):
+        return _SO
+    nv = _nvcc()
+    flags = [ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+             "-I" + _INCLUDE, "-I" + _CSRC]
+    objs = []
+
+    def compile_one(src):
+        obj = os.path.join(_BUILD, src.replace(".cu", f".{os.getpid()}.o"))
+        cmd = [nv] + flags + ["-c", os.path.join(_CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose:
+            print(r.stdout, r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(len(_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, _SOURCES))
+    tmp = _SO + f".{os.getpid()}.tmp"
+    cmd = [nv, ARCH, "-shared", "-cudart", "shared", "-o", tmp] + objs + [
+        "-Xlinker", "-rpath," + _cuda_lib_dir()]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, _SO)
+    for o in objs:
+        try:
+            os.remove(o)
+        except OSError:
+            pass
+    return _SO
+
+
+# ------------------------------------------------------------------ C types
+class LayerWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "ln1_w", "w_qkv", "w_qkv_scale", "q_norm_w", "k_norm_w", "w_o",
+        "w_o_scale", "ln2_w", "w_gate_up", "w_gate_up_scale", "w_down",
+        "w_down_scale")]
+
+
+class Config(C.Structure):
+    _fields_ = [("hidden", C.c_int), ("inter", C.c_int), ("n_q_heads", C.c_int),
+                ("n_kv_heads", C.c_int), ("head_dim", C.c_int),
+                ("n_layers", C.c_int), ("vocab", C.c_int), ("eps", C.c_float),
+                ("rope_theta", C.c_float), ("weight_dtype", C.c_int),
+                ("num_requests", C.c_int), ("tokens_per_request", C.c_int),
+                ("page_size", C.c_int), ("num_pages", C.c_int),
+                ("max_pages_per_request", C.c_int), ("max_context", C.c_int),
+                ("num_sms", C.c_int), ("modes_mask", C.c_uint),
+                ("layers", C.POINTER(LayerWeights)),
+                ("final_norm_w", C.c_void_p), ("lm_head_w", C.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
+           "dl_decode_step_host", "dl_plan_status", "dl_plan_logits",
+           "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
+           "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
+           "dl_test_kv_gather")
+
+
+def lib(path: Optional[str] = None):
+    """Load libdl.so (building it if missing).  Raises if it cannot load."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        so = path or build()
+        L = C.CDLL(so)
+        vp, i32, u32 = C.c_void_p, C.c_int, C.c_uint
+        L.dl_plan_create.argtypes = [C.POINTER(Config)]
+        L.dl_plan_create.restype = vp
+        L.dl_last_error.restype = C.c_char_p
+        L.dl_decode_step.argtypes = [vp] * 7 + [i32, vp]
+        L.dl_decode_step.restype = i32
+        L.dl_decode_step_host.argtypes = [vp] * 7 + [i32, vp]
+        L.dl_decode_step_host.restype = i32
+        L.dl_plan_status.argtypes = [vp]
+        L.dl_plan_status.restype = i32
+        L.dl_plan_logits.argtypes = [vp]
+        L.dl_plan_logits.restype = vp
+        L.dl_plan_debug_buffer.argtypes = [vp, i32, C.POINTER(vp), C.POINTER(C.c_size_t)]
+        L.dl_plan_debug_buffer.restype = i32
+        L.dl_plan_kernel_count.argtypes = [vp, i32]
+        L.dl_plan_kernel_count.restype = i32
+        L.dl_plan_mega_info.argtypes = [vp, C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]
+        L.dl_plan_mega_info.restype = i32
+        L.dl_plan_debug_perturb_wait.argtypes = [vp, u32, C.c_ulonglong, i32]
+        L.dl_plan_debug_perturb_wait.restype = i32
+        L.dl_plan_destroy.argtypes = [vp]
+        L.dl_test_kv_write.argtypes = [vp] * 4 + [i32] * 8 + [vp]
+        L.dl_test_kv_write.restype = i32
+        L.dl_test_kv_gather.argtypes = [vp] * 3 + [i32] * 8 + [vp]
+        L.dl_test_kv_gather.restype = i32
+        if path is None:
+            _lib = L
+        return L
+
+
+class DLError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"dl status {status}: {msg}")
+        self.status = status
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise DLError(rc, lib().dl_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+class Plan:
+    """A prepared decode step for one configuration (device-resident weights
+    supplied as torch CUDA tensors, kept alive by the plan)."""
+
+    def __init__(self, cfg, weights: Dict, modes_mask: int = ALL_MODES,
+                 max_context: Optional[int] = None, num_sms: int = 0):
+        L = lib()
+        self.cfg = cfg
+        self._keep: List = [weights]
+        n = cfg.n_layers
+        arr = (LayerWeights * n)()
+        for l, lw in enumerate(weights["layers"]):
+            s = arr[l]
+            for name, _ in LayerWeights._fields_:
+                setattr(s, name, _ptr(lw.get(name)))
+        self._layers = arr
+        c = Config()
+        c.hidden, c.inter = cfg.hidden, cfg.inter
+        c.n_q_heads, c.n_kv_heads, c.head_dim = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+        c.n_layers, c.vocab = n, cfg.vocab
+        c.eps, c.rope_theta = cfg.eps, cfg.rope_theta
+        c.weight_dtype = 1 if cfg.fp8 else 0
+        c.num_requests, c.tokens_per_request = cfg.num_requests, cfg.tokens_per_request
+        c.page_size, c.num_pages = cfg.page_size, cfg.num_pages
+        c.max_pages_per_request = cfg.pages_per_request
+        c.max_context = max_context or cfg.context
+        c.num_sms = num_sms
+        c.modes_mask = modes_mask
+        c.layers = arr
+        c.final_norm_w = _ptr(weights.get("final_norm_w"))
+        c.lm_head_w = _ptr(weights.get("lm_head_w"))
+        self._c = c
+        h = L.dl_plan_create(C.byref(c))
+        if not h:
+            raise DLError(-1, L.dl_last_error().decode())
+        self._h = h
+
+    def step(self, x, residual, kv_pages, block_table, positions, out,
+             mode: int = MODE_SERIAL, stream=None):
+        _check(lib().dl_decode_step(self._h, _ptr(x), _ptr(residual), _ptr(kv_pages),
+                                    _ptr(block_table), _ptr(positions), _ptr(out),
+                                    mode, _stream_handle(stream)))
+
+    def step_host(self, x, residual, kv_pages, block_table, positions, out,
+                  mode: int = MODE_SERIAL, stream=None):
+        """x, residual, block_table, positions, out: (pinned) CPU tensors."""
+        _check(lib().dl_decode_step_host(self._h, _ptr(x), _ptr(residual), _ptr(kv_pages),
+                                         _ptr(block_table), _ptr(positions), _ptr(out),
+                                         mode, _stream_handle(stream)))
+
+    def status(self):
+        _check(lib().dl_plan_status(self._h))
+
+    def debug_buffer(self, name: str):
+        p, n = C.c_void_p(), C.c_size_t()
+        _check(lib().dl_plan_debug_buffer(self._h, DEBUG_BUFFERS[name], C.byref(p), C.byref(n)))
+        return p.value, n.value
+
+    def logits_ptr(self) -> Optional[int]:
+        return lib().dl_plan_logits(self._h)
+
+    def kernel_count(self, mode: int) -> int:
+        return lib().dl_plan_kernel_count(self._h, mode)
+
+    def mega_info(self):
+        w, q, e = C.c_int(), C.c_int(), C.c_int()
+        _check(lib().dl_plan_mega_info(self._h, C.byref(w), C.byref(q), C.byref(e)))
+        return w.value, q.value, e.value
+
+    def perturb_wait(self, delta: int, budget_ns: int, validate: bool):
+        return lib().dl_plan_debug_perturb_wait(self._h, delta, budget_ns, int(validate))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().dl_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

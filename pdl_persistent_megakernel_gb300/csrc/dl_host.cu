@@ -1,0 +1,1030 @@
+// dl_host.cu -- the plan: validation, buffers, TMA descriptors, per-op launch
+// lists, graph capture (serial / graph / graph+PDL schedules), megakernel
+// queue packing and validation, and the C ABI of include/dl.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dl.h"
+#include "dl_internal.h"
+#include "dl_kernels.h"
+
+using namespace dl;
+
+// ------------------------------------------------------------------ errors
+static thread_local std::string g_err;
+
+static dl_status fail(dl_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+extern "C" const char* dl_last_error(void) { return g_err.c_str(); }
+
+#define CK(call)                                                             \
+  do {                                                                       \
+    cudaError_t e_ = (call);                                                 \
+    if (e_ != cudaSuccess)                                                   \
+      return fail(DL_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+// ------------------------------------------------------- tensor map encode
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static bool load_encode() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                       cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// [rows, K] row-major matrix, boxes of 128 bytes of K by box_rows rows,
+// 128-byte swizzle (the tcgen05 K-major canonical layout).
+static bool encode_map(CUtensorMap* m, const void* base, bool u8, uint64_t K,
+                       uint64_t rows, uint32_t box_rows) {
+  const int eb = u8 ? 1 : 2;
+  cuuint64_t dims[2] = {K, rows};
+  cuuint64_t strides[1] = {K * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(
+      m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// -------------------------------------------------------------------- plan
+namespace {
+
+struct LaunchOp {
+  OpArgs args;
+  const void* kernel = nullptr;
+  int grid = 0;
+  int smem = 0;
+  int branch = 0;  // 0 main chain, 1 side branch (DAG lists)
+  std::string name;
+};
+
+DPtr fixed(void* p) {
+  DPtr d;
+  d.p = p;
+  d.slot = -1;
+  d.pad = 0;
+  d.offset = 0;
+  return d;
+}
+
+DPtr bound(int slot, long long offset = 0) {
+  DPtr d;
+  d.p = nullptr;
+  d.slot = slot;
+  d.pad = 0;
+  d.offset = offset;
+  return d;
+}
+
+}  // namespace
+
+struct dl_plan {
+  dl_config cfg{};
+  std::vector<dl_layer_weights> layers;
+  int dev = 0, sms = 0, M = 0, Mp = 0, Mrows = 0, H = 0, I = 0, Hq = 0, Hkv = 0, d = 0;
+  int L = 0, V = 0, R = 0, T = 0, P = 0;
+  bool fp8 = false, full = false, mma = false;
+  unsigned long long budget_ns = 1000000000ull;
+
+  std::vector<void*> allocs;
+  Binding* d_binding = nullptr;
+  DevStatus* d_status = nullptr;
+  void *h1 = nullptr, *attn = nullptr, *h2 = nullptr, *act = nullptr;
+  float *h1s = nullptr, *attns = nullptr, *h2s = nullptr, *acts = nullptr;
+  void *r1 = nullptr, *r2 = nullptr, *o2 = nullptr, *y = nullptr, *q = nullptr;
+  void *hfin = nullptr, *rfin = nullptr;
+  float* logits = nullptr;
+  float* best_val = nullptr;
+  int* best_idx = nullptr;
+  float* rope = nullptr;
+  float* ws_gemm[2] = {nullptr, nullptr};
+  float* ws_attn = nullptr;
+  unsigned* counters = nullptr;
+  size_t n_counters = 0;
+  CUtensorMap* d_maps = nullptr;
+  std::vector<CUtensorMap> h_maps;
+
+  std::vector<LaunchOp> lin, dag;
+
+  // megakernel
+  OpArgs* d_ops = nullptr;
+  Instr* d_queues = nullptr;
+  unsigned* d_events = nullptr;
+  unsigned* d_finish = nullptr;
+  std::vector<Instr> queues;
+  int qlen = 0, workers = 0, n_events = 0, mega_smem = 0;
+
+  cudaGraphExec_t exec[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  cudaStream_t cap = nullptr, side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+
+  Binding last{};
+  bool have_last = false;
+  int perturb_idx = -1;      // instruction whose wait the failure test raised
+  unsigned perturb_orig = 0;
+
+  // end-to-end staging
+  void *st_x = nullptr, *st_res = nullptr, *st_out = nullptr;
+  int *st_bt = nullptr, *st_pos = nullptr;
+};
+
+static dl_status dev_alloc(dl_plan* p, void** out, size_t bytes) {
+  void* ptr = nullptr;
+  if (bytes == 0) bytes = 16;
+  const cudaError_t e = cudaMalloc(&ptr, bytes);
+  if (e != cudaSuccess)
+    return fail(DL_ERR_OOM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  p->allocs.push_back(ptr);
+  if (cudaMemset(ptr, 0, bytes) != cudaSuccess) return fail(DL_ERR_CUDA, "cudaMemset");
+  *out = ptr;
+  return DL_OK;
+}
+
+template <typename T>
+static dl_status dalloc(dl_plan* p, T** out, size_t bytes) {
+  void* v = nullptr;
+  const dl_status s = dev_alloc(p, &v, bytes);
+  *out = static_cast<T*>(v);
+  return s;
+}
+
+static void free_plan(dl_plan* p) {
+  if (!p) return;
+  for (auto& e : p->exec)
+    if (e) cudaGraphExecDestroy(e);
+  if (p->cap) cudaStreamDestroy(p->cap);
+  if (p->side) cudaStreamDestroy(p->side);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  for (void* a : p->allocs) cudaFree(a);
+  delete p;
+}
+
+static KernelCtx make_ctx(const dl_plan* p, int op_id) {
+  KernelCtx c;
+  c.binding = p->d_binding;
+  c.status = p->d_status;
+  c.budget_ns = p->budget_ns;
+  c.op_id = op_id;
+  return c;
+}
+
+// ------------------------------------------------------------ op builders
+static int choose_stages(int stage_bytes, int fixed_bytes, int target) {
+  int s = (target - fixed_bytes) / stage_bytes;
+  return std::max(2, std::min(kMaxStages, s));
+}
+
+static LaunchOp make_norm(dl_plan* p, DPtr x, DPtr res, DPtr rout, const void* w, void* hout,
+                          float* hscale, bool fp8, const char* name) {
+  LaunchOp op;
+  std::memset(&op.args, 0, sizeof(op.args));
+  op.args.kind = OP_NORM;
+  NormArgs& a = op.args.norm;
+  a.x = x;
+  a.res = res;
+  a.r_out = rout;
+  a.w = w;
+  a.h_out = hout;
+  a.h_scale = hscale;
+  a.fp8 = fp8 ? 1 : 0;
+  a.M = p->M;
+  a.H = p->H;
+  a.rows_per_cta = 1;
+  a.eps = p->cfg.eps;
+  op.kernel = norm_kernel();
+  op.grid = p->M;
+  op.smem = norm_smem_bytes();
+  op.name = name;
+  return op;
+}
+
+struct GemmSpec {
+  const CUtensorMap* tw;
+  const CUtensorMap* tx;
+  const float* wscale;
+  const float* xscale;
+  bool fp8;
+  int K;
+  int NT;
+  int t_base;
+  bool pair;
+  int up_row;
+  int epi;
+  int ws_slot;
+  const char* name;
+};
+
+static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
+  LaunchOp op;
+  std::memset(&op.args, 0, sizeof(op.args));
+  op.args.kind = OP_GEMM;
+  GemmArgs& a = op.args.gemm;
+  a.tmap_w = s.tw;
+  a.tmap_x = s.tx;
+  a.w_scale = s.wscale;
+  a.x_scale = s.xscale;
+  a.fp8 = s.fp8 ? 1 : 0;
+  a.mma = p->mma ? 1 : 0;
+  a.M = p->M;
+  a.Mp = p->mma ? p->Mp : p->M;
+  a.K = s.K;
+  a.KB = s.K * (s.fp8 ? 1 : 2) / 128;
+  a.NT = s.NT;
+  a.t_base = s.t_base;
+  a.pair = s.pair ? 1 : 0;
+  a.up_row = s.up_row;
+  const long long U = static_cast<long long>(a.NT) * a.KB;
+  a.G = static_cast<int>(std::min<long long>(p->sms, U));
+  const int npair = s.pair ? 2 : 1;
+  const int stage_bytes = npair * 16384 + ((a.Mp * 128 + 1023) / 1024) * 1024;
+  const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0);
+  a.stages = choose_stages(stage_bytes, fixed_bytes, 112 * 1024);
+  a.epi = s.epi;
+  a.ws = p->ws_gemm[s.ws_slot];
+  a.tile_cnt = cnt;
+  a.done_cnt = cnt + a.NT;
+  op.kernel = gemm_kernel(a.mma, a.mma ? a.Mp : a.M);
+  op.grid = a.G;
+  op.smem = gemm_smem_bytes(npair, a.Mp, a.stages);
+  op.name = s.name;
+  return op;
+}
+
+static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
+  LaunchOp op;
+  std::memset(&op.args, 0, sizeof(op.args));
+  op.args.kind = OP_ATTN;
+  AttnArgs& a = op.args.attn;
+  a.kv = bound(SLOT_KV);
+  a.bt = bound(SLOT_BT);
+  a.pos = bound(SLOT_POS);
+  a.q = p->q;
+  a.out = p->attn;
+  a.out_scale = p->attns;
+  a.fp8 = p->fp8 ? 1 : 0;
+  a.R = p->R;
+  a.T = p->T;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.d = p->d;
+  a.P = p->P;
+  a.num_pages = p->cfg.num_pages;
+  a.max_pages = p->cfg.max_pages_per_request;
+  a.layer = layer;
+  a.QR = p->T * (p->Hq / p->Hkv);
+  a.QRp = a.QR <= 16 ? 16 : (a.QR <= 32 ? 32 : 64);
+  a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
+  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
+  a.G = static_cast<int>(std::min<long long>(p->sms, U));
+  a.stages = 3;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d)));
+  a.ws = p->ws_attn;
+  a.pair_cnt = cnt;
+  op.kernel = attn_kernel();
+  op.grid = a.G;
+  op.smem = attn_smem_bytes(a.QRp, a.stages);
+  op.name = "attention";
+  return op;
+}
+
+// ------------------------------------------------------------ validation
+static dl_status check_config(const dl_config* c) {
+  if (!c) return fail(DL_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->hidden <= 0 || c->inter <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->n_layers <= 0 || c->num_requests <= 0 || c->tokens_per_request <= 0 ||
+      c->page_size <= 0 || c->num_pages <= 0 || c->max_pages_per_request <= 0 ||
+      c->max_context <= 0 || c->vocab < 0)
+    return fail(DL_ERR_INVALID_ARG, "non-positive size in cfg");
+  if (c->head_dim != 128) return fail(DL_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (c->n_q_heads % c->n_kv_heads) return fail(DL_ERR_INVALID_ARG, "n_q_heads % n_kv_heads != 0");
+  if (c->hidden % 128 || c->inter % 128) return fail(DL_ERR_UNSUPPORTED, "hidden and inter must be multiples of 128");
+  if (c->hidden > 8192) return fail(DL_ERR_UNSUPPORTED, "hidden > 8192");
+  if (c->vocab % 128) return fail(DL_ERR_UNSUPPORTED, "vocab must be a multiple of 128");
+  const int M = c->num_requests * c->tokens_per_request;
+  if (M > kMaxM) return fail(DL_ERR_UNSUPPORTED, "more than 64 tokens per step");
+  const int QR = c->tokens_per_request * (c->n_q_heads / c->n_kv_heads);
+  if (QR > kMaxQRows) return fail(DL_ERR_UNSUPPORTED, "tokens_per_request * group size > 64");
+  if (!(c->page_size % kAttnKeys == 0 || kAttnKeys % c->page_size == 0))
+    return fail(DL_ERR_UNSUPPORTED, "page_size must divide 64 or be a multiple of 64");
+  if (static_cast<long long>(c->max_pages_per_request) * c->page_size < c->max_context)
+    return fail(DL_ERR_INVALID_ARG, "max_pages_per_request * page_size < max_context");
+  if (c->weight_dtype != DL_WEIGHT_BF16 && c->weight_dtype != DL_WEIGHT_FP8_E4M3_B128)
+    return fail(DL_ERR_INVALID_ARG, "unknown weight_dtype");
+  if (c->weight_dtype == DL_WEIGHT_FP8_E4M3_B128 && c->vocab)
+    return fail(DL_ERR_UNSUPPORTED, "FP8 weights are supported for layer plans");
+  if (!c->layers) return fail(DL_ERR_INVALID_ARG, "layers is NULL");
+  return DL_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------- graph / launch helpers
+static cudaError_t launch_op(const dl_plan* p, const LaunchOp& op, cudaStream_t s, bool pdl,
+                             int op_id) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(op.grid);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = op.smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  KernelCtx ctx = make_ctx(p, op_id);
+  switch (op.args.kind) {
+    case OP_NORM: {
+      NormArgs a = op.args.norm;
+      void* args[] = {&a, &ctx};
+      return cudaLaunchKernelExC(&lc, op.kernel, args);
+    }
+    case OP_GEMM: {
+      GemmArgs a = op.args.gemm;
+      void* args[] = {&a, &ctx};
+      return cudaLaunchKernelExC(&lc, op.kernel, args);
+    }
+    case OP_ATTN: {
+      AttnArgs a = op.args.attn;
+      void* args[] = {&a, &ctx};
+      return cudaLaunchKernelExC(&lc, op.kernel, args);
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+static cudaError_t enqueue_list(dl_plan* p, const std::vector<LaunchOp>& ops, cudaStream_t s,
+                                bool pdl) {
+  for (size_t i = 0; i < ops.size(); ++i) {
+    const LaunchOp& op = ops[i];
+    if (op.branch == 1) {
+      // side branch: forks from the main stream after the previous main op
+      cudaError_t e = cudaEventRecord(p->ev_fork, s);
+      if (e != cudaSuccess) return e;
+      e = cudaStreamWaitEvent(p->side, p->ev_fork, 0);
+      if (e != cudaSuccess) return e;
+      e = launch_op(p, op, p->side, pdl, static_cast<int>(i));
+      if (e != cudaSuccess) return e;
+      e = cudaEventRecord(p->ev_join, p->side);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    if (op.branch == 2) {
+      // join point: the main stream waits for the side branch first
+      cudaError_t e = cudaStreamWaitEvent(s, p->ev_join, 0);
+      if (e != cudaSuccess) return e;
+    }
+    const cudaError_t e = launch_op(p, op, s, pdl, static_cast<int>(i));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static dl_status capture_graph(dl_plan* p, int mode) {
+  const bool dag = (mode == DL_MODE_PDL_GRAPH || mode == DL_MODE_GRAPH_DAG);
+  const bool pdl = (mode == DL_MODE_PDL_GRAPH || mode == DL_MODE_GRAPH_LINEAR_PDL);
+  const std::vector<LaunchOp>& ops = dag ? p->dag : p->lin;
+  cudaGraph_t g = nullptr;
+  CK(cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal));
+  const cudaError_t e = enqueue_list(p, ops, p->cap, pdl);
+  const cudaError_t e2 = cudaStreamEndCapture(p->cap, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return fail(DL_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
+  }
+  if (e2 != cudaSuccess) return fail(DL_ERR_CUDA, std::string("end capture: ") + cudaGetErrorString(e2));
+  const cudaError_t e3 = cudaGraphInstantiate(&p->exec[mode], g, 0);
+  cudaGraphDestroy(g);
+  if (e3 != cudaSuccess) return fail(DL_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e3));
+  return DL_OK;
+}
+
+// ------------------------------------------------------------ megakernel
+// Instructions of op k run on workers 0 .. G_k - 1; every instruction of op k
+// waits until event k-1 (one count per finished instruction of op k-1)
+// reaches G_{k-1}, and adds 1 to event k when done.  The ops are listed in a
+// topological order in which each depends on its predecessor, so the chain
+// of waits orders every true dependency (and every write-after-read reuse
+// of a buffer) of the list.
+static dl_status build_mega(dl_plan* p) {
+  const std::vector<LaunchOp>& ops = p->lin;
+  const int nops = static_cast<int>(ops.size());
+  p->workers = p->sms;
+  std::vector<std::vector<Instr>> qs(p->workers);
+  for (int k = 0; k < nops; ++k) {
+    const int G = ops[k].grid;
+    if (G > p->workers) return fail(DL_ERR_PLAN_INVALID, "op wider than the worker grid");
+    for (int c = 0; c < G; ++c) {
+      Instr in;
+      std::memset(&in, 0, sizeof(in));
+      in.op_row = static_cast<uint32_t>(k);
+      in.cta = static_cast<uint32_t>(c);
+      if (k > 0) {
+        in.n_wait = 1;
+        in.wait_event[0] = static_cast<uint32_t>(k - 1);
+        in.wait_value[0] = static_cast<uint32_t>(ops[k - 1].grid);
+      }
+      in.n_signal = 1;
+      in.signal_event[0] = static_cast<uint32_t>(k);
+      in.signal_inc[0] = 1;
+      qs[c].push_back(in);
+    }
+  }
+  p->qlen = 0;
+  for (auto& q : qs) p->qlen = std::max<int>(p->qlen, static_cast<int>(q.size()));
+  p->qlen += 1;  // at least one NoOp terminator per queue
+  p->queues.assign(static_cast<size_t>(p->workers) * p->qlen, Instr{});
+  for (int w = 0; w < p->workers; ++w)
+    for (int i = 0; i < p->qlen; ++i) {
+      Instr& dst = p->queues[static_cast<size_t>(w) * p->qlen + i];
+      if (i < static_cast<int>(qs[w].size())) {
+        dst = qs[w][i];
+      } else {
+        std::memset(&dst, 0, sizeof(dst));
+        dst.op_row = 0xffffffffu;
+      }
+    }
+  p->n_events = nops;
+  return DL_OK;
+}
+
+// Host validator: every wait names an event of an earlier op whose total
+// signals reach the threshold, queues are in global op order, and the grid
+// fits co-resident.  Returns DL_ERR_PLAN_INVALID with a message otherwise.
+static dl_status validate_mega(const dl_plan* p) {
+  std::vector<unsigned long long> total(p->n_events, 0);
+  for (const Instr& in : p->queues) {
+    if (in.op_row == 0xffffffffu) continue;
+    for (uint32_t s = 0; s < in.n_signal; ++s) {
+      if (in.signal_event[s] >= static_cast<uint32_t>(p->n_events))
+        return fail(DL_ERR_PLAN_INVALID, "signal of an unknown event");
+      total[in.signal_event[s]] += in.signal_inc[s];
+    }
+  }
+  for (int w = 0; w < p->workers; ++w) {
+    long long prev = -1;
+    bool ended = false;
+    for (int i = 0; i < p->qlen; ++i) {
+      const Instr& in = p->queues[static_cast<size_t>(w) * p->qlen + i];
+      if (in.op_row == 0xffffffffu) {
+        ended = true;
+        continue;
+      }
+      if (ended) return fail(DL_ERR_PLAN_INVALID, "instruction after the NoOp terminator");
+      if (static_cast<long long>(in.op_row) <= prev)
+        return fail(DL_ERR_PLAN_INVALID, "queue not in global op order");
+      prev = in.op_row;
+      if (in.n_wait > 4 || in.n_signal > 2) return fail(DL_ERR_PLAN_INVALID, "too many waits/signals");
+      for (uint32_t k = 0; k < in.n_wait; ++k) {
+        const uint32_t e = in.wait_event[k];
+        if (e >= in.op_row)
+          return fail(DL_ERR_PLAN_INVALID, "wait on an event of a later op (deadlock)");
+        if (in.wait_value[k] > total[e])
+          return fail(DL_ERR_PLAN_INVALID, "wait threshold above the event's total signals");
+      }
+    }
+  }
+  return DL_OK;
+}
+
+static dl_status upload_mega(dl_plan* p) {
+  CK(cudaMemcpy(p->d_queues, p->queues.data(), p->queues.size() * sizeof(Instr),
+                cudaMemcpyHostToDevice));
+  return DL_OK;
+}
+
+static cudaError_t launch_mega(dl_plan* p, cudaStream_t s) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(p->workers);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = p->mega_smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  MegaArgs m;
+  m.ops = p->d_ops;
+  m.queues = p->d_queues;
+  m.qlen = p->qlen;
+  m.workers = p->workers;
+  m.events = p->d_events;
+  m.finish_cnt = p->d_finish;
+  m.num_events = p->n_events;
+  m.budget_ns = p->budget_ns;
+  m.trace = nullptr;
+  KernelCtx ctx = make_ctx(p, -1);
+  void* args[] = {&m, &ctx};
+  return cudaLaunchKernelExC(&lc, mega_kernel(), args);
+}
+
+// ------------------------------------------------------------- creation
+static dl_status build_plan(dl_plan* p) {
+  const dl_config& c = p->cfg;
+  CK(cudaGetDevice(&p->dev));
+  int sms = 0;
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->dev));
+  p->sms = c.num_sms > 0 ? std::min(c.num_sms, sms) : sms;
+  p->H = c.hidden;
+  p->I = c.inter;
+  p->Hq = c.n_q_heads;
+  p->Hkv = c.n_kv_heads;
+  p->d = c.head_dim;
+  p->L = c.n_layers;
+  p->V = c.vocab;
+  p->R = c.num_requests;
+  p->T = c.tokens_per_request;
+  p->P = c.page_size;
+  p->M = p->R * p->T;
+  p->fp8 = c.weight_dtype == DL_WEIGHT_FP8_E4M3_B128;
+  p->full = c.vocab > 0;
+  p->mma = p->M > 8;
+  p->Mp = p->mma ? (p->M <= 16 ? 16 : (p->M <= 32 ? 32 : 64)) : p->M;
+  p->Mrows = p->Mp;
+  if (!load_encode()) return fail(DL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+
+  const int H = p->H, I = p->I, M = p->M, Mr = p->Mrows, QD = p->Hq * p->d;
+  const size_t eb = p->fp8 ? 1 : 2;
+  dl_status s;
+#define DA(ptr, bytes)                       \
+  if ((s = dalloc(p, &(ptr), (bytes))) != DL_OK) return s;
+  DA(p->d_binding, sizeof(Binding));
+  DA(p->d_status, sizeof(DevStatus));
+  DA(p->h1, static_cast<size_t>(Mr) * H * eb);
+  DA(p->h2, static_cast<size_t>(Mr) * H * eb);
+  DA(p->attn, static_cast<size_t>(Mr) * QD * eb);
+  DA(p->act, static_cast<size_t>(Mr) * I * eb);
+  DA(p->h1s, static_cast<size_t>(M) * (H / 128) * 4);
+  DA(p->h2s, static_cast<size_t>(M) * (H / 128) * 4);
+  DA(p->attns, static_cast<size_t>(M) * (QD / 128) * 4);
+  DA(p->acts, static_cast<size_t>(M) * (I / 128) * 4);
+  DA(p->r1, static_cast<size_t>(M) * H * 2);
+  DA(p->r2, static_cast<size_t>(M) * H * 2);
+  DA(p->o2, static_cast<size_t>(M) * H * 2);
+  DA(p->y, static_cast<size_t>(M) * H * 2);
+  DA(p->q, static_cast<size_t>(M) * QD * 2);
+  const int NTlm = p->full ? p->V / 128 : 0;
+  if (p->full) {
+    DA(p->hfin, static_cast<size_t>(Mr) * H * 2);
+    DA(p->rfin, static_cast<size_t>(M) * H * 2);
+    DA(p->logits, static_cast<size_t>(M) * p->V * 4);
+    DA(p->best_val, static_cast<size_t>(NTlm) * M * 4);
+    DA(p->best_idx, static_cast<size_t>(NTlm) * M * 4);
+  }
+  // RoPE table [max_context][d/2] (cos, sin), computed in double
+  {
+    const int maxp = c.max_context, half = p->d / 2;
+    std::vector<float> tab(static_cast<size_t>(maxp) * half * 2);
+    for (int pos = 0; pos < maxp; ++pos)
+      for (int i = 0; i < half; ++i) {
+        const double inv = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / p->d);
+        const double ang = static_cast<double>(pos) * inv;
+        tab[(static_cast<size_t>(pos) * half + i) * 2] = static_cast<float>(std::cos(ang));
+        tab[(static_cast<size_t>(pos) * half + i) * 2 + 1] = static_cast<float>(std::sin(ang));
+      }
+    DA(p->rope, tab.size() * 4);
+    CK(cudaMemcpy(p->rope, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice));
+  }
+  // workspaces: partial sums of the widest GEMM / attention split
+  {
+    const int npair = 2;
+    const size_t gws = static_cast<size_t>(p->sms) * 2 * npair * p->Mp * 128 * 4;
+    DA(p->ws_gemm[0], gws);
+    DA(p->ws_gemm[1], gws);
+    const int QR = p->T * (p->Hq / p->Hkv);
+    const int QRp = QR <= 16 ? 16 : (QR <= 32 ? 32 : 64);
+    DA(p->ws_attn, static_cast<size_t>(p->sms) * 2 * QRp * 129 * 4);
+  }
+  // tensor maps: 4 per layer (weights), 4 activations, lm_head + its input
+  const int n_maps = 4 * p->L + 4 + (p->full ? 2 : 0);
+  p->h_maps.resize(n_maps);
+  {
+    void* m = nullptr;
+    if ((s = dev_alloc(p, &m, sizeof(CUtensorMap) * n_maps)) != DL_OK) return s;
+    p->d_maps = static_cast<CUtensorMap*>(m);
+  }
+  const uint32_t xrows = static_cast<uint32_t>(p->mma ? p->Mp : p->M);
+  auto wmap = [&](int idx, const void* w, int N, int K) -> bool {
+    if (!w || !aligned16(w)) return false;
+    return encode_map(&p->h_maps[idx], w, p->fp8, K, N, 128);
+  };
+  for (int l = 0; l < p->L; ++l) {
+    const dl_layer_weights& lw = p->layers[l];
+    if (!lw.ln1_w || !lw.ln2_w || !lw.q_norm_w || !lw.k_norm_w)
+      return fail(DL_ERR_INVALID_ARG, "norm weight pointer is NULL");
+    if (p->fp8 && (!lw.w_qkv_scale || !lw.w_o_scale || !lw.w_gate_up_scale || !lw.w_down_scale))
+      return fail(DL_ERR_INVALID_ARG, "FP8 weights need scale pointers");
+    if (!wmap(4 * l + 0, lw.w_qkv, (p->Hq + 2 * p->Hkv) * p->d, H) ||
+        !wmap(4 * l + 1, lw.w_o, H, QD) || !wmap(4 * l + 2, lw.w_gate_up, 2 * I, H) ||
+        !wmap(4 * l + 3, lw.w_down, H, I))
+      return fail(DL_ERR_INVALID_ARG, "weight pointer NULL, unaligned or not encodable");
+  }
+  const int xm = 4 * p->L;
+  if (!encode_map(&p->h_maps[xm + 0], p->h1, p->fp8, H, xrows, xrows) ||
+      !encode_map(&p->h_maps[xm + 1], p->attn, p->fp8, QD, xrows, xrows) ||
+      !encode_map(&p->h_maps[xm + 2], p->h2, p->fp8, H, xrows, xrows) ||
+      !encode_map(&p->h_maps[xm + 3], p->act, p->fp8, I, xrows, xrows))
+    return fail(DL_ERR_CUDA, "activation tensor map encode failed");
+  if (p->full) {
+    if (!c.lm_head_w || !aligned16(c.lm_head_w) || !c.final_norm_w)
+      return fail(DL_ERR_INVALID_ARG, "lm_head / final norm pointer invalid");
+    if (!encode_map(&p->h_maps[xm + 4], c.lm_head_w, false, H, p->V, 128) ||
+        !encode_map(&p->h_maps[xm + 5], p->hfin, false, H, xrows, xrows))
+      return fail(DL_ERR_CUDA, "lm_head tensor map encode failed");
+  }
+  CK(cudaMemcpy(p->d_maps, p->h_maps.data(), sizeof(CUtensorMap) * n_maps,
+                cudaMemcpyHostToDevice));
+
+  // counters: per op its own slice (tile / pair counters + one done counter)
+  const int ntq = p->Hq + 2 * p->Hkv;
+  const size_t per_layer = (ntq + 1) * 2 + (p->R * p->Hkv + 1) + (H / 128 + 1) + (I / 128 + 1) +
+                           (H / 128 + 1) + 8;
+  p->n_counters = per_layer * p->L + (NTlm + 1) + 16;
+  DA(p->counters, p->n_counters * sizeof(unsigned));
+  size_t cpos = 0;
+  auto take = [&](size_t n) {
+    unsigned* r = p->counters + cpos;
+    cpos += n;
+    return r;
+  };
+
+  const size_t MH2 = static_cast<size_t>(M) * H * 2;
+  for (int l = 0; l < p->L; ++l) {
+    const dl_layer_weights& lw = p->layers[l];
+    const bool last = (l == p->L - 1);
+    const CUtensorMap* tm = p->d_maps;
+    // 1. residual add + RMSNorm (+ quant)
+    LaunchOp n1 = make_norm(p, l == 0 ? bound(SLOT_X) : fixed(p->y),
+                            l == 0 ? bound(SLOT_RES) : fixed(p->r2), fixed(p->r1), lw.ln1_w, p->h1,
+                            p->h1s, p->fp8, "add_rmsnorm1");
+    // 2. QKV projection + QK-norm + RoPE + paged KV write
+    GemmSpec qs{tm + 4 * l + 0, tm + xm + 0, lw.w_qkv_scale, p->h1s, p->fp8, H, ntq, 0, false, 0,
+                EPI_QKV_ROPE, 0, "qkv_rope_kvwrite"};
+    auto fill_qkv = [&](LaunchOp& op) {
+      GemmArgs& a = op.args.gemm;
+      a.q_out = p->q;
+      a.kv = bound(SLOT_KV);
+      a.bt = bound(SLOT_BT);
+      a.pos = bound(SLOT_POS);
+      a.q_norm_w = lw.q_norm_w;
+      a.k_norm_w = lw.k_norm_w;
+      a.rope_cs = p->rope;
+      a.rope_max_pos = c.max_context;
+      a.Hq = p->Hq;
+      a.Hkv = p->Hkv;
+      a.d = p->d;
+      a.T = p->T;
+      a.P = p->P;
+      a.num_pages = c.num_pages;
+      a.max_pages = c.max_pages_per_request;
+      a.layer = l;
+      a.eps = c.eps;
+    };
+    LaunchOp qkv = make_gemm(p, qs, take(ntq + 1));
+    fill_qkv(qkv);
+    // DAG variant: q heads on the main chain, k/v heads on a side branch
+    GemmSpec qq = qs;
+    qq.NT = p->Hq;
+    qq.name = "q_rope";
+    LaunchOp qop = make_gemm(p, qq, take(p->Hq + 1));
+    fill_qkv(qop);
+    GemmSpec qkvs = qs;
+    qkvs.NT = 2 * p->Hkv;
+    qkvs.t_base = p->Hq;
+    qkvs.ws_slot = 1;
+    qkvs.name = "kv_rope_write";
+    LaunchOp kvop = make_gemm(p, qkvs, take(2 * p->Hkv + 1));
+    fill_qkv(kvop);
+    kvop.branch = 1;
+    // 3. attention
+    LaunchOp at = make_attn(p, l, take(p->R * p->Hkv + 1));
+    // 4. O projection
+    GemmSpec os{tm + 4 * l + 1, tm + xm + 1, lw.w_o_scale, p->attns, p->fp8, QD, H / 128, 0,
+                false, 0, EPI_STORE_BF16, 0, "o_proj"};
+    LaunchOp oop = make_gemm(p, os, take(H / 128 + 1));
+    oop.args.gemm.out = fixed(p->o2);
+    oop.args.gemm.ldo = H;
+    // 5. residual add + RMSNorm (+ quant)
+    const DPtr r2dst = (last && !p->full) ? bound(SLOT_OUT, static_cast<long long>(MH2)) : fixed(p->r2);
+    LaunchOp n2 = make_norm(p, fixed(p->o2), fixed(p->r1), r2dst, lw.ln2_w, p->h2, p->h2s, p->fp8,
+                            "add_rmsnorm2");
+    // 6. gate/up + SiLU*mul (+ quant)
+    GemmSpec gs{tm + 4 * l + 2, tm + xm + 2, lw.w_gate_up_scale, p->h2s, p->fp8, H, I / 128, 0,
+                true, I, EPI_SILU_MUL, 0, "gate_up_silu"};
+    LaunchOp gop = make_gemm(p, gs, take(I / 128 + 1));
+    gop.args.gemm.act = p->act;
+    gop.args.gemm.act_scale = p->acts;
+    gop.args.gemm.act_ld = I;
+    // 7. down projection
+    GemmSpec ds{tm + 4 * l + 3, tm + xm + 3, lw.w_down_scale, p->acts, p->fp8, I, H / 128, 0,
+                false, 0, EPI_STORE_BF16, 0, "down_proj"};
+    LaunchOp dop = make_gemm(p, ds, take(H / 128 + 1));
+    dop.args.gemm.out = (last && !p->full) ? bound(SLOT_OUT, 0) : fixed(p->y);
+    dop.args.gemm.ldo = H;
+
+    for (LaunchOp* op : {&n1, &qkv, &at, &oop, &n2, &gop, &dop}) p->lin.push_back(*op);
+    LaunchOp at_join = at;
+    at_join.branch = 2;
+    for (LaunchOp* op : {&n1, &qop, &kvop, &at_join, &oop, &n2, &gop, &dop}) p->dag.push_back(*op);
+  }
+  if (p->full) {
+    LaunchOp nf = make_norm(p, fixed(p->y), fixed(p->r2), fixed(p->rfin), c.final_norm_w, p->hfin,
+                            nullptr, false, "final_norm");
+    const CUtensorMap* tm = p->d_maps;
+    GemmSpec ls{tm + xm + 4, tm + xm + 5, nullptr, nullptr, false, H, NTlm, 0, false, 0, EPI_LOGITS,
+                0, "lm_head_argmax"};
+    LaunchOp lop = make_gemm(p, ls, take(NTlm + 1));
+    lop.args.gemm.out = fixed(p->logits);
+    lop.args.gemm.ldo = p->V;
+    lop.args.gemm.best_val = p->best_val;
+    lop.args.gemm.best_idx = p->best_idx;
+    lop.args.gemm.ids = bound(SLOT_OUT);
+    p->lin.push_back(nf);
+    p->lin.push_back(lop);
+    p->dag.push_back(nf);
+    p->dag.push_back(lop);
+  }
+  if (cpos > p->n_counters) return fail(DL_ERR_CUDA, "counter pool overflow");
+
+  // kernel attributes: dynamic shared memory
+  int max_smem = 0;
+  for (const auto* list : {&p->lin, &p->dag})
+    for (const LaunchOp& op : *list) {
+      CK(cudaFuncSetAttribute(op.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, op.smem));
+      max_smem = std::max(max_smem, op.smem);
+    }
+
+  // streams / events for capture and the DAG fork
+  CK(cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking));
+  CK(cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking));
+  CK(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
+  CK(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
+
+  // e2e staging buffers
+  DA(p->st_x, MH2);
+  DA(p->st_res, MH2);
+  DA(p->st_bt, static_cast<size_t>(p->R) * c.max_pages_per_request * 4);
+  DA(p->st_pos, static_cast<size_t>(M) * 4);
+  DA(p->st_out, p->full ? static_cast<size_t>(M) * 4 : 2 * MH2);
+
+  // megakernel
+  if (c.modes_mask & (1u << DL_MODE_MEGAKERNEL)) {
+    if ((s = build_mega(p)) != DL_OK) return s;
+    if ((s = validate_mega(p)) != DL_OK) return s;
+    p->mega_smem = max_smem;
+    CK(cudaFuncSetAttribute(mega_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            p->mega_smem));
+    int per_sm = 0;
+    CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mega_kernel(), kThreads,
+                                                     p->mega_smem));
+    if (per_sm < 1) return fail(DL_ERR_PLAN_INVALID, "megakernel worker does not fit on an SM");
+    std::vector<OpArgs> h_ops;
+    for (const LaunchOp& op : p->lin) h_ops.push_back(op.args);
+    DA(p->d_ops, h_ops.size() * sizeof(OpArgs));
+    CK(cudaMemcpy(p->d_ops, h_ops.data(), h_ops.size() * sizeof(OpArgs), cudaMemcpyHostToDevice));
+    DA(p->d_queues, p->queues.size() * sizeof(Instr));
+    if ((s = upload_mega(p)) != DL_OK) return s;
+    DA(p->d_events, static_cast<size_t>(p->n_events) * 4);
+    DA(p->d_finish, 64);
+  }
+#undef DA
+  CK(cudaDeviceSynchronize());
+  // graphs
+  for (int mode : {DL_MODE_PDL_GRAPH, DL_MODE_GRAPH_LINEAR, DL_MODE_GRAPH_LINEAR_PDL,
+                   DL_MODE_GRAPH_DAG})
+    if (c.modes_mask & (1u << mode))
+      if ((s = capture_graph(p, mode)) != DL_OK) return s;
+  return DL_OK;
+}
+
+extern "C" dl_plan* dl_plan_create(const dl_config* cfg) {
+  if (check_config(cfg) != DL_OK) return nullptr;
+  dl_plan* p = new dl_plan();
+  p->cfg = *cfg;
+  p->layers.assign(cfg->layers, cfg->layers + cfg->n_layers);
+  p->cfg.layers = nullptr;
+  const dl_status s = build_plan(p);
+  if (s != DL_OK) {
+    const std::string msg = g_err;
+    free_plan(p);
+    g_err = msg;
+    return nullptr;
+  }
+  g_err.clear();
+  return p;
+}
+
+extern "C" void dl_plan_destroy(dl_plan* p) {
+  if (p) cudaDeviceSynchronize();
+  free_plan(p);
+}
+
+// ------------------------------------------------------------------ steps
+static dl_status bind(dl_plan* p, const Binding& b, cudaStream_t s) {
+  if (p->have_last && std::memcmp(&b, &p->last, sizeof(Binding)) == 0) return DL_OK;
+  CK(launch_bind(p->d_binding, b, s));
+  p->last = b;
+  p->have_last = true;
+  return DL_OK;
+}
+
+extern "C" dl_status dl_decode_step(dl_plan* p, const void* x, const void* residual,
+                                    void* kv_pages, const int32_t* block_table,
+                                    const int32_t* positions, void* out, int mode, void* stream) {
+  if (!p) return fail(DL_ERR_INVALID_ARG, "plan is NULL");
+  if (!x || !residual || !kv_pages || !block_table || !positions || !out)
+    return fail(DL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(kv_pages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3) || (reinterpret_cast<uintptr_t>(positions) & 3))
+    return fail(DL_ERR_INVALID_ARG, "misaligned tensor pointer");
+  if (mode < 0 || mode > 5) return fail(DL_ERR_INVALID_ARG, "unknown mode");
+  if (mode != DL_MODE_SERIAL && !(p->cfg.modes_mask & (1u << mode)))
+    return fail(DL_ERR_INVALID_ARG, "mode not prepared (modes_mask)");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Binding b{};
+  b.p[SLOT_X] = const_cast<void*>(x);
+  b.p[SLOT_RES] = const_cast<void*>(residual);
+  b.p[SLOT_KV] = kv_pages;
+  b.p[SLOT_BT] = const_cast<int32_t*>(block_table);
+  b.p[SLOT_POS] = const_cast<int32_t*>(positions);
+  b.p[SLOT_OUT] = out;
+  dl_status st = bind(p, b, s);
+  if (st != DL_OK) return st;
+  switch (mode) {
+    case DL_MODE_SERIAL: {
+      for (size_t i = 0; i < p->lin.size(); ++i) CK(launch_op(p, p->lin[i], s, false, static_cast<int>(i)));
+      break;
+    }
+    case DL_MODE_MEGAKERNEL:
+      CK(launch_mega(p, s));
+      break;
+    default:
+      CK(cudaGraphLaunch(p->exec[mode], s));
+      break;
+  }
+  return DL_OK;
+}
+
+extern "C" dl_status dl_decode_step_host(dl_plan* p, const void* x_host, const void* residual_host,
+                                         void* kv_pages, const int32_t* block_table_host,
+                                         const int32_t* positions_host, void* out_host, int mode,
+                                         void* stream) {
+  if (!p) return fail(DL_ERR_INVALID_ARG, "plan is NULL");
+  if (!x_host || !residual_host || !block_table_host || !positions_host || !out_host)
+    return fail(DL_ERR_INVALID_ARG, "NULL host pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t MH2 = static_cast<size_t>(p->M) * p->H * 2;
+  CK(cudaMemcpyAsync(p->st_x, x_host, MH2, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(p->st_res, residual_host, MH2, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(p->st_bt, block_table_host,
+                     static_cast<size_t>(p->R) * p->cfg.max_pages_per_request * 4,
+                     cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(p->st_pos, positions_host, static_cast<size_t>(p->M) * 4,
+                     cudaMemcpyHostToDevice, s));
+  const dl_status st = dl_decode_step(p, p->st_x, p->st_res, kv_pages, p->st_bt, p->st_pos,
+                                      p->st_out, mode, stream);
+  if (st != DL_OK) return st;
+  CK(cudaMemcpyAsync(out_host, p->st_out, p->full ? static_cast<size_t>(p->M) * 4 : 2 * MH2,
+                     cudaMemcpyDeviceToHost, s));
+  return DL_OK;
+}
+
+extern "C" dl_status dl_plan_status(dl_plan* p) {
+  if (!p) return fail(DL_ERR_INVALID_ARG, "plan is NULL");
+  DevStatus st;
+  CK(cudaMemcpy(&st, p->d_status, sizeof(st), cudaMemcpyDeviceToHost));
+  if (st.code == DERR_NONE) return DL_OK;
+  char buf[256];
+  std::snprintf(buf, sizeof(buf), "device error %u: op %u cta %u where %u value %u (block %u thread %u)",
+                st.code, st.info[0], st.info[1], st.info[2], st.info[3], st.info[4], st.info[5]);
+  // clear the status and every counter a failed step may have left raised
+  CK(cudaMemset(p->d_status, 0, sizeof(DevStatus)));
+  CK(cudaMemset(p->counters, 0, p->n_counters * sizeof(unsigned)));
+  if (p->d_events) CK(cudaMemset(p->d_events, 0, static_cast<size_t>(p->n_events) * 4));
+  if (p->d_finish) CK(cudaMemset(p->d_finish, 0, 64));
+  CK(cudaDeviceSynchronize());
+  return fail(st.code == DERR_TIMEOUT ? DL_ERR_TIMEOUT
+              : st.code == DERR_BOUNDS ? DL_ERR_DEVICE_BOUNDS
+                                       : DL_ERR_CUDA,
+              buf);
+}
+
+extern "C" const float* dl_plan_logits(dl_plan* p) { return p ? p->logits : nullptr; }
+
+extern "C" dl_status dl_plan_debug_buffer(dl_plan* p, int which, void** ptr, size_t* bytes) {
+  if (!p || !ptr || !bytes) return fail(DL_ERR_INVALID_ARG, "NULL argument");
+  const size_t eb = p->fp8 ? 1 : 2, M = p->M, Mr = p->Mrows, H = p->H, I = p->I;
+  const size_t QD = static_cast<size_t>(p->Hq) * p->d;
+  switch (which) {
+    case 0: *ptr = p->r1; *bytes = M * H * 2; break;
+    case 1: *ptr = p->h1; *bytes = Mr * H * eb; break;
+    case 2: *ptr = p->h1s; *bytes = M * (H / 128) * 4; break;
+    case 3: *ptr = p->q; *bytes = M * QD * 2; break;
+    case 4: *ptr = p->attn; *bytes = Mr * QD * eb; break;
+    case 5: *ptr = p->attns; *bytes = M * (QD / 128) * 4; break;
+    case 6: *ptr = p->o2; *bytes = M * H * 2; break;
+    case 7: *ptr = p->r2; *bytes = M * H * 2; break;
+    case 8: *ptr = p->h2; *bytes = Mr * H * eb; break;
+    case 9: *ptr = p->h2s; *bytes = M * (H / 128) * 4; break;
+    case 10: *ptr = p->act; *bytes = Mr * I * eb; break;
+    case 11: *ptr = p->acts; *bytes = M * (I / 128) * 4; break;
+    case 12: *ptr = p->y; *bytes = M * H * 2; break;
+    default: return fail(DL_ERR_INVALID_ARG, "unknown debug buffer");
+  }
+  return DL_OK;
+}
+
+extern "C" int dl_plan_kernel_count(dl_plan* p, int mode) {
+  if (!p) return -1;
+  if (mode == DL_MODE_MEGAKERNEL) return 1;
+  if (mode == DL_MODE_PDL_GRAPH || mode == DL_MODE_GRAPH_DAG) return static_cast<int>(p->dag.size());
+  return static_cast<int>(p->lin.size());
+}
+
+extern "C" dl_status dl_plan_mega_info(dl_plan* p, int* workers, int* qlen, int* events) {
+  if (!p || !p->d_queues) return fail(DL_ERR_INVALID_ARG, "no megakernel plan");
+  if (workers) *workers = p->workers;
+  if (qlen) *qlen = p->qlen;
+  if (events) *events = p->n_events;
+  return DL_OK;
+}
+
+extern "C" dl_status dl_plan_debug_perturb_wait(dl_plan* p, unsigned delta,
+                                                unsigned long long budget_ns, int validate) {
+  if (!p || !p->d_queues) return fail(DL_ERR_INVALID_ARG, "no megakernel plan");
+  static const unsigned long long kDefault = 1000000000ull;
+  // worker 0's first instruction with a wait
+  if (p->perturb_idx < 0) {
+    for (int i = 0; i < p->qlen; ++i) {
+      const Instr& in = p->queues[i];
+      if (in.op_row != 0xffffffffu && in.n_wait > 0) {
+        p->perturb_idx = i;
+        p->perturb_orig = in.wait_value[0];
+        break;
+      }
+    }
+  }
+  if (p->perturb_idx < 0) return fail(DL_ERR_INVALID_ARG, "no waiting instruction");
+  Instr* target = &p->queues[p->perturb_idx];
+  const unsigned base_value = p->perturb_orig;
+  target->wait_value[0] = base_value + delta;
+  p->budget_ns = delta ? budget_ns : kDefault;
+  if (validate) {
+    const dl_status v = validate_mega(p);
+    if (v != DL_OK) {
+      target->wait_value[0] = base_value;
+      p->budget_ns = kDefault;
+      return v;
+    }
+  }
+  return upload_mega(p);
+}
+
+// ------------------------------------------------------------ test hooks
+extern "C" dl_status dl_test_kv_write(const void* src, void* kv_pages, const int32_t* block_table,
+                                      const int32_t* positions, int layer, int M, int T,
+                                      int n_kv_heads, int head_dim, int page_size, int num_pages,
+                                      int max_pages, void* stream) {
+  if (!src || !kv_pages || !block_table || !positions || M <= 0 || T <= 0)
+    return fail(DL_ERR_INVALID_ARG, "bad argument");
+  static DevStatus* st = nullptr;
+  if (!st && cudaMalloc(&st, sizeof(DevStatus)) == cudaSuccess) cudaMemset(st, 0, sizeof(DevStatus));
+  CK(launch_test_kv_write(src, kv_pages, block_table, positions, layer, M, T, n_kv_heads, head_dim,
+                          page_size, num_pages, max_pages, st, static_cast<cudaStream_t>(stream)));
+  return DL_OK;
+}
+
+extern "C" dl_status dl_test_kv_gather(const void* kv_pages, const int32_t* block_table, void* dst,
+                                       int layer, int R, int n_keys, int n_kv_heads, int head_dim,
+                                       int page_size, int num_pages, int max_pages, void* stream) {
+  if (!kv_pages || !block_table || !dst || R <= 0 || n_keys <= 0)
+    return fail(DL_ERR_INVALID_ARG, "bad argument");
+  static DevStatus* st = nullptr;
+  if (!st && cudaMalloc(&st, sizeof(DevStatus)) == cudaSuccess) cudaMemset(st, 0, sizeof(DevStatus));
+  CK(launch_test_kv_gather(kv_pages, block_table, dst, layer, R, n_keys, n_kv_heads, head_dim,
+                           page_size, num_pages, max_pages, st, static_cast<cudaStream_t>(stream)));
+  return DL_OK;
+}

@@ -1,0 +1,201 @@
+// dl_internal.h -- structures shared by the host planner and the device code
+// of the decode-step library (not part of the public C ABI).
+//
+// Every operation of the decode step is a "tile engine" that a CTA runs over
+// its share of the operation's work.  The same engine runs inside the
+// standalone kernels (serial and graph schedules, one kernel per operation)
+// and inside the persistent megakernel (one instruction per CTA share), so
+// the three schedules differ only in how shares are ordered on the GPU.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda.h>
+
+namespace dl {
+
+// ------------------------------------------------------------------ limits
+constexpr int kThreads = 288;        // 9 warps: warp 0 loads, warps 1-8 compute
+constexpr int kConsumerThreads = 256;
+constexpr int kBN = 128;             // weight rows per GEMM tile
+constexpr int kBKBytes = 128;        // bytes of K per pipeline stage (one
+                                     // 128-byte swizzle atom: 64 bf16 / 128 e4m3)
+constexpr int kMaxM = 64;            // tokens per step
+constexpr int kAttnKeys = 64;        // keys per attention pipeline stage
+constexpr int kMaxQRows = 64;        // query rows per (request, kv head)
+constexpr int kMaxStages = 8;
+
+// ----------------------------------------------------- runtime bindings
+// Pointers supplied per decode call (the caller's tensors).  Kernels read
+// them from a small device table so that captured graphs and megakernel
+// queues stay valid when the caller passes new buffers.
+enum BindingSlot : int {
+  SLOT_X = 0,        // bf16 [M, H]          layer-0 input
+  SLOT_RES = 1,      // bf16 [M, H]          layer-0 residual
+  SLOT_KV = 2,       // bf16 paged KV cache [L][pages][2][Hkv][P][d]
+  SLOT_BT = 3,       // int32 [R, max_pages] block table
+  SLOT_POS = 4,      // int32 [M]            positions
+  SLOT_OUT = 5,      // bf16 [2, M, H] (layer plans) / int32 [M] (full plans)
+  NUM_SLOTS = 8
+};
+
+struct Binding {
+  void* p[NUM_SLOTS];
+};
+
+// A pointer operand: a fixed plan-owned address, or (slot >= 0) a binding
+// slot plus a byte offset.
+struct DPtr {
+  void* p;
+  int slot;
+  int pad;
+  long long offset;
+};
+
+// Device-side error word.  code != 0 after a step means a bounded wait gave
+// up or a bounds check failed; info holds (op, cta, where, value).
+struct DevStatus {
+  unsigned code;
+  unsigned info[7];
+  unsigned abort;     // set with code: every worker leaves its loop early
+  unsigned pad[7];
+};
+
+enum DevErr : unsigned {
+  DERR_NONE = 0,
+  DERR_TIMEOUT = 1,
+  DERR_BOUNDS = 2,
+  DERR_BAD_OP = 3,
+};
+
+// ------------------------------------------------------------------ ops
+enum OpKind : int {
+  OP_NOP = 0,
+  OP_NORM = 1,        // residual add + RMSNorm (+ FP8 quant)
+  OP_GEMM = 2,        // weight-streaming projection + fused epilogue
+  OP_ATTN = 3,        // split-KV attention + log-sum-exp combine (+ quant)
+};
+
+enum Epilogue : int {
+  EPI_QKV_ROPE = 0,   // QK-norm + RoPE; q -> buffer, k/v -> paged cache
+  EPI_STORE_BF16 = 1, // out[m][n] = bf16(acc)
+  EPI_SILU_MUL = 2,   // a = silu(bf16 g) * bf16 u (+ FP8 quant per 128)
+  EPI_LOGITS = 3,     // fp32 logits + greedy argmax (lowest index on ties)
+};
+
+struct NormArgs {
+  DPtr x, res;        // bf16 [M, H]
+  DPtr r_out;         // bf16 [M, H] new residual
+  const void* w;      // bf16 [H]
+  void* h_out;        // bf16 [Mp, H] or e4m3 codes [Mp, H]
+  float* h_scale;     // FP8: [M, H/128]
+  int fp8, M, H, rows_per_cta;
+  float eps;
+};
+
+struct GemmArgs {
+  const CUtensorMap* tmap_w;  // weights [N, K], 128B-swizzled boxes (128 B x 128 rows)
+  const CUtensorMap* tmap_x;  // activations [Mp, K], boxes (128 B x Mp rows)
+  const float* w_scale;       // FP8 block scales [N/128, K/128]
+  const float* x_scale;       // FP8 activation scales [M, K/128]
+  int fp8;
+  int mma;                    // 1: tcgen05 (M > 8), 0: CUDA-core GEMV
+  int M, Mp;                  // tokens, rows of the activation tile
+  int K;                      // elements
+  int KB;                     // 128-byte k-blocks per tile
+  int NT;                     // output tiles (pairs for gate/up)
+  int t_base;                 // first tile (a branch may cover a sub-range)
+  int pair;                   // 1: tile t = gate rows t*128.. + up rows up_row+t*128..
+  int up_row;                 // first up row (= I) for gate/up
+  int G;                      // CTAs sharing the units
+  int stages;
+  int epi;
+  // partial sums (Stream-K fix-up) and counters
+  float* ws;                  // [G][2][npair][Mp][128] fp32
+  unsigned* tile_cnt;         // [NT]
+  unsigned* done_cnt;         // [1] (EPI_LOGITS)
+  // epilogue operands
+  DPtr out;                   // STORE_BF16: bf16 [M, ldo]; LOGITS: fp32 [M, V]
+  int ldo;
+  void* act;                  // SILU_MUL: bf16 [Mp, I] or codes [Mp, I]
+  float* act_scale;           // [M, I/128]
+  int act_ld;
+  // QKV epilogue
+  void* q_out;                // bf16 [M, Hq, d]
+  DPtr kv, bt, pos;
+  const void* q_norm_w;
+  const void* k_norm_w;
+  const float* rope_cs;       // [max_pos][d/2][2] (cos, sin) fp32
+  int rope_max_pos;
+  int Hq, Hkv, d, T, P, num_pages, max_pages, layer;
+  float eps;
+  // LOGITS epilogue
+  float* best_val;            // [NT][M]
+  int* best_idx;              // [NT][M]
+  DPtr ids;                   // int32 [M]
+};
+
+struct AttnArgs {
+  DPtr kv, bt, pos;
+  const void* q;              // bf16 [M, Hq, d] (after QK-norm + RoPE)
+  void* out;                  // bf16 [Mp, Hq d] or codes
+  float* out_scale;           // FP8: [M, Hq d / 128]
+  int fp8;
+  int R, T, Hq, Hkv, d, P, num_pages, max_pages, layer;
+  int QR, QRp;                // query rows per pair (T * G), padded to 16
+  int NB;                     // 64-key blocks per pair (from max_context)
+  int G;                      // CTAs
+  int stages;
+  float scale_log2;           // log2(e) / sqrt(d)
+  float* ws;                  // partials [G][2][QRp][d] + lse [G][2][QRp]
+  unsigned* pair_cnt;         // [R * Hkv]
+};
+
+struct OpArgs {
+  int kind;
+  int pad[3];
+  union {
+    NormArgs norm;
+    GemmArgs gemm;
+    AttnArgs attn;
+  };
+};
+
+// ------------------------------------------------- megakernel instructions
+// 32 x u32 = 128 bytes.  Addresses live in the op-argument table, never in
+// the instruction; an instruction names its op row and its CTA share.
+struct Instr {
+  uint32_t op_row;            // index into the OpArgs table (0xffffffff: NoOp)
+  uint32_t cta;               // this worker's share index within the op
+  uint32_t n_wait;
+  uint32_t n_signal;
+  uint32_t wait_event[4];
+  uint32_t wait_value[4];     // wait until event >= value
+  uint32_t signal_event[2];
+  uint32_t signal_inc[2];
+  uint32_t pad[16];
+};
+static_assert(sizeof(Instr) == 128, "instruction is 128 bytes");
+
+struct MegaArgs {
+  const OpArgs* ops;
+  const Instr* queues;        // [workers][qlen]
+  int qlen;
+  int workers;
+  unsigned* events;           // event counters; the last worker to leave
+                              // zeroes them (and finish_cnt) for the next step
+  unsigned* finish_cnt;
+  int num_events;
+  unsigned long long budget_ns;
+  unsigned* trace;            // optional [workers][qlen][4] (start, ready, done)
+};
+
+struct KernelCtx {
+  const Binding* binding;
+  DevStatus* status;
+  unsigned long long budget_ns;   // bounded-wait budget
+  int op_id;                      // for error reports
+};
+
+}  // namespace dl

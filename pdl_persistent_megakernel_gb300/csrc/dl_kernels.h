@@ -1,0 +1,26 @@
+// dl_kernels.h -- host-visible entry points of dl_kernels.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "dl_internal.h"
+
+namespace dl {
+
+const void* gemm_kernel(int mma, int m_or_mp);
+const void* norm_kernel();
+const void* attn_kernel();
+const void* mega_kernel();
+cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s);
+int gemm_smem_bytes(int npair, int Mp, int stages);
+int attn_smem_bytes(int QRp, int stages);
+int norm_smem_bytes();
+cudaError_t launch_test_kv_write(const void* src, void* kv, const int* bt, const int* pos,
+                                 int layer, int M, int T, int Hkv, int d, int P,
+                                 int num_pages, int max_pages, DevStatus* st,
+                                 cudaStream_t s);
+cudaError_t launch_test_kv_gather(const void* kv, const int* bt, void* dst, int layer, int R,
+                                  int n_keys, int Hkv, int d, int P, int num_pages,
+                                  int max_pages, DevStatus* st, cudaStream_t s);
+
+}  // namespace dl

@@ -1,0 +1,51 @@
+"""CPU checks of the C ABI library: it builds for sm_103a, loads, and exports
+every function include/dl.h declares (no compute call without a GPU)."""
+import os
+import re
+
+import pytest
+
+import pdl_persistent_megakernel_gb300 as dl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            txt = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"\b(dl_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    try:
+        so = dl.build()
+    except (RuntimeError, FileNotFoundError) as e:  # no nvcc here
+        pytest.skip(f"cannot build: {e}")
+    L = dl.lib()
+    declared = _declared()
+    assert {"dl_plan_create", "dl_decode_step", "dl_plan_destroy"} <= declared
+    missing = [n for n in declared if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(dl.EXPORTS) <= declared
+
+
+def test_last_error_is_empty_string_initially():
+    L = dl.lib()
+    assert isinstance(L.dl_last_error(), bytes)
+
+
+def test_plan_create_rejects_bad_config_without_gpu():
+    # config validation runs before any CUDA call
+    from pdl_persistent_megakernel_gb300 import synth
+    cfg = synth.DecodeConfig("bad", hidden=256, inter=384, n_q_heads=4, n_kv_heads=2,
+                             head_dim=64, n_layers=1, vocab=0, fp8=False, num_requests=1,
+                             tokens_per_request=1, context=100, page_size=16)
+    import torch
+    w = {"layers": [{}]}
+    with pytest.raises(dl.DLError) as e:
+        dl.Plan(cfg, w)
+    assert "head_dim" in str(e.value)

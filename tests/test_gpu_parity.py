@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, on
+seeded inputs, element by element, for every schedule.
+
+Small cases span several weight tiles and Stream-K splits with a ragged KV
+tail; the full-size cases are the Qwen3-0.6B layer (batch 1, ctx 1024) and
+the Qwen3-8B FP8 layer (M = 16, ctx 8192) in the launch configuration the
+bench times.  Tolerances: bf16 paths |gpu - oracle| <= 1e-2 (1 + |oracle|);
+the FP8 path max error <= 5e-2 * rms(oracle) per tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import pdl_persistent_megakernel_gb300 as dl
+from pdl_persistent_megakernel_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_harness import (Case, as_bf16_np, as_f32_np, as_u8_np, bf16_close,
+                             dequant, f64, read_debug, rel_rms_close)
+
+SMALL = {
+    # GEMV (M = 1), 16-token pages, ctx 100 = 64 + a ragged 36
+    "bf16_m1": synth.DecodeConfig("bf16_m1", hidden=256, inter=384, n_q_heads=4, n_kv_heads=2,
+                                  head_dim=128, n_layers=1, vocab=0, fp8=False, num_requests=1,
+                                  tokens_per_request=1, context=100, page_size=16, seed=11),
+    # GEMV with 4 tokens (2 requests x 2), GQA group 4
+    "bf16_m4": synth.DecodeConfig("bf16_m4", hidden=512, inter=640, n_q_heads=8, n_kv_heads=2,
+                                  head_dim=128, n_layers=1, vocab=0, fp8=False, num_requests=2,
+                                  tokens_per_request=2, context=150, page_size=16, seed=12),
+    # tcgen05 path, bf16, M = 16 (2 x 8), 64-token pages
+    "bf16_m16": synth.DecodeConfig("bf16_m16", hidden=512, inter=768, n_q_heads=8, n_kv_heads=2,
+                                   head_dim=128, n_layers=1, vocab=0, fp8=False, num_requests=2,
+                                   tokens_per_request=8, context=200, page_size=64, seed=13),
+    # tcgen05 path, FP8, M = 16
+    "fp8_m16": synth.DecodeConfig("fp8_m16", hidden=512, inter=768, n_q_heads=8, n_kv_heads=2,
+                                  head_dim=128, n_layers=1, vocab=0, fp8=True, num_requests=2,
+                                  tokens_per_request=8, context=200, page_size=64, seed=14),
+    # two layers + lm_head + argmax, M = 1
+    "step_m1": synth.DecodeConfig("step_m1", hidden=256, inter=384, n_q_heads=4, n_kv_heads=2,
+                                  head_dim=128, n_layers=2, vocab=1024, fp8=False,
+                                  num_requests=1, tokens_per_request=1, context=70,
+                                  page_size=16, seed=15),
+}
+
+MODES = [dl.MODE_SERIAL, dl.MODE_PDL_GRAPH, dl.MODE_MEGAKERNEL, dl.MODE_GRAPH_LINEAR,
+         dl.MODE_GRAPH_LINEAR_PDL, dl.MODE_GRAPH_DAG]
+
+_cases = {}
+
+
+def case(name):
+    if name not in _cases:
+        cfg = SMALL[name] if name in SMALL else synth.CONFIGS[name]
+        _cases[name] = Case(cfg)
+    return _cases[name]
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: dl.MODE_NAMES[m])
+def test_small_layer_all_modes(name, mode):
+    c = case(name)
+    plan = c.plan()
+    out, kv = c.run(plan, mode)
+    if c.cfg.vocab:
+        ids = out.cpu().numpy()
+        logits = c.ref["logits"]
+        top2 = np.sort(logits, axis=1)[:, -2:]
+        sure = (top2[:, 1] - top2[:, 0]) > 1e-2
+        assert np.array_equal(ids[sure], c.ref["ids"][sure]), (ids, c.ref["ids"])
+    else:
+        c.check_layer_out(out, f"{name}/{dl.MODE_NAMES[mode]}")
+    c.check_kv(kv, f"{name}/{dl.MODE_NAMES[mode]}")
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["bf16_m1", "bf16_m4", "bf16_m16", "fp8_m16"])
+def test_small_intermediates(name):
+    """Every row of the step against the oracle's intermediates."""
+    c = case(name)
+    cfg = c.cfg
+    plan = c.plan(modes=1 << dl.MODE_SERIAL)
+    c.run(plan, dl.MODE_SERIAL)
+    M, H, I = cfg.M, cfg.hidden, cfg.inter
+    QD = cfg.n_q_heads * cfg.head_dim
+    bf16_close(as_bf16_np(read_debug(plan, "r1"), (M, H)), c.ref["r1"], "r1")
+    bf16_close(as_bf16_np(read_debug(plan, "q_rot"), (M, QD)), c.ref["q_rot"], "q_rot")
+    bf16_close(as_bf16_np(read_debug(plan, "r2"), (M, H)), c.ref["r2"], "r2")
+    if cfg.fp8:
+        for nm, K in (("h1", H), ("attn", QD), ("h2", H), ("act", I)):
+            codes = as_u8_np(read_debug(plan, nm), (M, K))
+            sc = as_f32_np(read_debug(plan, nm + "_scales"), (M, K // 128))
+            got = dequant(codes, sc)
+            want = dequant(c.ref[nm + "_codes"], c.ref[nm + "_scales"])
+            rel_rms_close(got, want, nm)
+        rel_rms_close(f64(as_bf16_np(read_debug(plan, "o2"), (M, H))), f64(c.ref["o2"]), "o2")
+    else:
+        bf16_close(as_bf16_np(read_debug(plan, "h1"), (M, H)), c.ref["h1"], "h1")
+        bf16_close(as_bf16_np(read_debug(plan, "attn"), (M, QD)), c.ref["attn"], "attn")
+        bf16_close(as_bf16_np(read_debug(plan, "o2"), (M, H)), c.ref["o2"], "o2")
+        bf16_close(as_bf16_np(read_debug(plan, "h2"), (M, H)), c.ref["h2"], "h2")
+        bf16_close(as_bf16_np(read_debug(plan, "act"), (M, I)), c.ref["act"], "act")
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["bf16_m1", "fp8_m16", "step_m1"])
+def test_schedules_bitwise_identical(name):
+    """Serial, graph (linear, +PDL) and megakernel run the same tile engines
+    over the same work split, so their results are bit-identical; replaying
+    a step with the same inputs reproduces it exactly."""
+    c = case(name)
+    plan = c.plan()
+    outs = {}
+    for mode in (dl.MODE_SERIAL, dl.MODE_GRAPH_LINEAR, dl.MODE_GRAPH_LINEAR_PDL,
+                 dl.MODE_MEGAKERNEL):
+        out, kv = c.run(plan, mode, steps=3)
+        outs[mode] = (out.cpu(), kv.cpu())
+    base = outs[dl.MODE_SERIAL]
+    for mode, (o, k) in outs.items():
+        assert torch.equal(o, base[0]), dl.MODE_NAMES[mode]
+        assert torch.equal(k, base[1]), dl.MODE_NAMES[mode]
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["q06_layer_b1_ctx1024", "q8_layer_m16_ctx8192_fp8"])
+@pytest.mark.parametrize("mode", [dl.MODE_SERIAL, dl.MODE_PDL_GRAPH, dl.MODE_MEGAKERNEL],
+                         ids=lambda m: dl.MODE_NAMES[m])
+def test_full_size_layer(name, mode):
+    c = case(name)
+    plan = c.plan(modes=(1 << dl.MODE_SERIAL) | (1 << dl.MODE_PDL_GRAPH) | (1 << dl.MODE_MEGAKERNEL))
+    out, kv = c.run(plan, mode)
+    c.check_layer_out(out, f"{name}/{dl.MODE_NAMES[mode]}")
+    c.check_kv(kv, f"{name}/{dl.MODE_NAMES[mode]}")
+    plan.close()
