@@ -31,12 +31,14 @@ def test_kv_write_and_gather_bit_exact(P, ctx):
     dev = torch.device("cuda")
     kv = cache.to(dev)
     layer = 1
-    rc = dl.lib().dl_test_kv_write(src.to(dev).data_ptr(), kv.data_ptr(), perm.to(dev).data_ptr(),
-                                   pos.to(dev).data_ptr(), layer, R * T, T, Hkv, d, P, NP, ppr,
+    # keep every device tensor referenced while the asynchronous calls use it
+    src_d, bt_d, pos_d = src.to(dev), perm.to(dev), pos.to(dev)
+    rc = dl.lib().dl_test_kv_write(src_d.data_ptr(), kv.data_ptr(), bt_d.data_ptr(),
+                                   pos_d.data_ptr(), layer, R * T, T, Hkv, d, P, NP, ppr,
                                    _stream())
     assert rc == 0
     dst = torch.empty((R, 2, Hkv, ctx, d), dtype=torch.int16, device=dev)
-    rc = dl.lib().dl_test_kv_gather(kv.data_ptr(), perm.to(dev).data_ptr(), dst.data_ptr(), layer,
+    rc = dl.lib().dl_test_kv_gather(kv.data_ptr(), bt_d.data_ptr(), dst.data_ptr(), layer,
                                     R, ctx, Hkv, d, P, NP, ppr, _stream())
     assert rc == 0
     torch.cuda.synchronize()
