@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode step on GB300.
+
+Workload (default): the Qwen3-8B-shaped decode layer at M = 16 (2 requests x
+8 tokens), context 8192, FP8 e4m3 weights with 128x128 block scales,
+activations quantised per token per 128, bf16 paged KV cache in 64-token
+pages.  Weights, caches and inputs are seeded synthetic tensors.
+
+Per schedule (serial / graph + multistream + PDL / megakernel) it times
+--steps decode steps with CUDA events on the launching stream after
+--warmup untimed steps, flushing L2 (a 256 MiB write) between timed steps
+outside the events.  The headline value is the achieved HBM bandwidth of the
+best schedule: algorithmic bytes (weights + scales, each request's K/V once,
+new K/V, activations) / device time per step.  One JSON line on rank 0.
+
+--impl reference times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step).  Under torchrun each rank runs an
+independent replica (the decode path has no exchange step) and the reported
+value is all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode-layer µs & achieved HBM GB/s vs 8 TB/s "
+          "(Qwen3-8B shape, M=16, KV=8192)")
+HBM_NOMINAL_GBS = 8000.0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smmax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smmax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smmax) if smmax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_workload(name: str, device, cpu_weights: bool):
+    from pdl_persistent_megakernel_gb300 import synth
+    cfg = synth.CONFIGS[name]
+    gen_dev = "cpu" if cpu_weights else device
+    w = synth.make_weights(cfg, device=gen_dev)
+    inp = synth.make_inputs(cfg, device="cpu")
+    return cfg, w, inp
+
+
+def to_dev(w, device):
+    return {"layers": [{k: (v.to(device) if v is not None else None) for k, v in lw.items()}
+                       for lw in w["layers"]],
+            "final_norm_w": None if w.get("final_norm_w") is None else w["final_norm_w"].to(device),
+            "lm_head_w": None if w.get("lm_head_w") is None else w["lm_head_w"].to(device)}
+
+
+def time_cpu_oracle(cfg, w, inp, min_seconds: float, max_reps: int):
+    """The oracle as it stands on the host cores; returns (s/step, reps, threads)."""
+    import oracle
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode_step(cfg, w, inp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or n >= max_reps:
+            break
+    return el / n, n, oracle.num_threads()
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the CPU oracle, timed on this host's cores."""
+    if rank != 0:
+        return
+    from pdl_persistent_megakernel_gb300 import bytes_model
+    cfg, w, inp = build_workload(args.config, "cpu", True)
+    byts = bytes_model.algorithmic_bytes(cfg)["total"]
+    for _ in range(min(args.warmup, 1)):
+        time_cpu_oracle(cfg, w, inp, 0.0, 1)
+    per = []
+    threads = 1
+    for _ in range(args.steps):
+        s, n, threads = time_cpu_oracle(cfg, w, inp, 0.0, 1)
+        per.append(s)
+    sec = sum(per) / len(per)
+    val = byts / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": cfg.n_layers, "M": cfg.M,
+                   "context": cfg.context, "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"one full {cfg.name} step per timed step"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="q8_layer_m16_ctx8192_fp8")
+    ap.add_argument("--modes", default="serial,pdl_graph,megakernel")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--per-kernel", action="store_true", default=True)
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import pdl_persistent_megakernel_gb300 as dl
+    from pdl_persistent_megakernel_gb300 import bytes_model
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("gloo")
+
+    need_cpu = (rank == 0 and ws == 1 and not args.no_cpu)
+    cfg, w, inp = build_workload(args.config, device, cpu_weights=True)
+    wd = to_dev(w, device)
+    modes = [m for m in args.modes.split(",") if m]
+    name_to_mode = {v: k for k, v in dl.MODE_NAMES.items()}
+    mask = (1 << dl.MODE_SERIAL)
+    for m in modes:
+        mask |= 1 << name_to_mode[m]
+    plan = dl.Plan(cfg, wd, modes_mask=mask)
+    stream = torch.cuda.Stream(device)
+    x, res = inp["x"].to(device), inp["residual"].to(device)
+    kv = inp["kv_pages"].to(device)
+    bt, pos = inp["block_table"].to(device), inp["positions"].to(device)
+    out = (torch.empty((cfg.M,), dtype=torch.int32, device=device) if cfg.vocab
+           else torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    algo = bytes_model.algorithmic_bytes(cfg)["total"]
+    peak, peak_kind = measured_peaks()
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if ws > 1:
+            dist.barrier()
+
+    def timed_steps(mode, k, w_):
+        with torch.cuda.stream(stream):
+            for _ in range(w_):
+                flush.zero_()
+                plan.step(x, res, kv, bt, pos, out, mode, stream)
+            barrier()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(k)]
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                plan.step(x, res, kv, bt, pos, out, mode, stream)
+                b.record(stream)
+            barrier()
+        plan.status()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    results = {}
+    launches = {}
+    with Clocks(local) as clk:
+        for m in modes:
+            mode = name_to_mode[m]
+            ms = timed_steps(mode, args.steps, args.warmup)
+            mean_ms = sum(ms) / len(ms)
+            if ws > 1:
+                t = torch.tensor([mean_ms], dtype=torch.float64)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                mean_ms = float(t.item())
+            results[m] = {"us": mean_ms * 1e3, "us_median": statistics.median(ms) * 1e3,
+                          "us_p10": sorted(ms)[max(0, len(ms) // 10)] * 1e3,
+                          "GBs": ws * algo / (mean_ms * 1e-3) / 1e9}
+            results[m]["frac_of_8TBs"] = results[m]["GBs"] / HBM_NOMINAL_GBS
+            launches[m] = plan.kernel_count(mode) * args.steps
+    clocks = clk.summary()
+    best = min(results, key=lambda m: results[m]["us"])
+
+    # per-kernel durations of the serial schedule (events around each launch,
+    # L2 flushed before each)
+    per_kernel = {}
+    ops = plan.ops()
+    with torch.cuda.stream(stream):
+        for i, (nm, grid, smem) in enumerate(ops):
+            evs = []
+            for _ in range(max(3, args.steps)):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                plan.launch_op(i, stream)
+                b.record(stream)
+                evs.append((a, b))
+            torch.cuda.synchronize(device)
+            t_us = sum(a.elapsed_time(b) for a, b in evs) / len(evs) * 1e3
+            key = nm if nm not in per_kernel else f"{nm}#{i}"
+            try:
+                ob = bytes_model.op_bytes(cfg, nm)
+            except KeyError:
+                ob = None
+            per_kernel[key] = {"us": t_us, "grid": grid, "smem": smem,
+                               "bytes": ob, "GBs": (ob / (t_us * 1e-6) / 1e9) if ob else None}
+    plan.status()
+    dom = max((k for k in per_kernel if per_kernel[k]["bytes"]),
+              key=lambda k: per_kernel[k]["bytes"])
+    dk = per_kernel[dom]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("workload") == cfg.name and tj.get("kernel") == dom:
+                traffic = tj.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["GBs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["GBs"] / peak, "traffic": traffic,
+                "peak_kind": peak_kind, "algorithmic_bytes": dk["bytes"], "us": dk["us"]}
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    xh, rh = inp["x"].pin_memory(), inp["residual"].pin_memory()
+    bth, posh = inp["block_table"].pin_memory(), inp["positions"].pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    emode = name_to_mode[best]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            plan.step_host(xh, rh, kv, bth, posh, outh, emode, stream)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        evs = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            plan.step_host(xh, rh, kv, bth, posh, outh, emode, stream)
+            b.record(stream)
+            evs.append((a, b))
+        barrier()
+    plan.status()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * 2 + rh.numel() * 2 + bth.numel() * 4 + posh.numel() * 4
+    d2h = outh.numel() * outh.element_size()
+    e2e = {"value": ws * algo / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "us": e2e_ms * 1e3,
+           "schedule": best}
+
+    cpu = None
+    if need_cpu:
+        sec, reps, threads = time_cpu_oracle(cfg, w, inp, args.cpu_seconds, 50)
+        cpu = {"value": algo / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{reps} full {cfg.name} step(s) of the fp64 C oracle, "
+                         f"{sec * 1e3:.0f} ms each"}
+
+    if rank == 0:
+        r = results[best]
+        sched = {m: {k: (round(v, 3) if isinstance(v, float) else v) for k, v in d.items()}
+                 for m, d in results.items()}
+        line = {
+            "metric": METRIC, "value": r["GBs"], "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["us"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3" if cfg.fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "schedule": best, "layers": cfg.n_layers,
+                       "M": cfg.M, "requests": cfg.num_requests,
+                       "tokens_per_request": cfg.tokens_per_request, "context": cfg.context,
+                       "page_size": cfg.page_size,
+                       "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16",
+                       "algorithmic_bytes": algo, "l2": "256 MiB write between timed steps",
+                       "replicas": ws},
+            "us_per_layer": r["us"] / cfg.n_layers,
+            "frac_of_8TBs": r["frac_of_8TBs"],
+            "frac_of_measured_hbm": r["GBs"] / ws / peak,
+            "schedules": sched,
+            "serial_pdl_mega_us": [round(results[m]["us"], 2) if m in results else None
+                                   for m in ("serial", "pdl_graph", "megakernel")],
+            "roofline": roofline,
+            "per_kernel_us": {k: round(v["us"], 2) for k, v in per_kernel.items()},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches[best],
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

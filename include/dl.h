@@ -168,6 +168,15 @@ dl_status dl_plan_debug_buffer(dl_plan* plan, int which, void** ptr,
 /* Number of kernels one step of `mode` launches (for accounting). */
 int dl_plan_kernel_count(dl_plan* plan, int mode);
 
+/* The serial schedule's operations: how many, the name of op i, and a
+ * launch of op i alone on `stream` (for per-kernel timing; operands are
+ * those bound by the last dl_decode_step on this plan).  dl_plan_op_info
+ * also reports the op's grid (CTAs) and dynamic shared memory bytes. */
+int dl_plan_op_count(dl_plan* plan);
+dl_status dl_plan_op_info(dl_plan* plan, int i, char* name, size_t name_len,
+                          int* grid, int* smem_bytes);
+dl_status dl_plan_launch_op(dl_plan* plan, int i, void* stream);
+
 /* Megakernel queue statistics: workers, queue length, events. */
 dl_status dl_plan_mega_info(dl_plan* plan, int* workers, int* qlen,
                             int* events);

@@ -117,7 +117,8 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_decode_step_host", "dl_plan_status", "dl_plan_logits",
            "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
-           "dl_test_kv_gather")
+           "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
+           "dl_plan_launch_op")
 
 
 def lib(path: Optional[str] = None):
@@ -149,6 +150,13 @@ def lib(path: Optional[str] = None):
         L.dl_plan_debug_perturb_wait.argtypes = [vp, u32, C.c_ulonglong, i32]
         L.dl_plan_debug_perturb_wait.restype = i32
         L.dl_plan_destroy.argtypes = [vp]
+        L.dl_plan_op_count.argtypes = [vp]
+        L.dl_plan_op_count.restype = i32
+        L.dl_plan_op_info.argtypes = [vp, i32, C.c_char_p, C.c_size_t, C.POINTER(i32),
+                                      C.POINTER(i32)]
+        L.dl_plan_op_info.restype = i32
+        L.dl_plan_launch_op.argtypes = [vp, i32, vp]
+        L.dl_plan_launch_op.restype = i32
         L.dl_test_kv_write.argtypes = [vp] * 4 + [i32] * 8 + [vp]
         L.dl_test_kv_write.restype = i32
         L.dl_test_kv_gather.argtypes = [vp] * 3 + [i32] * 8 + [vp]
@@ -248,6 +256,20 @@ class Plan:
         w, q, e = C.c_int(), C.c_int(), C.c_int()
         _check(lib().dl_plan_mega_info(self._h, C.byref(w), C.byref(q), C.byref(e)))
         return w.value, q.value, e.value
+
+    def ops(self):
+        """[(name, grid, smem_bytes)] of the serial schedule's operations."""
+        L = lib()
+        res = []
+        for i in range(L.dl_plan_op_count(self._h)):
+            buf = C.create_string_buffer(64)
+            g, s = C.c_int(), C.c_int()
+            _check(L.dl_plan_op_info(self._h, i, buf, 64, C.byref(g), C.byref(s)))
+            res.append((buf.value.decode(), g.value, s.value))
+        return res
+
+    def launch_op(self, i: int, stream=None):
+        _check(lib().dl_plan_launch_op(self._h, i, _stream_handle(stream)))
 
     def perturb_wait(self, delta: int, budget_ns: int, validate: bool):
         return lib().dl_plan_debug_perturb_wait(self._h, delta, budget_ns, int(validate))

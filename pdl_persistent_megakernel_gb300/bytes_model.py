@@ -87,3 +87,36 @@ def gap_model(kernels: Sequence[Tuple[str, int]], bandwidth: float,
         "under_1us": sum(1 for _, b in kernels if b / bandwidth * 1e6 < 1.0),
         "mean_us": t_data / n,
     }
+
+
+def op_bytes(cfg: DecodeConfig, name: str) -> float:
+    """Algorithmic bytes of one launch of a serial-schedule operation (inputs
+    read once, outputs written once, weights once)."""
+    H, I, d = cfg.hidden, cfg.inter, cfg.head_dim
+    M, R = cfg.M, cfg.num_requests
+    qd, kvd = cfg.n_q_heads * d, cfg.n_kv_heads * d
+    eb = 1 if cfg.fp8 else 2
+
+    def act(K):  # a quantised (or bf16) activation [M, K]
+        return M * K * eb + (M * (K // 128) * 4 if cfg.fp8 else 0)
+
+    def wts(N, K):
+        return N * K * eb + ((N // 128) * (K // 128) * 4 if cfg.fp8 else 0)
+
+    if name in ("add_rmsnorm1", "add_rmsnorm2"):
+        return 3 * M * H * 2 + act(H) + H * 2
+    if name == "final_norm":
+        return 3 * M * H * 2 + M * H * 2 + H * 2
+    if name == "qkv_rope_kvwrite":
+        return wts(cfg.qkv_rows, H) + act(H) + M * qd * 2 + M * 2 * kvd * 2 + 2 * d * 2
+    if name == "attention":
+        return R * cfg.context * kvd * 2 * 2 + M * qd * 2 + act(qd)
+    if name == "o_proj":
+        return wts(H, qd) + act(qd) + M * H * 2
+    if name == "gate_up_silu":
+        return wts(2 * I, H) + act(H) + act(I)
+    if name == "down_proj":
+        return wts(H, I) + act(I) + M * H * 2
+    if name == "lm_head_argmax":
+        return cfg.vocab * H * 2 + M * H * 2 + M * cfg.vocab * 4 + M * 4
+    raise KeyError(name)

@@ -109,6 +109,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Every lane of a warp waits (bounded) for the phase; the warp agrees on the
+// outcome, so a timeout never splits a warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          const KernelCtx& ctx, unsigned where) {
+  const bool ok = mbar_wait(bar, parity, ctx, where);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %3, 0;\n\t"
+      "bar.red.or.pred p, %1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
 // Drain: wait (bounded, ignoring the abort flag) for a phase to complete.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity,
                                            unsigned long long budget_ns) {
@@ -135,6 +157,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+
+// A descriptor that an earlier kernel wrote with ordinary stores: order
+// those stores before this thread's tensor-map (TMA) reads of it.
+__device__ __forceinline__ void fence_tmap_acquire(const CUtensorMap* m) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m)
+               : "memory");
 }
 
 // 2-D tiled load: box at element coordinates (c0 inner, c1 outer).  c0 * the

@@ -191,6 +191,7 @@ static KernelCtx make_ctx(const dl_plan* p, int op_id) {
 }
 
 // ------------------------------------------------------------ op builders
+constexpr int kGemmSmemTarget = 210 * 1024;
 static int choose_stages(int stage_bytes, int fixed_bytes, int target) {
   int s = (target - fixed_bytes) / stage_bytes;
   return std::max(2, std::min(kMaxStages, s));
@@ -259,15 +260,17 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   a.G = static_cast<int>(std::min<long long>(p->sms, U));
   const int npair = s.pair ? 2 : 1;
   const int stage_bytes = npair * 16384 + ((a.Mp * 128 + 1023) / 1024) * 1024;
-  const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0);
-  a.stages = choose_stages(stage_bytes, fixed_bytes, 112 * 1024);
+  const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0, a.KB, a.fp8, s.epi, a.M);
+  // one CTA per SM: a deep ring keeps ~200 KB of weights in flight per SM
+  a.stages = choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget);
+  a.tmem_bufs = a.mma ? std::min(4, 512 / (npair * a.Mp)) : 1;
   a.epi = s.epi;
   a.ws = p->ws_gemm[s.ws_slot];
   a.tile_cnt = cnt;
   a.done_cnt = cnt + a.NT;
   op.kernel = gemm_kernel(a.mma, a.mma ? a.Mp : a.M);
   op.grid = a.G;
-  op.smem = gemm_smem_bytes(npair, a.Mp, a.stages);
+  op.smem = gemm_smem_bytes(npair, a.Mp, a.stages, a.KB, a.fp8, s.epi, a.M);
   op.name = s.name;
   return op;
 }
@@ -297,12 +300,16 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.QRp = a.QR <= 16 ? 16 : (a.QR <= 32 ? 32 : 64);
   a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
   const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  a.G = static_cast<int>(std::min<long long>(p->sms, U));
-  a.stages = 3;
+  // at most ~62 CTAs may share one (request, kv head) stream: the combine's
+  // weight table holds 64 contributors
+  a.G = static_cast<int>(std::min<long long>(std::min<long long>(p->sms, U),
+                                             62LL * a.R * a.Hkv));
+  a.stages = std::max(2, std::min(kMaxStages, (kGemmSmemTarget - attn_smem_bytes(a.QRp, 0)) /
+                                                    (4 * kAttnKeys * 128)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d)));
   a.ws = p->ws_attn;
   a.pair_cnt = cnt;
-  op.kernel = attn_kernel();
+  op.kernel = attn_kernel(a.QRp);
   op.grid = a.G;
   op.smem = attn_smem_bytes(a.QRp, a.stages);
   op.name = "attention";
@@ -561,7 +568,7 @@ static dl_status build_plan(dl_plan* p) {
   p->M = p->R * p->T;
   p->fp8 = c.weight_dtype == DL_WEIGHT_FP8_E4M3_B128;
   p->full = c.vocab > 0;
-  p->mma = p->M > 8;
+  p->mma = p->M > 4;   // CUDA-core GEMV up to 4 tokens, tcgen05 beyond
   p->Mp = p->mma ? (p->M <= 16 ? 16 : (p->M <= 32 ? 32 : 64)) : p->M;
   p->Mrows = p->Mp;
   if (!load_encode()) return fail(DL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -769,13 +776,24 @@ static dl_status build_plan(dl_plan* p) {
   }
   if (cpos > p->n_counters) return fail(DL_ERR_CUDA, "counter pool overflow");
 
-  // kernel attributes: dynamic shared memory
+  // kernel attributes: dynamic shared memory (the largest user of each kernel)
   int max_smem = 0;
-  for (const auto* list : {&p->lin, &p->dag})
-    for (const LaunchOp& op : *list) {
-      CK(cudaFuncSetAttribute(op.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, op.smem));
-      max_smem = std::max(max_smem, op.smem);
-    }
+  {
+    std::vector<std::pair<const void*, int>> need;
+    for (const auto* list : {&p->lin, &p->dag})
+      for (const LaunchOp& op : *list) {
+        bool found = false;
+        for (auto& kv : need)
+          if (kv.first == op.kernel) {
+            kv.second = std::max(kv.second, op.smem);
+            found = true;
+          }
+        if (!found) need.emplace_back(op.kernel, op.smem);
+        max_smem = std::max(max_smem, op.smem);
+      }
+    for (auto& kv : need)
+      CK(cudaFuncSetAttribute(kv.first, cudaFuncAttributeMaxDynamicSharedMemorySize, kv.second));
+  }
 
   // streams / events for capture and the DAG fork
   CK(cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking));
@@ -843,8 +861,19 @@ extern "C" void dl_plan_destroy(dl_plan* p) {
 }
 
 // ------------------------------------------------------------------ steps
-static dl_status bind(dl_plan* p, const Binding& b, cudaStream_t s) {
-  if (p->have_last && std::memcmp(&b, &p->last, sizeof(Binding)) == 0) return DL_OK;
+static dl_status bind(dl_plan* p, Binding& b, cudaStream_t s) {
+  if (p->have_last && std::memcmp(b.p, p->last.p, sizeof(b.p)) == 0) return DL_OK;
+  // TMA descriptor of the bound cache, [rows, head_dim] bf16
+  const uint64_t rows = static_cast<uint64_t>(p->L) * p->cfg.num_pages * 2 * p->Hkv * p->P;
+  const uint32_t box = static_cast<uint32_t>(std::min(p->P, kAttnKeys));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->d), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->d) * 2};
+  cuuint32_t boxd[2] = {64, box};
+  cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&b.kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b.p[SLOT_KV], dims, strides, boxd,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return fail(DL_ERR_INVALID_ARG, "kv_pages cannot be described by a TMA descriptor");
   CK(launch_bind(p->d_binding, b, s));
   p->last = b;
   p->have_last = true;
@@ -864,7 +893,8 @@ extern "C" dl_status dl_decode_step(dl_plan* p, const void* x, const void* resid
   if (mode != DL_MODE_SERIAL && !(p->cfg.modes_mask & (1u << mode)))
     return fail(DL_ERR_INVALID_ARG, "mode not prepared (modes_mask)");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Binding b{};
+  Binding b;
+  std::memset(&b, 0, sizeof(b));
   b.p[SLOT_X] = const_cast<void*>(x);
   b.p[SLOT_RES] = const_cast<void*>(residual);
   b.p[SLOT_KV] = kv_pages;
@@ -962,6 +992,30 @@ extern "C" int dl_plan_kernel_count(dl_plan* p, int mode) {
   if (mode == DL_MODE_MEGAKERNEL) return 1;
   if (mode == DL_MODE_PDL_GRAPH || mode == DL_MODE_GRAPH_DAG) return static_cast<int>(p->dag.size());
   return static_cast<int>(p->lin.size());
+}
+
+extern "C" int dl_plan_op_count(dl_plan* p) { return p ? static_cast<int>(p->lin.size()) : -1; }
+
+extern "C" dl_status dl_plan_op_info(dl_plan* p, int i, char* name, size_t name_len, int* grid,
+                                     int* smem_bytes) {
+  if (!p || i < 0 || i >= static_cast<int>(p->lin.size()))
+    return fail(DL_ERR_INVALID_ARG, "op index out of range");
+  const LaunchOp& op = p->lin[i];
+  if (name && name_len) {
+    std::strncpy(name, op.name.c_str(), name_len - 1);
+    name[name_len - 1] = 0;
+  }
+  if (grid) *grid = op.grid;
+  if (smem_bytes) *smem_bytes = op.smem;
+  return DL_OK;
+}
+
+extern "C" dl_status dl_plan_launch_op(dl_plan* p, int i, void* stream) {
+  if (!p || i < 0 || i >= static_cast<int>(p->lin.size()))
+    return fail(DL_ERR_INVALID_ARG, "op index out of range");
+  if (!p->have_last) return fail(DL_ERR_INVALID_ARG, "no operands bound yet");
+  CK(launch_op(p, p->lin[i], static_cast<cudaStream_t>(stream), false, i));
+  return DL_OK;
 }
 
 extern "C" dl_status dl_plan_mega_info(dl_plan* p, int* workers, int* qlen, int* events) {

@@ -24,7 +24,7 @@ constexpr int kBKBytes = 128;        // bytes of K per pipeline stage (one
 constexpr int kMaxM = 64;            // tokens per step
 constexpr int kAttnKeys = 64;        // keys per attention pipeline stage
 constexpr int kMaxQRows = 64;        // query rows per (request, kv head)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 
 // ----------------------------------------------------- runtime bindings
 // Pointers supplied per decode call (the caller's tensors).  Kernels read
@@ -40,8 +40,12 @@ enum BindingSlot : int {
   NUM_SLOTS = 8
 };
 
-struct Binding {
+struct alignas(64) Binding {
   void* p[NUM_SLOTS];
+  // TMA descriptor of the bound KV cache viewed as [rows, head_dim] bf16
+  // (rows = layers * pages * 2 * kv_heads * page_size), 128-byte swizzle,
+  // boxes of 64 head-dim elements by min(page_size, 64) rows.
+  CUtensorMap kv_map;
 };
 
 // A pointer operand: a fixed plan-owned address, or (slot >= 0) a binding
@@ -100,7 +104,7 @@ struct GemmArgs {
   const float* w_scale;       // FP8 block scales [N/128, K/128]
   const float* x_scale;       // FP8 activation scales [M, K/128]
   int fp8;
-  int mma;                    // 1: tcgen05 (M > 8), 0: CUDA-core GEMV
+  int mma;                    // 1: tcgen05 (M > 4), 0: CUDA-core GEMV
   int M, Mp;                  // tokens, rows of the activation tile
   int K;                      // elements
   int KB;                     // 128-byte k-blocks per tile
@@ -110,6 +114,7 @@ struct GemmArgs {
   int up_row;                 // first up row (= I) for gate/up
   int G;                      // CTAs sharing the units
   int stages;
+  int tmem_bufs;              // tcgen05 accumulator ring depth
   int epi;
   // partial sums (Stream-K fix-up) and counters
   float* ws;                  // [G][2][npair][Mp][128] fp32

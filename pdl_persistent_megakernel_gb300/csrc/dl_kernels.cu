@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(GemmArgs a, KernelCtx ctx)
   uint32_t tmem = 0;
   int cols = 0;
   if constexpr (kMp > 0) {
-    cols = tmem_cols_pow2(2 * (a.pair ? 2 : 1) * kMp);
+    cols = tmem_cols_pow2(a.tmem_bufs * (a.pair ? 2 : 1) * kMp);
     if ((threadIdx.x >> 5) == 1) {
       tmem_alloc(&tmem_slot, cols);
       tmem_relinquish();
@@ -56,11 +56,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(GemmArgs a, KernelCtx ctx)
   }
 }
 
+template <int kNMT>
 __global__ void __launch_bounds__(kThreads, 1) k_attn(AttnArgs a, KernelCtx ctx) {
   extern __shared__ uint8_t smem_raw[];
   Dep dep{};
   dep.mode = 0;
-  attn_op(a, blockIdx.x, dep, ctx, align1024(smem_raw));
+  attn_op_t<kNMT>(a, blockIdx.x, dep, ctx, align1024(smem_raw));
 }
 
 __global__ void k_bind(Binding* dst, Binding v) { *dst = v; }
@@ -111,10 +112,8 @@ __device__ void mega_gemm(const GemmArgs& a, int c, const Dep& dep,
       gemm_op_t<1, 0>(a, c, dep, ctx, smem, tmem);
     else if (a.M <= 2)
       gemm_op_t<2, 0>(a, c, dep, ctx, smem, tmem);
-    else if (a.M <= 4)
-      gemm_op_t<4, 0>(a, c, dep, ctx, smem, tmem);
     else
-      gemm_op_t<8, 0>(a, c, dep, ctx, smem, tmem);
+      gemm_op_t<4, 0>(a, c, dep, ctx, smem, tmem);
   } else {
     if (a.Mp <= 16)
       gemm_op_t<0, 16>(a, c, dep, ctx, smem, tmem);
@@ -139,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
   __shared__ int stop;
   uint8_t* smem = align1024(smem_raw);
   const int tid = threadIdx.x;
-  constexpr int kTmemCols = 256;
+  constexpr int kTmemCols = 512;   // one worker per SM owns all of TMEM
   if ((tid >> 5) == 1) {
     tmem_alloc(&tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -220,8 +219,7 @@ const void* gemm_kernel(int mma, int m_or_mp) {
   if (!mma) {
     if (m_or_mp <= 1) return reinterpret_cast<const void*>(&k_gemm<1, 0>);
     if (m_or_mp <= 2) return reinterpret_cast<const void*>(&k_gemm<2, 0>);
-    if (m_or_mp <= 4) return reinterpret_cast<const void*>(&k_gemm<4, 0>);
-    return reinterpret_cast<const void*>(&k_gemm<8, 0>);
+    return reinterpret_cast<const void*>(&k_gemm<4, 0>);
   }
   if (m_or_mp <= 16) return reinterpret_cast<const void*>(&k_gemm<0, 16>);
   if (m_or_mp <= 32) return reinterpret_cast<const void*>(&k_gemm<0, 32>);
@@ -229,7 +227,11 @@ const void* gemm_kernel(int mma, int m_or_mp) {
 }
 
 const void* norm_kernel() { return reinterpret_cast<const void*>(&k_norm); }
-const void* attn_kernel() { return reinterpret_cast<const void*>(&k_attn); }
+const void* attn_kernel(int QRp) {
+  if (QRp <= 16) return reinterpret_cast<const void*>(&k_attn<1>);
+  if (QRp <= 32) return reinterpret_cast<const void*>(&k_attn<2>);
+  return reinterpret_cast<const void*>(&k_attn<4>);
+}
 const void* mega_kernel() { return reinterpret_cast<const void*>(&k_mega); }
 
 cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s) {
@@ -237,8 +239,8 @@ cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int gemm_smem_bytes(int npair, int Mp, int stages) {
-  return gemm_smem_layout(npair, Mp, stages).total + 1024;
+int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M) {
+  return gemm_smem_layout(npair, Mp, stages, KB, fp8, epi, M).total + 1024;
 }
 
 int attn_smem_bytes(int QRp, int stages) {

@@ -9,10 +9,10 @@ namespace dl {
 
 const void* gemm_kernel(int mma, int m_or_mp);
 const void* norm_kernel();
-const void* attn_kernel();
+const void* attn_kernel(int QRp);
 const void* mega_kernel();
 cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s);
-int gemm_smem_bytes(int npair, int Mp, int stages);
+int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M);
 int attn_smem_bytes(int QRp, int stages);
 int norm_smem_bytes();
 cudaError_t launch_test_kv_write(const void* src, void* kv, const int* bt, const int* pos,

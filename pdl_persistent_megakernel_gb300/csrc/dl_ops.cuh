@@ -117,13 +117,19 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   const int ct = tid - 32, lane = tid & 31, wc = ct >> 5;
   float* red = reinterpret_cast<float*>(smem);     // [2][8]
   int* sflag = reinterpret_cast<int*>(smem + 128);
+  const int H = a.H, nvec = H >> 3;
+  // the norm weight does not depend on the previous op: load it first
+  const uint16_t* w = static_cast<const uint16_t*>(a.w);
+  uint4 wv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    wv[j] = (ct + j * 256 < nvec) ? __ldg(reinterpret_cast<const uint4*>(w + (ct + j * 256) * 8))
+                                  : make_uint4(0, 0, 0, 0);
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag)) return;
   const Binding* bd = ctx.binding;
   const uint16_t* x = resolve<const uint16_t>(a.x, bd);
   const uint16_t* res = resolve<const uint16_t>(a.res, bd);
   uint16_t* rout = resolve<uint16_t>(a.r_out, bd);
-  const uint16_t* w = static_cast<const uint16_t*>(a.w);
-  const int H = a.H, nvec = H >> 3;
   const int m0 = c * a.rows_per_cta;
   const int m1 = min(a.M, m0 + a.rows_per_cta);
   for (int m = m0; m < m1; ++m) {
@@ -165,8 +171,7 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
       const bool act = v < nvec;
       float h[8];
       if (act) {
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w + v * 8));
-        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           h[2 * e] = r[j][2 * e] * inv * bf16_lo(ws[e]);
@@ -211,143 +216,227 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
 }
 
 // =================================================================== GEMM
+constexpr int kMaxTmemBufs = 4;   // TMEM accumulator ring depth (tcgen05 path)
+
 struct GemmSmem {
-  int w_bytes, x_bytes, stage_bytes, tile_off, bar_off, misc_off, nb_off, total;
+  int w_bytes, x_bytes, stage_bytes, tile_off, sx_off, sw_off, epi_off, bar_off,
+      misc_off, total;
 };
 
-__host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp,
-                                                     int stages) {
+constexpr int kMaxContrib = 256;  // CTAs that may share one tile / KV pair
+
+// Shared-memory layout of one GEMM CTA: the operand ring, the finished tile,
+// the FP8 scales of the current tile run (staged once per run), the QKV
+// epilogue's per-token positions / cache rows / RoPE rows, barriers and a
+// small control area (flags, contributor list of a Stream-K fix-up).
+__host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stages,
+                                                     int KB, int fp8, int epi, int M) {
   GemmSmem L;
   L.w_bytes = 16384;
   L.x_bytes = ((Mp * 128 + 1023) / 1024) * 1024;
   L.stage_bytes = npair * L.w_bytes + L.x_bytes;
   L.tile_off = stages * L.stage_bytes;
-  L.bar_off = L.tile_off + npair * Mp * 128 * 4;
-  L.misc_off = L.bar_off + (2 * kMaxStages + 4) * 8;  // flags, reductions
-  L.nb_off = L.misc_off + 256;                         // rope exchange [4][128]
-  L.total = L.nb_off + 4 * 128 * 4;
+  L.sx_off = L.tile_off + npair * Mp * 128 * 4;
+  L.sw_off = L.sx_off + (fp8 ? KB * Mp * 4 : 0);
+  L.epi_off = ((L.sw_off + (fp8 ? 2 * KB * 4 : 0)) + 15) & ~15;
+  L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) : 0);
+  L.bar_off = (L.bar_off + 15) & ~15;
+  L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs) * 8;
+  L.total = L.misc_off + 256 + kMaxContrib * 4;
   return L;
 }
 
 struct GemmShared {
   uint8_t* stage0;
   float* tout;
+  float* sx;      // [run][M] activation scales of the current tile run
+  float* sw;      // [2][run] weight scales of the current tile run
+  int* tok_pos;   // [M] positions (QKV epilogue)
+  int* tok_row;   // [M] cache row of (layer, page, K, head 0, slot) (QKV epilogue)
+  float2* rope;   // [M][64] (cos, sin) at each token's position (QKV epilogue)
   uint64_t* full;
   uint64_t* empty;
   uint64_t* tfull;
   uint64_t* tempty;
   int* flag;      // [4]
-  float* red;     // [2][2][4] reductions
-  float* nb;      // [2][128] rope exchange (aliases misc space below)
-  int* bidx;      // [2][4]
+  int* ctb;       // [kMaxContrib] contributor list of a fix-up
 };
+
+// Sum of `nc` fp32 partials (float4 granular, nel4 float4s each) listed in
+// ctb as workspace slot indices, in list order, into dst; up to 8 loads per
+// thread in flight.
+__device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_t part,
+                                             const int* ctb, int nc, int nel4, int nthr,
+                                             int ct) {
+  for (int e4 = ct; e4 < nel4; e4 += nthr) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < nc; j0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = (j0 + j < nc)
+                   ? __ldcg(reinterpret_cast<const float4*>(ws + static_cast<size_t>(ctb[j0 + j]) * part) + e4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < nc) {
+          acc.x += v[j].x;
+          acc.y += v[j].y;
+          acc.z += v[j].z;
+          acc.w += v[j].w;
+        }
+      }
+    }
+    dst[e4] = acc;
+  }
+}
+
+// Stream-K bookkeeping shared by the GEMM fix-up and the attention combine:
+// write the list of CTAs whose ranges intersect units [ts, ts + len) (in
+// CTA order, as workspace slot indices c * 2 + slot) and return its size.
+__device__ __forceinline__ int sk_contributors(long long U, int G, long long ts, int len,
+                                               int* ctb) {
+  const int cf = sk_owner(U, G, ts), cl = sk_owner(U, G, ts + len - 1);
+  int n = 0;
+  for (int cc = cf; cc <= cl && n < kMaxContrib; ++cc) {
+    const long long b0 = sk_begin(U, G, cc);
+    if (sk_begin(U, G, cc + 1) <= b0) continue;
+    ctb[n++] = cc * 2 + ((b0 >= ts) ? 0 : 1);
+  }
+  return n;
+}
 
 // ------------------------------------------------------- GEMM epilogues
 // tout = the finished tile: [npair][Mp][128] fp32 (rows of the weight tile on
-// the fast axis).  nthr threads (128 or 256) with group barrier `bar`;
-// tokens are processed by groups of 128 threads.
+// the fast axis).  nthr threads (128 or 256) with group barrier `bar`; the
+// per-token epilogues run one warp per token, lane l holding elements
+// l, l + 32, l + 64, l + 96.
 
 __device__ void epi_store_bf16(const GemmArgs& a, int tg, const float* tout,
                                int nthr, int ct, const Binding* bd) {
   uint16_t* out = resolve<uint16_t>(a.out, bd);
-  for (int e = ct; e < a.M * 128; e += nthr) {
-    const int m = e >> 7, i = e & 127;
-    out[static_cast<size_t>(m) * a.ldo + tg * 128 + i] = f2bf(tout[m * 128 + i]);
+  for (int e = ct; e < a.M * 32; e += nthr) {
+    const int m = e >> 5, i = (e & 31) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(tout + m * 128 + i);
+    const uint32_t lo = static_cast<uint32_t>(f2bf(v.x)) | (static_cast<uint32_t>(f2bf(v.y)) << 16);
+    const uint32_t hi = static_cast<uint32_t>(f2bf(v.z)) | (static_cast<uint32_t>(f2bf(v.w)) << 16);
+    *reinterpret_cast<uint2*>(out + static_cast<size_t>(m) * a.ldo + tg * 128 + i) = make_uint2(lo, hi);
   }
 }
 
-__device__ void epi_qkv_rope(const GemmArgs& a, int tg, const float* tout,
-                             int nthr, int ct, int bar, const KernelCtx& ctx,
-                             const GemmShared& sh) {
-  const int ng = nthr >> 7, g = ct >> 7, i = ct & 127, wg = (ct >> 5) & 3;
-  const int lane = ct & 31;
+// Per-token operands of the QKV epilogue, loaded once per CTA: positions,
+// the cache row of each token's slot, and the (cos, sin) rows at each
+// position.  Out-of-range positions or pages are reported and skipped.
+__device__ void qkv_epi_prepare(const GemmArgs& a, int nthr, int ct, int bar,
+                                const KernelCtx& ctx, const GemmShared& sh) {
   const Binding* bd = ctx.binding;
   const int* pos = resolve<const int>(a.pos, bd);
   const int* bt = resolve<const int>(a.bt, bd);
-  uint16_t* kv = resolve<uint16_t>(a.kv, bd);
+  for (int m = ct; m < a.M; m += nthr) {
+    int p = pos[m];
+    int row = -1;
+    if (p < 0 || p >= a.rope_max_pos) {
+      report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 20, p);
+      p = 0;
+    } else {
+      const int lp = p / a.P;
+      const int page = lp < a.max_pages ? bt[static_cast<size_t>(m / a.T) * a.max_pages + lp] : -1;
+      if (page < 0 || page >= a.num_pages)
+        report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 21, lp);
+      else
+        row = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, 0, p % a.P));
+    }
+    sh.tok_pos[m] = p;
+    sh.tok_row[m] = row;
+  }
+  named_bar(bar, nthr);
+  const float2* cs = reinterpret_cast<const float2*>(a.rope_cs);
+  for (int e = ct; e < a.M * 64; e += nthr)
+    sh.rope[e] = cs[static_cast<size_t>(sh.tok_pos[e >> 6]) * 64 + (e & 63)];
+  named_bar(bar, nthr);
+}
+
+// QK-norm + RoPE (neox pairs i, i + 64) for q and k heads; q heads go to the
+// q buffer, k and v heads to their slot in the paged cache.
+__device__ void epi_qkv_rope(const GemmArgs& a, int tg, const float* tout,
+                             int nthr, int ct, const KernelCtx& ctx,
+                             const GemmShared& sh) {
+  const int lane = ct & 31, wi = ct >> 5, nw = nthr >> 5;
+  uint16_t* kv = resolve<uint16_t>(a.kv, ctx.binding);
   const int hh = tg;
   const bool is_q = hh < a.Hq;
   const bool is_k = !is_q && hh < a.Hq + a.Hkv;
-  float wn = 1.f;
+  float wn[4] = {1.f, 1.f, 1.f, 1.f};
   if (is_q || is_k) {
-    const uint16_t* nw = static_cast<const uint16_t*>(is_q ? a.q_norm_w : a.k_norm_w);
-    wn = __uint_as_float(static_cast<uint32_t>(nw[i]) << 16);
+    const uint16_t* nw_ = static_cast<const uint16_t*>(is_q ? a.q_norm_w : a.k_norm_w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wn[k] = __uint_as_float(static_cast<uint32_t>(nw_[lane + 32 * k]) << 16);
   }
-  for (int mb = 0; mb < a.M; mb += ng) {
-    const int m = mb + g;
-    const bool act = m < a.M;
-    const float v = act ? bfround(tout[m * 128 + i]) : 0.f;
-    float outv = v;
-    int p = 0;
-    if (act) {
-      p = pos[m];
-      if (p < 0 || p >= a.rope_max_pos) {
-        report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 20, p);
-        p = 0;
-      }
-    }
+  for (int m = wi; m < a.M; m += nw) {
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = bfround(tout[m * 128 + lane + 32 * k]);
+    float o[4];
     if (is_q || is_k) {
-      const float ss = warp_sum(v * v);
-      if (lane == 0) sh.red[((mb / ng) & 1) * 8 + g * 4 + wg] = ss;
-      named_bar(bar, nthr);
-      const float* rr = sh.red + ((mb / ng) & 1) * 8 + g * 4;
-      const float tot = rr[0] + rr[1] + rr[2] + rr[3];
-      const float xn = bfround(v * rsqrtf(tot * (1.f / 128.f) + a.eps) * wn);
-      sh.nb[(((mb / ng) & 1) * 2 + g) * 128 + i] = xn;
-      named_bar(bar, nthr);
-      const float partner = sh.nb[(((mb / ng) & 1) * 2 + g) * 128 + (i ^ 64)];
-      const float2 cs = *reinterpret_cast<const float2*>(
-          a.rope_cs + (static_cast<size_t>(p) * 64 + (i & 63)) * 2);
-      outv = i < 64 ? xn * cs.x - partner * cs.y : xn * cs.x + partner * cs.y;
-    }
-    if (!act) continue;
-    const uint16_t ob = f2bf(outv);
-    if (is_q) {
-      static_cast<uint16_t*>(a.q_out)[(static_cast<size_t>(m) * a.Hq + hh) * 128 + i] = ob;
+      const float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+      const float inv = rsqrtf(ss * (1.f / 128.f) + a.eps);
+      float xn[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) xn[k] = bfround(v[k] * inv * wn[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 cs = sh.rope[m * 64 + lane + 32 * (k & 1)];
+        const float partner = xn[k ^ 2];
+        o[k] = k < 2 ? xn[k] * cs.x - partner * cs.y : xn[k] * cs.x + partner * cs.y;
+      }
     } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = v[k];
+    }
+    if (is_q) {
+      uint16_t* dst = static_cast<uint16_t*>(a.q_out) + (static_cast<size_t>(m) * a.Hq + hh) * 128;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[lane + 32 * k] = f2bf(o[k]);
+    } else {
+      const int row = sh.tok_row[m];
+      if (row < 0) continue;
       const int kvsel = is_k ? 0 : 1;
       const int kh = is_k ? hh - a.Hq : hh - a.Hq - a.Hkv;
-      const int r = m / a.T;
-      const int lp = p / a.P;
-      const int page = lp < a.max_pages ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
-      if (page < 0 || page >= a.num_pages) {
-        report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 21, lp);
-        continue;
-      }
-      const size_t off =
-          kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, kvsel, kh, p % a.P) * 128 + i;
-      kv[off] = ob;
+      // row addresses (layer, page, K, head 0, slot): V is Hkv * P rows on,
+      // head kh is kh * P rows on
+      const size_t r = static_cast<size_t>(row) +
+                       (static_cast<size_t>(kvsel) * a.Hkv + kh) * a.P;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) kv[r * 128 + lane + 32 * k] = f2bf(o[k]);
     }
   }
 }
 
 __device__ void epi_silu_mul(const GemmArgs& a, int tg, const float* tout,
-                             int nthr, int ct, int bar, const GemmShared& sh) {
-  const int ng = nthr >> 7, g = ct >> 7, i = ct & 127, wg = (ct >> 5) & 3;
-  const int lane = ct & 31;
-  for (int mb = 0; mb < a.M; mb += ng) {
-    const int m = mb + g;
-    const bool act = m < a.M;
-    float av = 0.f;
-    if (act) {
-      const float gv = bfround(tout[m * 128 + i]);
-      const float uv = bfround(tout[(a.Mp + m) * 128 + i]);
-      av = gv / (1.f + expf(-gv)) * uv;
+                             int nthr, int ct) {
+  const int lane = ct & 31, wi = ct >> 5, nw = nthr >> 5;
+  for (int m = wi; m < a.M; m += nw) {
+    float av[4];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float gv = bfround(tout[m * 128 + lane + 32 * k]);
+      const float uv = bfround(tout[(a.Mp + m) * 128 + lane + 32 * k]);
+      av[k] = gv / (1.f + expf(-gv)) * uv;
+      amax = fmaxf(amax, fabsf(av[k]));
     }
+    const size_t base = static_cast<size_t>(m) * a.act_ld + tg * 128;
     if (!a.fp8) {
-      if (act)
-        static_cast<uint16_t*>(a.act)[static_cast<size_t>(m) * a.act_ld + tg * 128 + i] = f2bf(av);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        static_cast<uint16_t*>(a.act)[base + lane + 32 * k] = f2bf(av[k]);
     } else {
-      const float am = warp_max(fabsf(av));
-      if (lane == 0) sh.red[((mb / ng) & 1) * 8 + g * 4 + wg] = am;
-      named_bar(bar, nthr);
-      const float* rr = sh.red + ((mb / ng) & 1) * 8 + g * 4;
-      const float amax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
-      const float s = amax > 0.f ? amax / 448.f : 1.f;
-      if (act) {
-        static_cast<uint8_t*>(a.act)[static_cast<size_t>(m) * a.act_ld + tg * 128 + i] = f2e4m3(av / s);
-        if (i == 0) a.act_scale[static_cast<size_t>(m) * (a.act_ld >> 7) + tg] = s;
-      }
+      amax = warp_max(amax);
+      const float sc = amax > 0.f ? amax / 448.f : 1.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        static_cast<uint8_t*>(a.act)[base + lane + 32 * k] = f2e4m3(av[k] / sc);
+      if (lane == 0) a.act_scale[static_cast<size_t>(m) * (a.act_ld >> 7) + tg] = sc;
     }
   }
 }
@@ -359,38 +448,30 @@ __device__ void epi_logits(const GemmArgs& a, int tg, int tl, const float* tout,
                            const GemmShared& sh) {
   const Binding* bd = ctx.binding;
   float* logits = resolve<float>(a.out, bd);
-  const int ng = nthr >> 7, g = ct >> 7, i = ct & 127, wg = (ct >> 5) & 3;
-  const int lane = ct & 31;
-  for (int mb = 0; mb < a.M; mb += ng) {
-    const int m = mb + g;
-    const bool act = m < a.M;
-    float v = act ? tout[m * 128 + i] : -INFINITY;
-    int idx = tg * 128 + i;
-    if (act) logits[static_cast<size_t>(m) * a.ldo + idx] = v;
+  const int lane = ct & 31, wi = ct >> 5, nw = nthr >> 5;
+  for (int m = wi; m < a.M; m += nw) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = lane + 32 * k;
+      const float v = tout[m * 128 + i];
+      logits[static_cast<size_t>(m) * a.ldo + tg * 128 + i] = v;
+      if (v > bv || (v == bv && tg * 128 + i < bi)) {
+        bv = v;
+        bi = tg * 128 + i;
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-      if (ov > v || (ov == v && oi < idx)) {
-        v = ov;
-        idx = oi;
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
       }
     }
     if (lane == 0) {
-      sh.red[((mb / ng) & 1) * 8 + g * 4 + wg] = v;
-      sh.bidx[((mb / ng) & 1) * 8 + g * 4 + wg] = idx;
-    }
-    named_bar(bar, nthr);
-    if (act && i == 0) {
-      const float* rv = sh.red + ((mb / ng) & 1) * 8 + g * 4;
-      const int* ri = sh.bidx + ((mb / ng) & 1) * 8 + g * 4;
-      float bv = rv[0];
-      int bi = ri[0];
-      for (int k = 1; k < 4; ++k)
-        if (rv[k] > bv || (rv[k] == bv && ri[k] < bi)) {
-          bv = rv[k];
-          bi = ri[k];
-        }
       a.best_val[static_cast<size_t>(tl) * a.M + m] = bv;
       a.best_idx[static_cast<size_t>(tl) * a.M + m] = bi;
     }
@@ -405,9 +486,7 @@ __device__ void epi_logits(const GemmArgs& a, int tg, int tl, const float* tout,
   if (!sh.flag[1]) return;
   __threadfence();
   int* ids = resolve<int>(a.ids, bd);
-  // one warp per token
-  const int wn = nthr >> 5, wi = ct >> 5;
-  for (int m = wi; m < a.M; m += wn) {
+  for (int m = wi; m < a.M; m += nw) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int t = lane; t < a.NT; t += 32) {
@@ -444,49 +523,36 @@ __device__ void gemm_finish_tile(const GemmArgs& a, int c, long long u0, int tl,
     const long long U = static_cast<long long>(a.NT) * a.KB;
     const long long ts = static_cast<long long>(tl) * a.KB;
     const int slot = (u0 >= ts) ? 0 : 1;
-    float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * nel;
-    for (int e = ct; e < nel; e += nthr) mine[e] = tout[e];
+    float4* mine = reinterpret_cast<float4*>(a.ws + static_cast<size_t>(c * 2 + slot) * nel);
+    for (int e4 = ct; e4 < nel / 4; e4 += nthr) mine[e4] = reinterpret_cast<const float4*>(tout)[e4];
     __threadfence();
     named_bar(bar, nthr);
-    const int cf = sk_owner(U, a.G, ts);
-    const int cl = sk_owner(U, a.G, ts + a.KB - 1);
     if (ct == 0) {
-      int n = 0;
-      for (int cc = cf; cc <= cl; ++cc)
-        if (sk_begin(U, a.G, cc + 1) > sk_begin(U, a.G, cc)) ++n;
+      const int n = sk_contributors(U, a.G, ts, a.KB, sh.ctb);
+      sh.flag[3] = n;
       const unsigned old = atomicAdd(a.tile_cnt + tl, 1u);
       sh.flag[0] = (old + 1 == static_cast<unsigned>(n)) ? 1 : 0;
     }
     named_bar(bar, nthr);
     if (!sh.flag[0]) return;
     __threadfence();
-    for (int e = ct; e < nel; e += nthr) {
-      float s = 0.f;
-      for (int cc = cf; cc <= cl; ++cc) {
-        const long long b0 = sk_begin(U, a.G, cc);
-        if (sk_begin(U, a.G, cc + 1) <= b0) continue;
-        if (cc == c) {
-          s += tout[e];
-        } else {
-          const int sl = (b0 >= ts) ? 0 : 1;
-          s += __ldcg(a.ws + static_cast<size_t>(cc * 2 + sl) * nel + e);
-        }
-      }
-      tout[e] = s;
-    }
+    // every partial, this CTA's included, is read back from the workspace in
+    // CTA order: the sum does not depend on which CTA arrived last
+    ordered_sum4(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb,
+                 sh.flag[3], nel / 4, nthr, ct);
     if (ct == 0) a.tile_cnt[tl] = 0u;
     named_bar(bar, nthr);
   }
   const int tg = a.t_base + tl;
   switch (a.epi) {
     case EPI_QKV_ROPE:
-      epi_qkv_rope(a, tg, tout, nthr, ct, bar, ctx, sh);
+      epi_qkv_rope(a, tg, tout, nthr, ct, ctx, sh);
       break;
     case EPI_STORE_BF16:
       epi_store_bf16(a, tg, tout, nthr, ct, ctx.binding);
       break;
     case EPI_SILU_MUL:
-      epi_silu_mul(a, tg, tout, nthr, ct, bar, sh);
+      epi_silu_mul(a, tg, tout, nthr, ct);
       break;
     case EPI_LOGITS:
       epi_logits(a, tg, tl, tout, nthr, ct, bar, ctx, sh);
@@ -525,8 +591,21 @@ __device__ __forceinline__ void unpack_e4m3x16(const uint4& v, float* f) {
 }
 
 // ------------------------------------------------------------ GEMM engine
-// kMG: GEMV token bound (1/2/4/8, CUDA cores); kMp: tcgen05 N (16/32/64).
+// kMG: GEMV token bound (1/2/4, CUDA cores); kMp: tcgen05 N (16/32/64).
 // Exactly one of them is non-zero.
+//
+// Roles.  Warp 0 lane 0 streams the weight tile(s) and the activation slice
+// of each unit into a ring of `stages` shared-memory stages (TMA, 128-byte
+// swizzle); before its first dependent read it issues the weights of the
+// first stages (they do not depend on the previous operation).
+//   GEMV (M <= 4): warps 1-8 each take 16 rows of a stage, 8 lanes per row.
+//   tcgen05 (M > 4): warp 1 lane 0 issues 4 MMAs (K = 32 bytes each) per
+//   unit into a ring of TMEM accumulators; warps 5-8 read each unit's
+//   accumulator (TMEM lane quarter = warp % 4), apply the FP8 block scales
+//   and accumulate the tile in registers.
+// Waits are per warp (all lanes poll, the warp agrees); a failed wait marks
+// the warp dead, it skips work but keeps the barrier sequence, and the group
+// agrees on failure with one OR-barrier per tile run.
 template <int kMG, int kMp>
 __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
                           const KernelCtx& ctx, uint8_t* smem,
@@ -534,35 +613,38 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   constexpr bool kMMA = kMp > 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npair = a.pair ? 2 : 1;
-  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages);
+  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M);
   GemmShared sh;
   sh.stage0 = smem;
   sh.tout = reinterpret_cast<float*>(smem + L.tile_off);
+  sh.sx = reinterpret_cast<float*>(smem + L.sx_off);
+  sh.sw = reinterpret_cast<float*>(smem + L.sw_off);
+  sh.tok_pos = reinterpret_cast<int*>(smem + L.epi_off);
+  sh.tok_row = sh.tok_pos + a.M;
+  sh.rope = reinterpret_cast<float2*>(smem + L.epi_off + a.M * 8);
   sh.full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   sh.empty = sh.full + kMaxStages;
   sh.tfull = sh.empty + kMaxStages;
-  sh.tempty = sh.tfull + 2;
+  sh.tempty = sh.tfull + kMaxTmemBufs;
   sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
-  sh.red = reinterpret_cast<float*>(smem + L.misc_off + 16);
-  sh.bidx = reinterpret_cast<int*>(smem + L.misc_off + 16 + 64);
-  sh.nb = reinterpret_cast<float*>(smem + L.nb_off);
+  sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
   const long long U = static_cast<long long>(a.NT) * a.KB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const int nunits = static_cast<int>(u1 - u0);
   const int S = a.stages;
+  const int NTB = kMMA ? a.tmem_bufs : 1;
   const int kel = a.fp8 ? 128 : 64;  // elements per k-block
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], kMMA ? 1 : 8);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxTmemBufs; ++b) {
       mbar_init(&sh.tfull[b], 1);
       mbar_init(&sh.tempty[b], 4);
     }
-    sh.flag[0] = sh.flag[1] = 0;
+    sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
     sh.flag[2] = 1;
-    sh.flag[3] = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -621,15 +703,31 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   }
 
   if constexpr (!kMMA) {
-    // ----------------------------------------------- CUDA-core GEMV (M <= 8)
+    // ----------------------------------------------- CUDA-core GEMV (M <= 4)
     const int ct = tid - 32;
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
+    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
     const int c8 = ct & 7, r0 = ct >> 3;
+    bool dead = false;
     int i = 0;
     while (i < nunits) {
       const long long u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
+      const int tg = a.t_base + tl;
+      if (a.fp8) {
+        // the run's scales, once: sx[k][m], sw[p][k]
+        for (int e = ct; e < run * a.M; e += 256) {
+          const int k = e / a.M, m = e % a.M;
+          sh.sx[e] = __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb0 + k);
+        }
+        for (int e = ct; e < npair * run; e += 256) {
+          const int p = e / run, k = e % run;
+          const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
+          sh.sw[p * run + k] = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb0 + k);
+        }
+        named_bar(1, 256);
+      }
       float acc[2][4][kMG];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
@@ -639,42 +737,49 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
           for (int m = 0; m < kMG; ++m) acc[p][j][m] = 0.f;
       for (int k = 0; k < run; ++k, ++i) {
         const int s = i % S;
-        if (ct == 0) sh.flag[2] = mbar_wait(&sh.full[s], (i / S) & 1, ctx, 13) ? 1 : 0;
-        named_bar(1, 256);
-        if (!sh.flag[2]) return;
+        if (!dead) dead = !warp_wait(&sh.full[s], (i / S) & 1, ctx, 13);
+        if (dead) continue;
         const uint8_t* st = sh.stage0 + s * L.stage_bytes;
         const uint8_t* xs = st + npair * 16384;
         uint4 xv[kMG];
 #pragma unroll
         for (int m = 0; m < kMG; ++m)
           xv[m] = *reinterpret_cast<const uint4*>(xs + m * 128 + ((c8 ^ (m & 7)) << 4));
-        const int kb = kb0 + k;
-        const int tg = a.t_base + tl;
-        for (int p = 0; p < npair; ++p) {
-          float sw = 1.f;
-          if (a.fp8) {
-            const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
-            sw = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb);
-          }
+        if (!a.fp8) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = r0 + 32 * j;
-            const uint4 wv = *reinterpret_cast<const uint4*>(
-                st + p * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4));
-            if (!a.fp8) {
+          for (int p = 0; p < 2; ++p) {
+            if (p >= npair) break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = r0 + 32 * j;
+              const uint4 wv = *reinterpret_cast<const uint4*>(
+                  st + p * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4));
 #pragma unroll
               for (int m = 0; m < kMG; ++m) acc[p][j][m] += dot8_bf16(wv, xv[m]);
-            } else {
+            }
+          }
+        } else {
+          // e4m3 x e4m3 in fp32
+          float xf[kMG][16];
+#pragma unroll
+          for (int m = 0; m < kMG; ++m) unpack_e4m3x16(xv[m], xf[m]);
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            if (p >= npair) break;
+            const float sw = sh.sw[p * run + k];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = r0 + 32 * j;
+              const uint4 wv = *reinterpret_cast<const uint4*>(
+                  st + p * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4));
               float wf[16];
               unpack_e4m3x16(wv, wf);
 #pragma unroll
               for (int m = 0; m < kMG; ++m) {
-                float xf[16];
-                unpack_e4m3x16(xv[m], xf);
                 float d = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) d = fmaf(wf[e], xf[e], d);
-                const float sa = m < a.M ? __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb) : 0.f;
+                for (int e = 0; e < 16; ++e) d = fmaf(wf[e], xf[m][e], d);
+                const float sa = m < a.M ? sh.sx[k * a.M + m] : 0.f;
                 acc[p][j][m] = fmaf(d, sw * sa, acc[p][j][m]);
               }
             }
@@ -698,11 +803,11 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
             if (c8 == 0 && m < a.M) sh.tout[(p * a.Mp + m) * 128 + r0 + 32 * j] = v;
           }
       }
-      named_bar(1, 256);
+      if (named_bar_or(1, 256, dead)) return;
       gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 256, ct, 1, ctx, sh);
     }
   } else {
-    // --------------------------------------------- tcgen05 (M > 8, N = kMp)
+    // --------------------------------------------- tcgen05 (M > 4, N = kMp)
     const int ncols = npair * kMp;  // TMEM columns per accumulator buffer
     if (warp == 1) {
       idle_wait(dep);
@@ -710,9 +815,9 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
         int issued = 0;
         for (int i = 0; i < nunits; ++i) {
-          const int s = i % S, b = i & 1;
+          const int s = i % S, b = i % NTB;
           if (!mbar_wait(&sh.full[s], (i / S) & 1, ctx, 14)) break;
-          if (i >= 2 && !mbar_wait(&sh.tempty[b], ((i >> 1) - 1) & 1, ctx, 15)) break;
+          if (i >= NTB && !mbar_wait(&sh.tempty[b], ((i / NTB) - 1) & 1, ctx, 15)) break;
           tc_fence_after();
           const uint32_t sa = smem_u32(sh.stage0 + s * L.stage_bytes);
           for (int p = 0; p < npair; ++p) {
@@ -732,8 +837,10 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
           issued = i + 1;
         }
         // no MMA may still read shared memory or write TMEM when we leave
-        if (issued > 0)
-          mbar_drain(&sh.tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1, ctx.budget_ns);
+        if (issued > 0) {
+          const int l = issued - 1;
+          mbar_drain(&sh.tfull[l % NTB], (l / NTB) & 1, ctx.budget_ns);
+        }
       }
       return;
     }
@@ -746,32 +853,40 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     const int q = warp & 3;
     const int row = q * 32 + lane;
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
+    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
+    bool dead = false;
     int i = 0;
     while (i < nunits) {
       const long long u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
       const int tg = a.t_base + tl;
+      if (a.fp8) {
+        for (int e = et; e < run * a.M; e += 128) {
+          const int k = e / a.M, m = e % a.M;
+          sh.sx[e] = __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb0 + k);
+        }
+        for (int e = et; e < npair * run; e += 128) {
+          const int p = e / run, k = e % run;
+          const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
+          sh.sw[p * run + k] = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb0 + k);
+        }
+        named_bar(2, 128);
+      }
       float acc[2][kMp];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
 #pragma unroll
         for (int m = 0; m < kMp; ++m) acc[p][m] = 0.f;
       for (int k = 0; k < run; ++k, ++i) {
-        const int b = i & 1;
-        if (et == 0) sh.flag[2] = mbar_wait(&sh.tfull[b], (i >> 1) & 1, ctx, 17) ? 1 : 0;
-        named_bar(2, 128);
-        if (!sh.flag[2]) return;
+        const int b = i % NTB;
+        if (!dead) dead = !warp_wait(&sh.tfull[b], (i / NTB) & 1, ctx, 17);
+        if (dead) continue;
         tc_fence_after();
-        const int kb = kb0 + k;
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
           if (p >= npair) break;
-          float sw = 1.f;
-          if (a.fp8) {
-            const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
-            sw = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb);
-          }
+          const float sw = a.fp8 ? sh.sw[p * run + k] : 1.f;
 #pragma unroll
           for (int c16 = 0; c16 < kMp / 16; ++c16) {
             float v[16];
@@ -781,7 +896,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int m = c16 * 16 + e;
-                const float sa = m < a.M ? __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb) : 0.f;
+                const float sa = m < a.M ? sh.sx[k * a.M + m] : 0.f;
                 acc[p][m] = fmaf(v[e], sw * sa, acc[p][m]);
               }
             } else {
@@ -801,7 +916,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
         for (int m = 0; m < kMp; ++m)
           if (m < a.M) sh.tout[(p * a.Mp + m) * 128 + row] = acc[p][m];
       }
-      named_bar(2, 128);
+      if (named_bar_or(2, 128, dead)) return;
       gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, sh);
     }
   }
@@ -809,23 +924,23 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 
 // ============================================================== ATTENTION
 struct AttnSmem {
-  int stage_bytes, q_off, s_off, p_off, o_off, stat_off, bar_off, misc_off, total;
+  int stage_bytes, q_off, o_off, stat_off, bar_off, misc_off, total;
 };
 
-constexpr int kSPitch = 68;   // fp32 score row pitch (64 keys + pad)
-
+// stage: K (d 0-63 | d 64-127) then V (same), each half 64 keys x 128 bytes,
+// 128-byte swizzle (TMA), 32 KiB per 64-key unit.
 __host__ __device__ inline AttnSmem attn_smem_layout(int QRp, int stages) {
   AttnSmem L;
-  L.stage_bytes = 2 * kAttnKeys * 128 * 2;            // K + V, 64 keys x 128 d bf16
-  L.q_off = stages * L.stage_bytes;                   // bf16 [QRp][128], swizzled
-  L.s_off = L.q_off + QRp * 256;                      // fp32 [QRp][kSPitch]
-  L.p_off = L.s_off + QRp * kSPitch * 4;              // bf16 [QRp][64], swizzled
-  L.o_off = L.p_off + QRp * 128;                      // fp32 [QRp][128]
-  L.stat_off = L.o_off + QRp * 128 * 4;               // m, l, scale, lse, wsum [QRp] + pos
-  L.bar_off = L.stat_off + QRp * 4 * 6 + 64;
+  L.stage_bytes = 4 * kAttnKeys * 128;
+  L.q_off = stages * L.stage_bytes;                 // bf16 [QRp][128], swizzled
+  L.o_off = L.q_off + QRp * 256;                    // fp32 [QRp][128]
+  L.stat_off = L.o_off + QRp * 128 * 4;             // m, l per key group, lse, w, pos
+  L.bar_off = L.stat_off + (4 * QRp * 2 + QRp * 3) * 4 + 64;
   L.bar_off = (L.bar_off + 15) & ~15;
+  // after the barriers: flags, producer page batch [32 units x 4 pages],
+  // token positions [64], contributor list, combine weights [kMaxContrib]
   L.misc_off = L.bar_off + 2 * kMaxStages * 8;
-  L.total = L.misc_off + 64;
+  L.total = L.misc_off + 64 + 32 * 4 * 4 + 64 * 4 + kMaxContrib * 4 + kMaxContrib * 4;
   return L;
 }
 
@@ -853,35 +968,52 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Split-KV GQA decode attention over 64-key blocks with an online softmax
-// (base-2 exponentials, scores pre-scaled by log2(e)/sqrt(d)), partial
-// outputs normalised per split with their log-sum-exp, and the combine
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
+}
+
+// Split-KV GQA decode attention over 64-key blocks.  The G = Hq / Hkv query
+// heads of T tokens (QR = T * G rows; row rr = t * G + g is token r * T + t,
+// q head h * G + g, causal limit positions[r * T + t]) share one K/V stream.
+// Scores are scaled by log2(e) / sqrt(d) so exponentials are base 2.
+//
+// Warps 1-8 = 4 key groups (16 keys of each block) x 2 head-dim halves.
+// Each warp keeps its own online-softmax state (row max m, row sum l) in
+// registers, computes S = Q K^T for its 16 keys (both halves of d; the two
+// d-half warps of a key group compute the same S), rescales its O slice and
+// adds P V for its 64 columns, reusing the S fragments as the A operand.  At
+// the end of a (request, kv-head) run the four key groups are merged in a
+// fixed order; a run covering only part of the KV stream leaves its
+// normalised partial O_i and lse_i, and the last CTA of the pair combines
 //   lse = log sum_i e^{lse_i},  O = sum_i e^{lse_i - lse} O_i
-// done by the last CTA of each (request, kv head) pair.  QR = T*G query rows
-// share one K/V stream; row rr = t*G + g is token r*T + t, q head h*G + g,
-// causal limit positions[r*T + t].
-__device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
-                        const KernelCtx& ctx, uint8_t* smem) {
+// in CTA order (deterministic).
+template <int kNMT>
+__device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
+                          const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int QRp = a.QRp, nmt = QRp >> 4, G = a.Hq / a.Hkv;
+  const int QRp = a.QRp, G = a.Hq / a.Hkv;
+  constexpr int nmt = kNMT;
   const AttnSmem L = attn_smem_layout(QRp, a.stages);
   uint8_t* stage0 = smem;
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q_off);
-  float* Sb = reinterpret_cast<float*>(smem + L.s_off);
-  uint16_t* Pb = reinterpret_cast<uint16_t*>(smem + L.p_off);
   float* Ob = reinterpret_cast<float*>(smem + L.o_off);
-  float* row_m = reinterpret_cast<float*>(smem + L.stat_off);
-  float* row_l = row_m + QRp;
-  float* row_sc = row_l + QRp;
-  float* row_lse = row_sc + QRp;
+  float* kg_m = reinterpret_cast<float*>(smem + L.stat_off);   // [4][QRp]
+  float* kg_l = kg_m + 4 * QRp;                                 // [4][QRp]
+  float* row_lse = kg_l + 4 * QRp;
   float* row_w = row_lse + QRp;
   int* row_pos = reinterpret_cast<int*>(row_w + QRp);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kMaxStages;
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
+  int* pgbuf = flag + 16;                 // [32][4] pages of the producer's batch
+  int* ppos = pgbuf + 32 * 4;             // [64] token positions (producer)
+  int* ctb = ppos + 64;                   // [kMaxContrib] combine contributors
+  float* cw = reinterpret_cast<float*>(ctb + kMaxContrib);  // [kMaxContrib] weights
   const int S = a.stages;
   const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const Binding* bd = ctx.binding;
+  const CUtensorMap* kvm = &bd->kv_map;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -892,7 +1024,6 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
     fence_barrier_init();
   }
   __syncthreads();
-  const Binding* bd = ctx.binding;
 
   if (warp == 0) {
     if (lane != 0) {
@@ -901,54 +1032,66 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
     }
     // ------------------------------------------------------- producer
     bool ok = single_wait(dep, ctx, 30);
+    fence_tmap_acquire(kvm);
+    prefetch_tmap(kvm);
     const int* pos = resolve<const int>(a.pos, bd);
     const int* bt = resolve<const int>(a.bt, bd);
-    const uint16_t* kv = resolve<const uint16_t>(a.kv, bd);
+    const int M = a.R * a.T;
+    for (int m = 0; m < M; ++m) ppos[m] = pos[m];
     const uint64_t pol = policy_evict_first();
+    const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
+    const int npg = kAttnKeys / box;                      // boxes per 64-key unit
+    const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
     int i = 0;
-    for (long long u = u0; ok && u < u1; ++u) {
-      const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
-      const int r = p / a.Hkv, h = p % a.Hkv;
-      const int ctxr = pos[r * a.T + a.T - 1] + 1;
-      const int k0 = blk * kAttnKeys;
-      if (k0 >= ctxr) continue;
-      const int s = i % S;
-      if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
-        ok = false;
-        break;
-      }
-      uint8_t* st = stage0 + s * L.stage_bytes;
-      const int nk = min(kAttnKeys, ctxr - k0);
-      if (a.P >= kAttnKeys) {
-        const int lp = k0 / a.P;
-        int page = lp < a.max_pages ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
-        if (page < 0 || page >= a.num_pages) {
-          report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, lp);
-          page = 0;
+    for (long long ub = u0; ok && ub < u1; ub += 32) {
+      const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
+      // the batch's page numbers: independent loads, one round trip
+#pragma unroll 4
+      for (int j = 0; j < nb; ++j) {
+        const long long u = ub + j;
+        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+        const int r = p / a.Hkv;
+        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+        for (int q = 0; q < npg; ++q) {
+          const int key = blk * kAttnKeys + q * box;
+          const int lp = key / a.P;
+          pgbuf[j * 4 + q] = (key < ctxr && lp < a.max_pages)
+                                 ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
         }
-        const size_t kb = kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, k0 % a.P);
-        const size_t vb = kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, k0 % a.P);
-        mbar_arrive_expect_tx(&full[s], 2 * kAttnKeys * 256);
-        bulk_load(st, kv + kb * 128, kAttnKeys * 256, &full[s], pol);
-        bulk_load(st + kAttnKeys * 256, kv + vb * 128, kAttnKeys * 256, &full[s], pol);
-      } else {
-        const int npg = kAttnKeys / a.P;
-        const int nvalid = min(npg, (nk + a.P - 1) / a.P);
-        mbar_arrive_expect_tx(&full[s], 2 * nvalid * a.P * 256);
-        for (int q = 0; q < nvalid; ++q) {
-          const int lp = k0 / a.P + q;
-          int page = lp < a.max_pages ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
+      }
+      for (int j = 0; j < nb && ok; ++j) {
+        const long long u = ub + j;
+        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+        const int r = p / a.Hkv, h = p % a.Hkv;
+        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+        const int k0 = blk * kAttnKeys;
+        if (k0 >= ctxr) continue;
+        const int s = i % S;
+        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stage0 + s * L.stage_bytes;
+        const int nk = min(kAttnKeys, ctxr - k0);
+        const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
+        mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
+        for (int q = 0; q < nbox; ++q) {
+          const int key = k0 + q * box;
+          int page = pgbuf[j * 4 + q];
           if (page < 0 || page >= a.num_pages) {
-            report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 33, lp);
+            report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, key / a.P);
             page = 0;
           }
-          const size_t kb = kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, 0);
-          const size_t vb = kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, 0);
-          bulk_load(st + q * a.P * 256, kv + kb * 128, a.P * 256, &full[s], pol);
-          bulk_load(st + kAttnKeys * 256 + q * a.P * 256, kv + vb * 128, a.P * 256, &full[s], pol);
+          const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
+          const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
+          uint8_t* dq = st + q * box * 128;
+          tma_load_2d(dq, kvm, &full[s], 0, rk, pol);
+          tma_load_2d(dq + half, kvm, &full[s], 64, rk, pol);
+          tma_load_2d(dq + 2 * half, kvm, &full[s], 0, rv, pol);
+          tma_load_2d(dq + 3 * half, kvm, &full[s], 64, rv, pol);
         }
+        ++i;
       }
-      ++i;
     }
     const int issued = i;
     for (int s = 0; s < S && s < issued; ++s) {
@@ -960,13 +1103,14 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
 
   // ---------------------------------------------------------- consumers
   const int ct = tid - 32, wc = warp - 1;  // wc: 0..7
+  const int kg = wc & 3, dh = wc >> 2;     // key group, head-dim half
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return;
   const int* pos = resolve<const int>(a.pos, bd);
   const uint16_t* qg = static_cast<const uint16_t*>(a.q);
-  const uint32_t qs_u32 = smem_u32(Qs), pb_u32 = smem_u32(Pb);
-  const int tpr = 256 / QRp;             // softmax threads per row
-  const int kpt = kAttnKeys / tpr;       // keys per softmax thread
-  int i = 0;                             // valid-unit counter (matches producer)
+  const uint32_t qs_u32 = smem_u32(Qs);
+  const int qr = lane >> 2, qc = lane & 3;  // fragment row / column pair
+  bool dead = false;
+  int i = 0;                               // valid-unit counter (matches producer)
   long long u = u0;
   while (u < u1) {
     const int p = static_cast<int>(u / a.NB);
@@ -975,7 +1119,7 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
     const int blk_b = static_cast<int>(run_end - static_cast<long long>(p) * a.NB);
     const int r = p / a.Hkv, h = p % a.Hkv;
     const int ctxr = pos[r * a.T + a.T - 1] + 1;
-    // load this pair's query rows (swizzled 16-byte chunks) and positions
+    // this pair's query rows (swizzled 16-byte chunks) and causal limits
     for (int e = ct; e < QRp * 16; e += 256) {
       const int rr = e >> 4, ch = e & 15;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -986,169 +1130,186 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
       }
       *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Qs) + rr * 256 + ((ch ^ (rr & 7)) << 4)) = v;
     }
-    for (int rr = ct; rr < QRp; rr += 256) {
-      row_m[rr] = -INFINITY;
-      row_l[rr] = 0.f;
-      row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
+    for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
+    named_bar(1, 256);
+    // per-thread limits of the rows this thread's fragments hold
+    int lim[kNMT][2];
+#pragma unroll
+    for (int mt = 0; mt < kNMT; ++mt) {
+      lim[mt][0] = row_pos[mt * 16 + qr];
+      lim[mt][1] = row_pos[mt * 16 + qr + 8];
     }
-    float o[4][2][4];
+    float o[kNMT][8][4];
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int mt = 0; mt < kNMT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-    named_bar(1, 256);
+    float mrow[kNMT][2], lrow[kNMT][2];
+#pragma unroll
+    for (int mt = 0; mt < kNMT; ++mt) {
+      mrow[mt][0] = mrow[mt][1] = -INFINITY;
+      lrow[mt][0] = lrow[mt][1] = 0.f;
+    }
     const int nvb = (ctxr + kAttnKeys - 1) / kAttnKeys;   // valid blocks
     for (int blk = blk_a; blk < min(blk_b, nvb); ++blk, ++i) {
       const int s = i % S;
-      if (ct == 0) flag[2] = mbar_wait(&full[s], (i / S) & 1, ctx, 35) ? 1 : 0;
-      named_bar(1, 256);
-      if (!flag[2]) return;
+      if (!dead) dead = !warp_wait(&full[s], (i / S) & 1, ctx, 35);
+      if (dead) continue;
       uint8_t* st = stage0 + s * L.stage_bytes;
-      const uint32_t ks_u32 = smem_u32(st), vs_u32 = smem_u32(st + kAttnKeys * 256);
+      const uint32_t kb_u32 = smem_u32(st), vb_u32 = smem_u32(st + 2 * kAttnKeys * 128);
       const int k0 = blk * kAttnKeys;
       const int nk = min(kAttnKeys, ctxr - k0);
       if (nk < kAttnKeys) {
-        // keys past the context were not loaded (or hold stale data): zero V
-        for (int e = ct; e < (kAttnKeys - nk) * 16; e += 256)
-          *reinterpret_cast<uint4*>(st + kAttnKeys * 256 + (nk + (e >> 4)) * 256 + (e & 15) * 16) =
-              make_uint4(0, 0, 0, 0);
-        fence_proxy_async_shared();  // ordered before the stage's next TMA fill
-      }
-      // S = Q K^T for keys [8 wc, 8 wc + 8) of the block
-      {
-        float sc[4][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sc[mt][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
-          uint32_t b0, b1, b2, b3;
-          const int key = wc * 8 + (lane & 7);
-          const int ch = ks * 2 + (lane >> 3);
-          ldsm_x4(ks_u32 + key * 256 + ch * 16, b0, b1, b2, b3);
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            if (mt >= nmt) break;
-            const int qrow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int qch = (ks + kk) * 2 + (lane >> 4);
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
-              if (kk == 0)
-                mma_bf16_16816(sc[mt], a0, a1, a2, a3, b0, b1);
-              else
-                mma_bf16_16816(sc[mt], a0, a1, a2, a3, b2, b3);
-            }
-          }
+        // keys past the context were not loaded (or hold stale data): zero
+        // this warp's V rows so that 0-probability keys contribute exactly 0
+        uint8_t* vh = st + (2 + dh) * kAttnKeys * 128;
+        for (int e = lane; e < 16 * 8; e += 32) {
+          const int key = kg * 16 + (e >> 3);
+          if (key >= nk) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
+        __syncwarp();
+      }
+      // S = Q K^T for keys [16 kg, 16 kg + 16) of the block
+      float sc[kNMT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < kNMT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int hk = ks >> 2;                 // which d-half holds this k-step
+        const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb_u32 + hk * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           if (mt >= nmt) break;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rr = mt * 16 + (lane >> 2) + (e >> 1) * 8;
-            const int col = wc * 8 + (lane & 3) * 2 + (e & 1);
-            const int key = k0 + col;
-            const bool valid = rr < a.QR && key <= row_pos[rr] && col < nk;
-            Sb[rr * kSPitch + col] = valid ? sc[mt][e] * a.scale_log2 : -INFINITY;
-          }
+          const int qrow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int qch = ks * 2 + (lane >> 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
+          mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
         }
       }
-      named_bar(1, 256);
-      // online softmax: tpr threads per row
-      {
-        const int rr = ct / tpr, sub = ct % tpr;
-        float sv[16];
-        float lmax = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if (k >= kpt) break;
-          sv[k] = Sb[rr * kSPitch + sub * kpt + k];
-          lmax = fmaxf(lmax, sv[k]);
-        }
-        for (int o2 = tpr >> 1; o2 > 0; o2 >>= 1)
-          lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o2));
-        const float mold = row_m[rr];
-        const float mnew = fmaxf(mold, lmax);
-        const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(mold - mnew);
-        float lsum = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if (k >= kpt) break;
-          const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sv[k] - mnew);
-          lsum += pv;
-          const int col = sub * kpt + k;
-          const int ch = col >> 3;
-          Pb[(rr * 128 + (((ch ^ (rr & 7)) << 4) + (col & 7) * 2)) >> 1] = f2bf(pv);
-        }
-        for (int o2 = tpr >> 1; o2 > 0; o2 >>= 1)
-          lsum += __shfl_xor_sync(0xffffffffu, lsum, o2);
-        named_bar(1, 256);   // everyone has read row_m before it changes
-        if (sub == 0) {
-          row_sc[rr] = alpha;
-          row_m[rr] = mnew;
-          row_l[rr] = row_l[rr] * alpha + lsum;
-        }
-      }
-      named_bar(1, 256);
-      // O = O * alpha + P V for d columns [16 wc, 16 wc + 16)
+      // scale, mask, online softmax on this warp's 16 keys
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         if (mt >= nmt) break;
-        const float s0 = row_sc[mt * 16 + (lane >> 2)];
-        const float s1 = row_sc[mt * 16 + (lane >> 2) + 8];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          o[mt][nt][0] *= s0;
-          o[mt][nt][1] *= s0;
-          o[mt][nt][2] *= s1;
-          o[mt][nt][3] *= s1;
+        for (int hr = 0; hr < 2; ++hr) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = kg * 16 + nt * 8 + qc * 2 + e;
+              const int key = k0 + col;
+              const bool valid = col < nk && key <= lim[mt][hr];
+              const float v = valid ? sc[mt][nt][hr * 2 + e] * a.scale_log2 : -INFINITY;
+              sc[mt][nt][hr * 2 + e] = v;
+              mx = fmaxf(mx, v);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mold = mrow[mt][hr];
+          const float mnew = fmaxf(mold, mx);
+          const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(mold - mnew);
+          float sum = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sc[mt][nt][hr * 2 + e] - mnew);
+              sc[mt][nt][hr * 2 + e] = pv;
+              sum += pv;
+            }
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          mrow[mt][hr] = mnew;
+          lrow[mt][hr] = lrow[mt][hr] * alpha + sum;
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) {
+            o[mt][nt][hr * 2] *= alpha;
+            o[mt][nt][hr * 2 + 1] *= alpha;
+          }
         }
       }
+      // O += P V for columns [64 dh, 64 dh + 64)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
+        const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ch = cp * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = wc * 2 + (lane >> 4);
-        ldsm_x4_t(vs_u32 + key * 256 + ch * 16, b0, b1, b2, b3);
+        ldsm_x4_t(vb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           if (mt >= nmt) break;
-          const int prow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int pch = ks * 2 + (lane >> 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(pb_u32 + prow * 128 + ((pch ^ (prow & 7)) << 4), a0, a1, a2, a3);
-          mma_bf16_16816(o[mt][0], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(o[mt][1], a0, a1, a2, a3, b2, b3);
+          const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+          const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+          const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+          const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+          mma_bf16_16816(o[mt][cp * 2], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(o[mt][cp * 2 + 1], a0, a1, a2, a3, b2, b3);
         }
       }
+      if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // ---- finish this pair: normalised partial O and its lse (base 2)
-    named_bar(1, 256);
+    // ---- merge the four key groups (fixed order) into Ob, then lse
+    if (named_bar_or(1, 256, dead)) return;
+    if (dh == 0 && qc == 0) {
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      if (mt >= nmt) break;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int rr = mt * 16 + (lane >> 2) + (e >> 1) * 8;
-        const float l = row_l[rr];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-          Ob[rr * 128 + wc * 16 + nt * 8 + (lane & 3) * 2 + (e & 1)] = o[mt][nt][e] * inv;
+      for (int mt = 0; mt < 4; ++mt) {
+        if (mt >= nmt) break;
+        kg_m[kg * QRp + mt * 16 + qr] = mrow[mt][0];
+        kg_m[kg * QRp + mt * 16 + qr + 8] = mrow[mt][1];
+        kg_l[kg * QRp + mt * 16 + qr] = lrow[mt][0];
+        kg_l[kg * QRp + mt * 16 + qr + 8] = lrow[mt][1];
       }
     }
+    named_bar(1, 256);
     for (int rr = ct; rr < QRp; rr += 256) {
-      const float l = row_l[rr];
-      row_lse[rr] = l > 0.f ? row_m[rr] + log2f(l) : -INFINITY;
+      float mx = -INFINITY;
+      for (int g4 = 0; g4 < 4; ++g4) mx = fmaxf(mx, kg_m[g4 * QRp + rr]);
+      float l = 0.f;
+      if (mx != -INFINITY)
+        for (int g4 = 0; g4 < 4; ++g4) l += kg_l[g4 * QRp + rr] * exp2f(kg_m[g4 * QRp + rr] - mx);
+      row_w[rr] = mx;
+      row_lse[rr] = l > 0.f ? mx + log2f(l) : -INFINITY;
+      kg_l[rr] = l;   // slot 0 now holds the merged row sum (read after the barrier)
     }
     named_bar(1, 256);
+    for (int g4 = 0; g4 < 4; ++g4) {
+      if (kg == g4) {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          if (mt >= nmt) break;
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int rr = mt * 16 + qr + hr * 8;
+            const float l = kg_l[rr];
+            const float f = (l > 0.f && mrow[mt][hr] != -INFINITY)
+                                ? exp2f(mrow[mt][hr] - row_w[rr]) / l : 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float* dst = Ob + rr * 128 + dh * 64 + nt * 8 + qc * 2 + e;
+                const float v = o[mt][nt][hr * 2 + e] * f;
+                *dst = g4 == 0 ? v : *dst + v;
+              }
+          }
+        }
+      }
+      named_bar(1, 256);
+    }
     const bool whole = (blk_a == 0 && blk_b == a.NB);
     if (!whole) {
       const long long ps = static_cast<long long>(p) * a.NB;
@@ -1159,49 +1320,63 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
       for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
       __threadfence();
       named_bar(1, 256);
-      const int cf = sk_owner(U, a.G, ps), cl = sk_owner(U, a.G, ps + a.NB - 1);
       if (ct == 0) {
-        int n = 0;
-        for (int cc = cf; cc <= cl; ++cc)
-          if (sk_begin(U, a.G, cc + 1) > sk_begin(U, a.G, cc)) ++n;
+        const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
+        flag[1] = n;
         const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
         flag[0] = (old + 1 == static_cast<unsigned>(n)) ? 1 : 0;
       }
       named_bar(1, 256);
       if (flag[0]) {
         __threadfence();
-        // per-row weights of every contributor: w_i = 2^(lse_i - max)
+        const int nc = flag[1];
+        // row weights: w_j = 2^(lse_j - max) / sum_k 2^(lse_k - max), all
+        // partials (this CTA's included) read back from the workspace
         for (int rr = ct; rr < QRp; rr += 256) {
           float mx = -INFINITY;
-          for (int cc = cf; cc <= cl; ++cc) {
-            const long long b0 = sk_begin(U, a.G, cc);
-            if (sk_begin(U, a.G, cc + 1) <= b0) continue;
-            const int sl = (b0 >= ps) ? 0 : 1;
-            const float le = cc == c ? row_lse[rr]
-                                     : __ldcg(a.ws + static_cast<size_t>(cc * 2 + sl) * part + QRp * 128 + rr);
-            mx = fmaxf(mx, le);
-          }
+          for (int j = 0; j < nc; ++j)
+            mx = fmaxf(mx, __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr));
           row_w[rr] = mx;
         }
         named_bar(1, 256);
-        for (int e = ct; e < QRp * 128; e += 256) {
-          const int rr = e >> 7;
+        // per-row weight table [nc][QRp] in the (now idle) Q buffer
+        float* wt = reinterpret_cast<float*>(Qs);
+        for (int e = ct; e < nc * QRp && e < QRp * 64; e += 256) {
+          const int j = e / QRp, rr = e % QRp;
           const float mx = row_w[rr];
-          float num = 0.f, den = 0.f;
-          if (mx != -INFINITY) {
-            for (int cc = cf; cc <= cl; ++cc) {
-              const long long b0 = sk_begin(U, a.G, cc);
-              if (sk_begin(U, a.G, cc + 1) <= b0) continue;
-              const int sl = (b0 >= ps) ? 0 : 1;
-              const float* src = a.ws + static_cast<size_t>(cc * 2 + sl) * part;
-              const float le = cc == c ? row_lse[rr] : __ldcg(src + QRp * 128 + rr);
-              const float ov = cc == c ? Ob[e] : __ldcg(src + e);
-              const float wgt = exp2f(le - mx);
-              num = fmaf(wgt, ov, num);
-              den += wgt;
+          const float le = __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
+          wt[e] = (mx == -INFINITY) ? 0.f : exp2f(le - mx);
+        }
+        named_bar(1, 256);
+        for (int rr = ct; rr < QRp; rr += 256) {
+          float den = 0.f;
+          for (int j = 0; j < nc; ++j) den += wt[j * QRp + rr];
+          cw[rr] = den > 0.f ? 1.f / den : 0.f;
+        }
+        named_bar(1, 256);
+        for (int e4 = ct; e4 < QRp * 32; e4 += 256) {
+          const int rr = e4 >> 5;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j0 = 0; j0 < nc; j0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[j] = (j0 + j < nc)
+                         ? __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<size_t>(ctb[j0 + j]) * part) + e4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j0 + j < nc) {
+                const float wgt = wt[(j0 + j) * QRp + rr];
+                acc.x = fmaf(wgt, v[j].x, acc.x);
+                acc.y = fmaf(wgt, v[j].y, acc.y);
+                acc.z = fmaf(wgt, v[j].z, acc.z);
+                acc.w = fmaf(wgt, v[j].w, acc.w);
+              }
             }
           }
-          Ob[e] = den > 0.f ? num / den : 0.f;
+          const float inv = cw[rr];
+          reinterpret_cast<float4*>(Ob)[e4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
         if (ct == 0) a.pair_cnt[p] = 0u;
         named_bar(1, 256);
@@ -1216,9 +1391,7 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
         const float4 v = *reinterpret_cast<const float4*>(Ob + rr * 128 + lane * 4);
         if (!a.fp8) {
           uint16_t* out = static_cast<uint16_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4;
-          const uint32_t lo = static_cast<uint32_t>(f2bf(v.x)) | (static_cast<uint32_t>(f2bf(v.y)) << 16);
-          const uint32_t hi = static_cast<uint32_t>(f2bf(v.z)) | (static_cast<uint32_t>(f2bf(v.w)) << 16);
-          *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
+          *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
         } else {
           const float am = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
           const float sc = am > 0.f ? am / 448.f : 1.f;
@@ -1234,6 +1407,16 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep,
     named_bar(1, 256);
     u = run_end;
   }
+}
+
+__device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
+                        uint8_t* smem) {
+  if (a.QRp <= 16)
+    attn_op_t<1>(a, c, dep, ctx, smem);
+  else if (a.QRp <= 32)
+    attn_op_t<2>(a, c, dep, ctx, smem);
+  else
+    attn_op_t<4>(a, c, dep, ctx, smem);
 }
 
 }  // namespace dl
