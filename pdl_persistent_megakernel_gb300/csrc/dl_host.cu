@@ -304,8 +304,9 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   // weight table holds 64 contributors
   a.G = static_cast<int>(std::min<long long>(std::min<long long>(p->sms, U),
                                              62LL * a.R * a.Hkv));
-  a.stages = std::max(2, std::min(kMaxStages, (kGemmSmemTarget - attn_smem_bytes(a.QRp, 0)) /
-                                                    (4 * kAttnKeys * 128)));
+  // 4 stages of 32 KiB keep the KV stream at full rate (more adds nothing)
+  a.stages = std::max(2, std::min(4, (kGemmSmemTarget - attn_smem_bytes(a.QRp, 0)) /
+                                         (4 * kAttnKeys * 128)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d)));
   a.ws = p->ws_attn;
   a.pair_cnt = cnt;

@@ -263,31 +263,48 @@ struct GemmShared {
 };
 
 // Sum of `nc` fp32 partials (float4 granular, nel4 float4s each) listed in
-// ctb as workspace slot indices, in list order, into dst; up to 8 loads per
-// thread in flight.
+// ctb as workspace slot indices, in list order, into dst.  Each thread owns
+// up to 8 float4s per pass and loads them for two contributors at a time,
+// so a pass costs about nc / 2 L2 round trips.
 __device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_t part,
                                              const int* ctb, int nc, int nel4, int nthr,
                                              int ct) {
-  for (int e4 = ct; e4 < nel4; e4 += nthr) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < nc; j0 += 8) {
-      float4 v[8];
+  constexpr int kQ = 8;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 * nthr < nel4; q0 += kQ) {
+    float4 acc[kQ];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = (j0 + j < nc)
-                   ? __ldcg(reinterpret_cast<const float4*>(ws + static_cast<size_t>(ctb[j0 + j]) * part) + e4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < kQ; ++q) acc[q] = z;
+    for (int j = 0; j < nc; j += 2) {
+      const float4* s0 = reinterpret_cast<const float4*>(ws + static_cast<size_t>(ctb[j]) * part);
+      const float4* s1 = j + 1 < nc
+          ? reinterpret_cast<const float4*>(ws + static_cast<size_t>(ctb[j + 1]) * part) : nullptr;
+      float4 v0[kQ], v1[kQ];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j0 + j < nc) {
-          acc.x += v[j].x;
-          acc.y += v[j].y;
-          acc.z += v[j].z;
-          acc.w += v[j].w;
+      for (int q = 0; q < kQ; ++q) {
+        const int e4 = ct + (q0 + q) * nthr;
+        v0[q] = e4 < nel4 ? __ldcg(s0 + e4) : z;
+        v1[q] = (s1 && e4 < nel4) ? __ldcg(s1 + e4) : z;
+      }
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        acc[q].x += v0[q].x;
+        acc[q].y += v0[q].y;
+        acc[q].z += v0[q].z;
+        acc[q].w += v0[q].w;
+        if (s1) {
+          acc[q].x += v1[q].x;
+          acc[q].y += v1[q].y;
+          acc[q].z += v1[q].z;
+          acc[q].w += v1[q].w;
         }
       }
     }
-    dst[e4] = acc;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int e4 = ct + (q0 + q) * nthr;
+      if (e4 < nel4) dst[e4] = acc[q];
+    }
   }
 }
 
@@ -590,6 +607,19 @@ __device__ __forceinline__ void unpack_e4m3x16(const uint4& v, float* f) {
   }
 }
 
+// The activation scales [M][KB] of the whole projection input, staged once
+// per CTA (float4 loads, several in flight per thread).
+__device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShared& sh,
+                                               int nthr, int ct, int bar) {
+  const int n4 = (a.M * a.KB) / 4;   // KB is a multiple of 4 for every projection
+  const float4* src = reinterpret_cast<const float4*>(a.x_scale);
+  float4* dst = reinterpret_cast<float4*>(sh.sx);
+#pragma unroll 4
+  for (int e = ct; e < n4; e += nthr) dst[e] = __ldcg(src + e);
+  for (int e = n4 * 4 + ct; e < a.M * a.KB; e += nthr) sh.sx[e] = __ldcg(a.x_scale + e);
+  named_bar(bar, nthr);
+}
+
 // ------------------------------------------------------------ GEMM engine
 // kMG: GEMV token bound (1/2/4, CUDA cores); kMp: tcgen05 N (16/32/64).
 // Exactly one of them is non-zero.
@@ -706,6 +736,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     // ----------------------------------------------- CUDA-core GEMV (M <= 4)
     const int ct = tid - 32;
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
+    if (a.fp8) stage_x_scales(a, sh, 256, ct, 1);
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
     const int c8 = ct & 7, r0 = ct >> 3;
     bool dead = false;
@@ -716,11 +747,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       const int run = min(nunits - i, a.KB - kb0);
       const int tg = a.t_base + tl;
       if (a.fp8) {
-        // the run's scales, once: sx[k][m], sw[p][k]
-        for (int e = ct; e < run * a.M; e += 256) {
-          const int k = e / a.M, m = e % a.M;
-          sh.sx[e] = __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb0 + k);
-        }
+        // this run's weight scales sw[p][k]
         for (int e = ct; e < npair * run; e += 256) {
           const int p = e / run, k = e % run;
           const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
@@ -779,7 +806,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
                 float d = 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) d = fmaf(wf[e], xf[m][e], d);
-                const float sa = m < a.M ? sh.sx[k * a.M + m] : 0.f;
+                const float sa = m < a.M ? sh.sx[m * a.KB + kb0 + k] : 0.f;
                 acc[p][j][m] = fmaf(d, sw * sa, acc[p][j][m]);
               }
             }
@@ -853,6 +880,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     const int q = warp & 3;
     const int row = q * 32 + lane;
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
+    if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
     bool dead = false;
     int i = 0;
@@ -862,10 +890,6 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       const int run = min(nunits - i, a.KB - kb0);
       const int tg = a.t_base + tl;
       if (a.fp8) {
-        for (int e = et; e < run * a.M; e += 128) {
-          const int k = e / a.M, m = e % a.M;
-          sh.sx[e] = __ldcg(a.x_scale + static_cast<size_t>(m) * a.KB + kb0 + k);
-        }
         for (int e = et; e < npair * run; e += 128) {
           const int p = e / run, k = e % run;
           const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
@@ -896,7 +920,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int m = c16 * 16 + e;
-                const float sa = m < a.M ? sh.sx[k * a.M + m] : 0.f;
+                const float sa = m < a.M ? sh.sx[m * a.KB + kb0 + k] : 0.f;
                 acc[p][m] = fmaf(v[e], sw * sa, acc[p][m]);
               }
             } else {
@@ -924,17 +948,21 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 
 // ============================================================== ATTENTION
 struct AttnSmem {
-  int stage_bytes, q_off, o_off, stat_off, bar_off, misc_off, total;
+  int stage_bytes, q_off, o_off, xs_off, stat_off, bar_off, misc_off, total;
 };
+
+constexpr int kOP = 136;   // fp32 row pitch of the merged O tile (bank spread)
 
 // stage: K (d 0-63 | d 64-127) then V (same), each half 64 keys x 128 bytes,
 // 128-byte swizzle (TMA), 32 KiB per 64-key unit.
 __host__ __device__ inline AttnSmem attn_smem_layout(int QRp, int stages) {
   AttnSmem L;
+  const int nmt = QRp / 16;
   L.stage_bytes = 4 * kAttnKeys * 128;
   L.q_off = stages * L.stage_bytes;                 // bf16 [QRp][128], swizzled
-  L.o_off = L.q_off + QRp * 256;                    // fp32 [QRp][128]
-  L.stat_off = L.o_off + QRp * 128 * 4;             // m, l per key group, lse, w, pos
+  L.o_off = L.q_off + QRp * 256;                    // fp32 [QRp][kOP]
+  L.xs_off = L.o_off + QRp * kOP * 4;               // partial-score exchange [2][8][nmt*8][32]
+  L.stat_off = L.xs_off + 2 * 8 * nmt * 8 * 32 * 4; // m, l per key group, lse, w, pos
   L.bar_off = L.stat_off + (4 * QRp * 2 + QRp * 3) * 4 + 64;
   L.bar_off = (L.bar_off + 15) & ~15;
   // after the barriers: flags, producer page batch [32 units x 4 pages],
@@ -977,26 +1005,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // q head h * G + g, causal limit positions[r * T + t]) share one K/V stream.
 // Scores are scaled by log2(e) / sqrt(d) so exponentials are base 2.
 //
-// Warps 1-8 = 4 key groups (16 keys of each block) x 2 head-dim halves.
-// Each warp keeps its own online-softmax state (row max m, row sum l) in
-// registers, computes S = Q K^T for its 16 keys (both halves of d; the two
-// d-half warps of a key group compute the same S), rescales its O slice and
-// adds P V for its 64 columns, reusing the S fragments as the A operand.  At
-// the end of a (request, kv-head) run the four key groups are merged in a
-// fixed order; a run covering only part of the KV stream leaves its
-// normalised partial O_i and lse_i, and the last CTA of the pair combines
+// Warps 1-8 = 4 key groups (16 keys of each block) x 2 head-dim halves.  The
+// two warps of a key group each compute the scores of its 16 keys over their
+// own half of d and exchange the fp32 partial sums through shared memory, so
+// both hold S = S_lo + S_hi.  Each warp keeps its own online-softmax state
+// (row max m, row sum l) in registers, rescales its O slice and adds P V for
+// its 64 columns, reusing the S fragments as the A operand.  At the end of a
+// (request, kv-head) run the four key groups are merged in a fixed order; a
+// run covering only part of the KV stream leaves its normalised partial O_i
+// and lse_i, and the last CTA of the pair combines
 //   lse = log sum_i e^{lse_i},  O = sum_i e^{lse_i - lse} O_i
-// in CTA order (deterministic).
+// over the partials in CTA order (deterministic).
 template <int kNMT>
 __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
                           const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QRp = a.QRp, G = a.Hq / a.Hkv;
   constexpr int nmt = kNMT;
+  constexpr int kXS = nmt * 8;   // partial-score floats per thread
   const AttnSmem L = attn_smem_layout(QRp, a.stages);
   uint8_t* stage0 = smem;
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q_off);
   float* Ob = reinterpret_cast<float*>(smem + L.o_off);
+  float* xs = reinterpret_cast<float*>(smem + L.xs_off);
   float* kg_m = reinterpret_cast<float*>(smem + L.stat_off);   // [4][QRp]
   float* kg_l = kg_m + 4 * QRp;                                 // [4][QRp]
   float* row_lse = kg_l + 4 * QRp;
@@ -1026,18 +1057,25 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   __syncthreads();
 
   if (warp == 0) {
-    if (lane != 0) {
-      idle_wait(dep);
-      return;
+    // ------------------------------------------ producer (warp 0, lane 0 issues)
+    bool ok = true;
+    if (dep.mode == 0) {
+      gdc_wait();
+      gdc_launch_dependents();
+      ok = !aborted(ctx.status);
+    } else {
+      if (lane == 0) ok = poll_deps(dep, ctx, 30);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
-    // ------------------------------------------------------- producer
-    bool ok = single_wait(dep, ctx, 30);
-    fence_tmap_acquire(kvm);
-    prefetch_tmap(kvm);
+    if (lane == 0) {
+      fence_tmap_acquire(kvm);
+      prefetch_tmap(kvm);
+    }
     const int* pos = resolve<const int>(a.pos, bd);
     const int* bt = resolve<const int>(a.bt, bd);
     const int M = a.R * a.T;
-    for (int m = 0; m < M; ++m) ppos[m] = pos[m];
+    for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
+    __syncwarp();
     const uint64_t pol = policy_evict_first();
     const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
     const int npg = kAttnKeys / box;                      // boxes per 64-key unit
@@ -1045,58 +1083,64 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     int i = 0;
     for (long long ub = u0; ok && ub < u1; ub += 32) {
       const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
-      // the batch's page numbers: independent loads, one round trip
-#pragma unroll 4
-      for (int j = 0; j < nb; ++j) {
+      // the batch's page numbers, loaded by the whole warp
+      for (int e = lane; e < nb * npg; e += 32) {
+        const int j = e / npg, q = e % npg;
         const long long u = ub + j;
         const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
         const int r = p / a.Hkv;
         const int ctxr = ppos[r * a.T + a.T - 1] + 1;
-        for (int q = 0; q < npg; ++q) {
-          const int key = blk * kAttnKeys + q * box;
-          const int lp = key / a.P;
-          pgbuf[j * 4 + q] = (key < ctxr && lp < a.max_pages)
-                                 ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
-        }
+        const int key = blk * kAttnKeys + q * box;
+        const int lp = key / a.P;
+        pgbuf[j * 4 + q] = (key < ctxr && lp < a.max_pages)
+                               ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
       }
-      for (int j = 0; j < nb && ok; ++j) {
-        const long long u = ub + j;
-        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
-        const int r = p / a.Hkv, h = p % a.Hkv;
-        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
-        const int k0 = blk * kAttnKeys;
-        if (k0 >= ctxr) continue;
-        const int s = i % S;
-        if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
-          ok = false;
-          break;
-        }
-        uint8_t* st = stage0 + s * L.stage_bytes;
-        const int nk = min(kAttnKeys, ctxr - k0);
-        const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
-        mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
-        for (int q = 0; q < nbox; ++q) {
-          const int key = k0 + q * box;
-          int page = pgbuf[j * 4 + q];
-          if (page < 0 || page >= a.num_pages) {
-            report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, key / a.P);
-            page = 0;
+      __syncwarp();
+      if (lane == 0) {
+        for (int j = 0; j < nb && ok; ++j) {
+          const long long u = ub + j;
+          const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+          const int r = p / a.Hkv, h = p % a.Hkv;
+          const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+          const int k0 = blk * kAttnKeys;
+          if (k0 >= ctxr) continue;
+          const int s = i % S;
+          if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
+            ok = false;
+            break;
           }
-          const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
-          const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
-          uint8_t* dq = st + q * box * 128;
-          tma_load_2d(dq, kvm, &full[s], 0, rk, pol);
-          tma_load_2d(dq + half, kvm, &full[s], 64, rk, pol);
-          tma_load_2d(dq + 2 * half, kvm, &full[s], 0, rv, pol);
-          tma_load_2d(dq + 3 * half, kvm, &full[s], 64, rv, pol);
+          uint8_t* st = stage0 + s * L.stage_bytes;
+          const int nk = min(kAttnKeys, ctxr - k0);
+          const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
+          mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
+          for (int q = 0; q < nbox; ++q) {
+            const int key = k0 + q * box;
+            int page = pgbuf[j * 4 + q];
+            if (page < 0 || page >= a.num_pages) {
+              report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, key / a.P);
+              page = 0;
+            }
+            const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
+            const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
+            uint8_t* dq = st + q * box * 128;
+            tma_load_2d(dq, kvm, &full[s], 0, rk, pol);
+            tma_load_2d(dq + half, kvm, &full[s], 64, rk, pol);
+            tma_load_2d(dq + 2 * half, kvm, &full[s], 0, rv, pol);
+            tma_load_2d(dq + 3 * half, kvm, &full[s], 64, rv, pol);
+          }
+          ++i;
         }
-        ++i;
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      i = __shfl_sync(0xffffffffu, i, 0);
+      __syncwarp();
     }
-    const int issued = i;
-    for (int s = 0; s < S && s < issued; ++s) {
-      const int last = s + ((issued - 1 - s) / S) * S;
-      mbar_drain(&full[s], (last / S) & 1, ctx.budget_ns);
+    if (lane == 0) {
+      const int issued = i;
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / S) * S;
+        mbar_drain(&full[s], (last / S) & 1, ctx.budget_ns);
+      }
     }
     return;
   }
@@ -1104,6 +1148,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   // ---------------------------------------------------------- consumers
   const int ct = tid - 32, wc = warp - 1;  // wc: 0..7
   const int kg = wc & 3, dh = wc >> 2;     // key group, head-dim half
+  const int partner = kg + 4 * (1 - dh);
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return;
   const int* pos = resolve<const int>(a.pos, bd);
   const uint16_t* qg = static_cast<const uint16_t*>(a.q);
@@ -1120,6 +1165,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     const int r = p / a.Hkv, h = p % a.Hkv;
     const int ctxr = pos[r * a.T + a.T - 1] + 1;
     // this pair's query rows (swizzled 16-byte chunks) and causal limits
+#pragma unroll 4
     for (int e = ct; e < QRp * 16; e += 256) {
       const int rr = e >> 4, ch = e & 15;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -1132,7 +1178,6 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     }
     for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
     named_bar(1, 256);
-    // per-thread limits of the rows this thread's fragments hold
     int lim[kNMT][2];
 #pragma unroll
     for (int mt = 0; mt < kNMT; ++mt) {
@@ -1156,22 +1201,11 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     for (int blk = blk_a; blk < min(blk_b, nvb); ++blk, ++i) {
       const int s = i % S;
       if (!dead) dead = !warp_wait(&full[s], (i / S) & 1, ctx, 35);
-      if (dead) continue;
       uint8_t* st = stage0 + s * L.stage_bytes;
       const uint32_t kb_u32 = smem_u32(st), vb_u32 = smem_u32(st + 2 * kAttnKeys * 128);
       const int k0 = blk * kAttnKeys;
       const int nk = min(kAttnKeys, ctxr - k0);
-      if (nk < kAttnKeys) {
-        // keys past the context were not loaded (or hold stale data): zero
-        // this warp's V rows so that 0-probability keys contribute exactly 0
-        uint8_t* vh = st + (2 + dh) * kAttnKeys * 128;
-        for (int e = lane; e < 16 * 8; e += 32) {
-          const int key = kg * 16 + (e >> 3);
-          if (key >= nk) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // S = Q K^T for keys [16 kg, 16 kg + 16) of the block
+      float* xbuf = xs + (i & 1) * (8 * kXS * 32);
       float sc[kNMT][2][4];
 #pragma unroll
       for (int mt = 0; mt < kNMT; ++mt)
@@ -1179,95 +1213,121 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int hk = ks >> 2;                 // which d-half holds this k-step
-        const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int ch = (ks & 3) * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb_u32 + hk * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          if (mt >= nmt) break;
-          const int qrow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int qch = ks * 2 + (lane >> 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
-          mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
+      if (!dead) {
+        if (nk < kAttnKeys) {
+          // keys past the context were not loaded (or hold stale data): zero
+          // this warp's V rows so that 0-probability keys contribute exactly 0
+          uint8_t* vh = st + (2 + dh) * kAttnKeys * 128;
+          for (int e = lane; e < 16 * 8; e += 32) {
+            const int key = kg * 16 + (e >> 3);
+            if (key >= nk) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
         }
-      }
-      // scale, mask, online softmax on this warp's 16 keys
+        // partial S over this warp's half of d
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        if (mt >= nmt) break;
+        for (int ks4 = 0; ks4 < 4; ++ks4) {
+          const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int ch = ks4 * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = kg * 16 + nt * 8 + qc * 2 + e;
-              const int key = k0 + col;
-              const bool valid = col < nk && key <= lim[mt][hr];
-              const float v = valid ? sc[mt][nt][hr * 2 + e] * a.scale_log2 : -INFINITY;
-              sc[mt][nt][hr * 2 + e] = v;
-              mx = fmaxf(mx, v);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float mold = mrow[mt][hr];
-          const float mnew = fmaxf(mold, mx);
-          const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(mold - mnew);
-          float sum = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sc[mt][nt][hr * 2 + e] - mnew);
-              sc[mt][nt][hr * 2 + e] = pv;
-              sum += pv;
-            }
-          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-          mrow[mt][hr] = mnew;
-          lrow[mt][hr] = lrow[mt][hr] * alpha + sum;
-#pragma unroll
-          for (int nt = 0; nt < 8; ++nt) {
-            o[mt][nt][hr * 2] *= alpha;
-            o[mt][nt][hr * 2 + 1] *= alpha;
+          for (int mt = 0; mt < kNMT; ++mt) {
+            const int qrow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int qch = (dh * 4 + ks4) * 2 + (lane >> 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
+            mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
           }
         }
+        float* mine = xbuf + wc * (kXS * 32);
+#pragma unroll
+        for (int mt = 0; mt < kNMT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mine[((mt * 2 + nt) * 4 + e) * 32 + lane] = sc[mt][nt][e];
       }
-      // O += P V for columns [64 dh, 64 dh + 64)
+      // the two d-half warps of this key group exchange partial scores
+      named_bar(2 + kg, 64);
+      if (!dead) {
+        const float* other = xbuf + partner * (kXS * 32);
 #pragma unroll
-      for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
-        const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = cp * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        for (int mt = 0; mt < kNMT; ++mt)
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          if (mt >= nmt) break;
-          const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-          const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-          const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-          const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
-          mma_bf16_16816(o[mt][cp * 2], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(o[mt][cp * 2 + 1], a0, a1, a2, a3, b2, b3);
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][nt][e] += other[((mt * 2 + nt) * 4 + e) * 32 + lane];
+        // scale, mask, online softmax on this key group's 16 keys
+#pragma unroll
+        for (int mt = 0; mt < kNMT; ++mt) {
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int col = kg * 16 + nt * 8 + qc * 2 + e;
+                const int key = k0 + col;
+                const bool valid = col < nk && key <= lim[mt][hr];
+                const float v = valid ? sc[mt][nt][hr * 2 + e] * a.scale_log2 : -INFINITY;
+                sc[mt][nt][hr * 2 + e] = v;
+                mx = fmaxf(mx, v);
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mold = mrow[mt][hr];
+            const float mnew = fmaxf(mold, mx);
+            const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(mold - mnew);
+            float sum = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sc[mt][nt][hr * 2 + e] - mnew);
+                sc[mt][nt][hr * 2 + e] = pv;
+                sum += pv;
+              }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            mrow[mt][hr] = mnew;
+            lrow[mt][hr] = lrow[mt][hr] * alpha + sum;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+              o[mt][nt][hr * 2] *= alpha;
+              o[mt][nt][hr * 2 + 1] *= alpha;
+            }
+          }
         }
+        // O += P V for columns [64 dh, 64 dh + 64)
+#pragma unroll
+        for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
+          const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int ch = cp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+          for (int mt = 0; mt < kNMT; ++mt) {
+            const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+            const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+            const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+            const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+            mma_bf16_16816(o[mt][cp * 2], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(o[mt][cp * 2 + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+        if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
     // ---- merge the four key groups (fixed order) into Ob, then lse
     if (named_bar_or(1, 256, dead)) return;
     if (dh == 0 && qc == 0) {
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        if (mt >= nmt) break;
+      for (int mt = 0; mt < kNMT; ++mt) {
         kg_m[kg * QRp + mt * 16 + qr] = mrow[mt][0];
         kg_m[kg * QRp + mt * 16 + qr + 8] = mrow[mt][1];
         kg_l[kg * QRp + mt * 16 + qr] = lrow[mt][0];
@@ -1286,26 +1346,41 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       kg_l[rr] = l;   // slot 0 now holds the merged row sum (read after the barrier)
     }
     named_bar(1, 256);
+    float fac[kNMT][2];
+#pragma unroll
+    for (int mt = 0; mt < kNMT; ++mt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int rr = mt * 16 + qr + hr * 8;
+        const float l = kg_l[rr];
+        fac[mt][hr] = (l > 0.f && mrow[mt][hr] != -INFINITY) ? exp2f(mrow[mt][hr] - row_w[rr]) / l : 0.f;
+      }
     for (int g4 = 0; g4 < 4; ++g4) {
       if (kg == g4) {
+        // per m-tile: load the running sum first (no store -> load chains),
+        // add this key group's scaled slice, store
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          if (mt >= nmt) break;
+        for (int mt = 0; mt < kNMT; ++mt) {
+          float2 prev[2][8];
+          if (g4 > 0) {
 #pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int rr = mt * 16 + qr + hr * 8;
-            const float l = kg_l[rr];
-            const float f = (l > 0.f && mrow[mt][hr] != -INFINITY)
-                                ? exp2f(mrow[mt][hr] - row_w[rr]) / l : 0.f;
+            for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                float* dst = Ob + rr * 128 + dh * 64 + nt * 8 + qc * 2 + e;
-                const float v = o[mt][nt][hr * 2 + e] * f;
-                *dst = g4 == 0 ? v : *dst + v;
-              }
+              for (int nt = 0; nt < 8; ++nt)
+                prev[hr][nt] = *reinterpret_cast<const float2*>(
+                    Ob + (mt * 16 + qr + hr * 8) * kOP + dh * 64 + nt * 8 + qc * 2);
           }
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+              float2 v = make_float2(o[mt][nt][hr * 2] * fac[mt][hr], o[mt][nt][hr * 2 + 1] * fac[mt][hr]);
+              if (g4 > 0) {
+                v.x += prev[hr][nt].x;
+                v.y += prev[hr][nt].y;
+              }
+              *reinterpret_cast<float2*>(Ob + (mt * 16 + qr + hr * 8) * kOP + dh * 64 + nt * 8 + qc * 2) = v;
+            }
         }
       }
       named_bar(1, 256);
@@ -1316,7 +1391,9 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       const int slot = (u >= ps) ? 0 : 1;
       const size_t part = static_cast<size_t>(QRp) * 129;
       float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
-      for (int e = ct; e < QRp * 128; e += 256) mine[e] = Ob[e];
+      for (int e4 = ct; e4 < QRp * 32; e4 += 256)
+        reinterpret_cast<float4*>(mine)[e4] =
+            *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
       for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
       __threadfence();
       named_bar(1, 256);
@@ -1330,22 +1407,24 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       if (flag[0]) {
         __threadfence();
         const int nc = flag[1];
-        // row weights: w_j = 2^(lse_j - max) / sum_k 2^(lse_k - max), all
-        // partials (this CTA's included) read back from the workspace
+        // lse table [nc][QRp] of every partial (this CTA's included), loaded
+        // cooperatively into the idle Q buffer (one round trip), then per-row
+        // weights w_j = 2^(lse_j - max) and 1 / sum_j w_j
+        float* wt = reinterpret_cast<float*>(Qs);
+        for (int e = ct; e < nc * QRp; e += 256) {
+          const int j = e / QRp, rr = e % QRp;
+          wt[e] = __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
+        }
+        named_bar(1, 256);
         for (int rr = ct; rr < QRp; rr += 256) {
           float mx = -INFINITY;
-          for (int j = 0; j < nc; ++j)
-            mx = fmaxf(mx, __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr));
+          for (int j = 0; j < nc; ++j) mx = fmaxf(mx, wt[j * QRp + rr]);
           row_w[rr] = mx;
         }
         named_bar(1, 256);
-        // per-row weight table [nc][QRp] in the (now idle) Q buffer
-        float* wt = reinterpret_cast<float*>(Qs);
-        for (int e = ct; e < nc * QRp && e < QRp * 64; e += 256) {
-          const int j = e / QRp, rr = e % QRp;
-          const float mx = row_w[rr];
-          const float le = __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
-          wt[e] = (mx == -INFINITY) ? 0.f : exp2f(le - mx);
+        for (int e = ct; e < nc * QRp; e += 256) {
+          const float mx = row_w[e % QRp];
+          wt[e] = (mx == -INFINITY) ? 0.f : exp2f(wt[e] - mx);
         }
         named_bar(1, 256);
         for (int rr = ct; rr < QRp; rr += 256) {
@@ -1354,29 +1433,49 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
           cw[rr] = den > 0.f ? 1.f / den : 0.f;
         }
         named_bar(1, 256);
-        for (int e4 = ct; e4 < QRp * 32; e4 += 256) {
-          const int rr = e4 >> 5;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int j0 = 0; j0 < nc; j0 += 8) {
-            float4 v[8];
+        // O = sum_j w_j O_j / sum_j w_j: 4 contributors x 4 float4s in flight
+        const int nel4 = QRp * 32;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 * 256 < nel4; q0 += 4) {
+          float4 acc[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              v[j] = (j0 + j < nc)
-                         ? __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<size_t>(ctb[j0 + j]) * part) + e4)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < 4; ++q) acc[q] = z;
+          for (int j0 = 0; j0 < nc; j0 += 4) {
+            float4 v[4][4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (j0 + j < nc) {
-                const float wgt = wt[(j0 + j) * QRp + rr];
-                acc.x = fmaf(wgt, v[j].x, acc.x);
-                acc.y = fmaf(wgt, v[j].y, acc.y);
-                acc.z = fmaf(wgt, v[j].z, acc.z);
-                acc.w = fmaf(wgt, v[j].w, acc.w);
+            for (int jj = 0; jj < 4; ++jj) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  a.ws + static_cast<size_t>(ctb[j0 + jj < nc ? j0 + jj : 0]) * part);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int e4 = ct + (q0 + q) * 256;
+                v[jj][q] = (j0 + jj < nc && e4 < nel4) ? __ldcg(src + e4) : z;
+              }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              if (j0 + jj >= nc) break;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int e4 = ct + (q0 + q) * 256;
+                const int rr = (e4 < nel4 ? e4 : 0) >> 5;
+                const float wgt = wt[(j0 + jj) * QRp + rr];
+                acc[q].x = fmaf(wgt, v[jj][q].x, acc[q].x);
+                acc[q].y = fmaf(wgt, v[jj][q].y, acc[q].y);
+                acc[q].z = fmaf(wgt, v[jj][q].z, acc[q].z);
+                acc[q].w = fmaf(wgt, v[jj][q].w, acc[q].w);
               }
             }
           }
-          const float inv = cw[rr];
-          reinterpret_cast<float4*>(Ob)[e4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int e4 = ct + (q0 + q) * 256;
+            if (e4 < nel4) {
+              const float inv = cw[e4 >> 5];
+              *reinterpret_cast<float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4) =
+                  make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+            }
+          }
         }
         if (ct == 0) a.pair_cnt[p] = 0u;
         named_bar(1, 256);
@@ -1388,7 +1487,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
         const int t = rr / G, g = rr % G;
         const size_t m = static_cast<size_t>(r) * a.T + t;
         const int hq = h * G + g;
-        const float4 v = *reinterpret_cast<const float4*>(Ob + rr * 128 + lane * 4);
+        const float4 v = *reinterpret_cast<const float4*>(Ob + rr * kOP + lane * 4);
         if (!a.fp8) {
           uint16_t* out = static_cast<uint16_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4;
           *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
