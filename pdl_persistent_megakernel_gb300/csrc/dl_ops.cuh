@@ -1388,7 +1388,9 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     const bool whole = (blk_a == 0 && blk_b == a.NB);
     if (!whole) {
       const long long ps = static_cast<long long>(p) * a.NB;
-      const int slot = (u >= ps) ? 0 : 1;
+      // slot 0: the pair where this CTA's range begins; slot 1: a later pair
+      // (the range's last one), matching sk_contributors
+      const int slot = (u0 >= ps) ? 0 : 1;
       const size_t part = static_cast<size_t>(QRp) * 129;
       float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
       for (int e4 = ct; e4 < QRp * 32; e4 += 256)

@@ -84,9 +84,29 @@ def test_small_layer_all_modes(name, mode):
 def test_small_intermediates(name):
     """Every row of the step against the oracle's intermediates."""
     c = case(name)
-    cfg = c.cfg
     plan = c.plan(modes=1 << dl.MODE_SERIAL)
     out, _ = c.run(plan, dl.MODE_SERIAL)
+    _check_intermediates(c, plan, out)
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["bf16_m4", "bf16_m16", "fp8_m16"])
+@pytest.mark.parametrize("num_sms", [5, 7])
+def test_small_intermediates_ctas_span_pairs(name, num_sms):
+    """With a few CTAs every Stream-K range crosses (request, kv head) pair
+    and GEMM tile boundaries: a CTA leaves one pair's partial and starts the
+    next, so both split-KV workspace slots and multi-contributor fix-ups are
+    exercised."""
+    c = case(name)
+    plan = c.plan(modes=1 << dl.MODE_SERIAL, num_sms=num_sms)
+    out, _ = c.run(plan, dl.MODE_SERIAL)
+    _check_intermediates(c, plan, out)
+    c.check_layer_out(out, f"{name}/sms{num_sms}")
+    plan.close()
+
+
+def _check_intermediates(c, plan, out):
+    cfg = c.cfg
     M, H, I = cfg.M, cfg.hidden, cfg.inter
     QD = cfg.n_q_heads * cfg.head_dim
     bf16_close(as_bf16_np(read_debug(plan, "r1"), (M, H)), c.ref["r1"], "r1")
@@ -115,7 +135,6 @@ def test_small_intermediates(name):
         bf16_close(as_bf16_np(read_debug(plan, "o2"), (M, H)), c.ref["o2"], "o2")
         bf16_close(as_bf16_np(read_debug(plan, "h2"), (M, H)), c.ref["h2"], "h2")
         bf16_close(as_bf16_np(read_debug(plan, "act"), (M, I)), c.ref["act"], "act")
-    plan.close()
 
 
 @pytest.mark.parametrize("name", ["bf16_m1", "fp8_m16", "step_m1"])
@@ -146,4 +165,15 @@ def test_full_size_layer(name, mode):
     out, kv = c.run(plan, mode)
     c.check_layer_out(out, f"{name}/{dl.MODE_NAMES[mode]}")
     c.check_kv(kv, f"{name}/{dl.MODE_NAMES[mode]}")
+    plan.close()
+
+
+@pytest.mark.parametrize("name", ["q06_layer_b1_ctx1024", "q8_layer_m16_ctx8192_fp8"])
+def test_full_size_intermediates(name):
+    """The layer output is dominated by the residual, so it can hide a wrong
+    attention or projection: check every intermediate at full size too."""
+    c = case(name)
+    plan = c.plan(modes=1 << dl.MODE_SERIAL)
+    out, _ = c.run(plan, dl.MODE_SERIAL)
+    _check_intermediates(c, plan, out)
     plan.close()
