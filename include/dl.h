@@ -192,6 +192,51 @@ dl_status dl_plan_debug_perturb_wait(dl_plan* plan, unsigned delta,
 
 void dl_plan_destroy(dl_plan* plan);
 
+/* ------------------------------------------- attention without allocation
+ * The split-KV GQA attention of one layer (per (request, kv head) the keys
+ * are split over CTAs, each partial keeps its row log-sum-exp, and the last
+ * CTA to finish merges them), for callers that may not allocate device
+ * memory where they call it: a framework that owns the device allocator and
+ * forbids foreign allocations, or code running under a memory-pool budget
+ * that is already spent.  The paper has no counterpart of this entry point;
+ * it packages the plans' attention kernel.  It allocates nothing, neither
+ * through CUDA nor through a library: its binding table, status word,
+ * arrival counters and fp32 partials live in one statically reserved 8 MiB
+ * device array, which every GPU that loads the library holds until exit.
+ *
+ *   cfg          only the attention fields are read: n_q_heads, n_kv_heads,
+ *                head_dim (128), n_layers, weight_dtype (FP8 selects e4m3
+ *                output), num_requests, tokens_per_request, page_size,
+ *                num_pages, max_pages_per_request, max_context, num_sms.
+ *   layer        which layer of the cache to attend over.
+ *   q            bf16 [M, n_q_heads, head_dim], after QK-norm and RoPE.
+ *   kv_pages, block_table, positions  as in dl_decode_step; the cache must
+ *                already hold this step's K/V (it is only read here).
+ *   out          bf16 [M, n_q_heads head_dim]; with FP8, e4m3 codes of the
+ *                same shape plus out_scale fp32 [M, n_q_heads head_dim / 128]
+ *                (one scale per token per 128 values; NULL for bf16).
+ *   check        0: asynchronous on `stream`; nonzero: also synchronise the
+ *                stream and report device-side failures (DL_ERR_TIMEOUT,
+ *                DL_ERR_DEVICE_BOUNDS).
+ * Limits: the partials take G x 2 x QRp x 516 bytes of the 8 MiB, where G
+ * is min(num_sms, key blocks) CTAs and QRp is tokens_per_request x group
+ * size rounded up to 16, 32 or 64, and num_requests x n_kv_heads <= 4096.
+ * Larger requests are rejected with DL_ERR_UNSUPPORTED and a message naming
+ * the bytes needed (on a 152-SM GPU, QRp = 64 needs num_sms <= 126).  All
+ * tensor pointers are caller-owned.
+ * Set-up: the first call on a device (made with that device current) looks
+ * up the scratch's device address and sets the kernels' shared-memory
+ * limit; make that first call before any stream capture.
+ * Concurrency: every call on a device uses the same scratch, which keeps the
+ * last call's contents; the call clears what must start at zero.  Calls
+ * whose GPU work may overlap in time (other streams, other threads) race
+ * and corrupt each other's results: order them on one stream or
+ * synchronise. */
+dl_status dl_attention_noalloc(const dl_config* cfg, int layer, const void* q,
+                               const void* kv_pages, const int32_t* block_table,
+                               const int32_t* positions, void* out,
+                               float* out_scale, int check, void* stream);
+
 /* ------------------------------------------------------ test-only exports
  * Bit-exact paged-KV indexing (the slot math of the QKV epilogue and the
  * block-table gather of attention) as pure copies:

@@ -20,7 +20,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libdl.so")
-_SOURCES = ["dl_kernels.cu", "dl_host.cu"]
+_SOURCES = ["dl_kernels.cu", "dl_host.cu", "dl_noalloc.cu"]
 _HEADERS = ["dl_internal.h", "dl_device.cuh", "dl_ops.cuh", "dl_kernels.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -118,7 +118,7 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
            "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
-           "dl_plan_launch_op")
+           "dl_plan_launch_op", "dl_attention_noalloc")
 
 
 def lib(path: Optional[str] = None):
@@ -157,6 +157,8 @@ def lib(path: Optional[str] = None):
         L.dl_plan_op_info.restype = i32
         L.dl_plan_launch_op.argtypes = [vp, i32, vp]
         L.dl_plan_launch_op.restype = i32
+        L.dl_attention_noalloc.argtypes = [C.POINTER(Config), i32] + [vp] * 6 + [i32, vp]
+        L.dl_attention_noalloc.restype = i32
         L.dl_test_kv_write.argtypes = [vp] * 4 + [i32] * 8 + [vp]
         L.dl_test_kv_write.restype = i32
         L.dl_test_kv_gather.argtypes = [vp] * 3 + [i32] * 8 + [vp]
@@ -186,6 +188,28 @@ def _stream_handle(stream) -> Optional[int]:
         import torch
         return torch.cuda.current_stream().cuda_stream
     return getattr(stream, "cuda_stream", stream)
+
+
+def attention_noalloc(cfg, layer: int, q, kv_pages, block_table, positions, out,
+                      out_scale=None, max_context: Optional[int] = None, num_sms: int = 0,
+                      check: bool = True, stream=None):
+    """Split-KV attention of one layer that allocates no device memory (its
+    scratch is a static device array; dl_attention_noalloc in include/dl.h).
+    Meant for callers that may not allocate at the call, such as code whose
+    framework owns the device allocator.  Calls on one device must not
+    overlap in time: they share the scratch."""
+    c = Config()
+    c.n_q_heads, c.n_kv_heads, c.head_dim = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    c.n_layers = cfg.n_layers
+    c.weight_dtype = 1 if cfg.fp8 else 0
+    c.num_requests, c.tokens_per_request = cfg.num_requests, cfg.tokens_per_request
+    c.page_size, c.num_pages = cfg.page_size, cfg.num_pages
+    c.max_pages_per_request = cfg.pages_per_request
+    c.max_context = max_context or cfg.context
+    c.num_sms = num_sms
+    _check(lib().dl_attention_noalloc(C.byref(c), layer, _ptr(q), _ptr(kv_pages),
+                                      _ptr(block_table), _ptr(positions), _ptr(out),
+                                      _ptr(out_scale), int(check), _stream_handle(stream)))
 
 
 class Plan:

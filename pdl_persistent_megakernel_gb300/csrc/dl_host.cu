@@ -28,6 +28,11 @@ static dl_status fail(dl_status s, const std::string& msg) {
 
 extern "C" const char* dl_last_error(void) { return g_err.c_str(); }
 
+// Error reporting for the other translation units of the library.
+namespace dl {
+dl_status set_last_error(dl_status s, const char* msg) { return fail(s, msg); }
+}  // namespace dl
+
 #define CK(call)                                                             \
   do {                                                                       \
     cudaError_t e_ = (call);                                                 \
