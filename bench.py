@@ -21,6 +21,7 @@ value is all ranks' bytes over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -44,6 +45,16 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def kernel_sources_hash():
+    """First 16 hex digits of the SHA-256 over the device sources; a DRAM
+    traffic figure measured under ncu counts only while it matches."""
+    h = hashlib.sha256()
+    for f in ("dl_ops.cuh", "dl_device.cuh", "dl_kernels.cu", "dl_internal.h"):
+        with open(os.path.join(ROOT, "pdl_persistent_megakernel_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def dist_env():
@@ -292,7 +303,8 @@ def main():
     if os.path.exists(tpath):
         try:
             tj = json.load(open(tpath))
-            if tj.get("workload") == cfg.name and tj.get("kernel") == dom:
+            if (tj.get("workload") == cfg.name and tj.get("kernel") == dom
+                    and tj.get("sources_sha256_16") == kernel_sources_hash()):
                 traffic = tj.get("bytes_per_launch")
         except Exception:
             traffic = None
