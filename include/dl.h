@@ -152,6 +152,24 @@ dl_status dl_decode_step_host(dl_plan* plan, const void* x_host,
  * it clears it. */
 dl_status dl_plan_status(dl_plan* plan);
 
+/* Trace build.  A plan created while the environment holds DL_TRACE=1
+ * records, for every CTA share of every operation it runs, %globaltimer
+ * stamps in nanoseconds (the in-kernel timeline the megakernel section of
+ * page "Kernel-Mega-PDL" reads its active-SM curve from):
+ *   [0] share starts  [1] inputs ready  [2] first unit's data consumed
+ *   [3] last unit consumed  [4] share done  [5] work units (a count, not a
+ *   time)  [6] end of the last Stream-K fix-up / split-KV combine the share
+ *   ran (0 if none)  [7] unused.
+ * Table layout: uint64 [n_ops][n_ctas][8]; op i is op i of the serial list
+ * (dl_plan_op_info) in the serial, linear-graph and megakernel schedules,
+ * and node i of the branch list in the DAG schedules.  dl_plan_trace
+ * reports the dimensions (either pointer may be NULL); with host_buf it
+ * synchronises the device, copies the table (bytes >= n_ops * n_ctas * 64)
+ * and clears it.  DL_ERR_UNSUPPORTED for a plan created without tracing.
+ * Tracing costs one predicated branch per stamp when off. */
+dl_status dl_plan_trace(dl_plan* plan, void* host_buf, size_t bytes,
+                        int* n_ops, int* n_ctas);
+
 /* fp32 logits [M, vocab] of the last full step (device pointer), or NULL. */
 const float* dl_plan_logits(dl_plan* plan);
 

@@ -118,7 +118,7 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
            "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
-           "dl_plan_launch_op", "dl_attention_noalloc")
+           "dl_plan_launch_op", "dl_attention_noalloc", "dl_plan_trace")
 
 
 def lib(path: Optional[str] = None):
@@ -157,6 +157,8 @@ def lib(path: Optional[str] = None):
         L.dl_plan_op_info.restype = i32
         L.dl_plan_launch_op.argtypes = [vp, i32, vp]
         L.dl_plan_launch_op.restype = i32
+        L.dl_plan_trace.argtypes = [vp, vp, C.c_size_t, C.POINTER(i32), C.POINTER(i32)]
+        L.dl_plan_trace.restype = i32
         L.dl_attention_noalloc.argtypes = [C.POINTER(Config), i32] + [vp] * 6 + [i32, vp]
         L.dl_attention_noalloc.restype = i32
         L.dl_test_kv_write.argtypes = [vp] * 4 + [i32] * 8 + [vp]
@@ -269,6 +271,16 @@ class Plan:
         p, n = C.c_void_p(), C.c_size_t()
         _check(lib().dl_plan_debug_buffer(self._h, DEBUG_BUFFERS[name], C.byref(p), C.byref(n)))
         return p.value, n.value
+
+    def trace(self):
+        """Trace table uint64 [ops, ctas, 8] (plan created with DL_TRACE=1);
+        reading it clears it."""
+        import numpy as np
+        n_ops, n_ctas = C.c_int(), C.c_int()
+        _check(lib().dl_plan_trace(self._h, None, 0, C.byref(n_ops), C.byref(n_ctas)))
+        buf = np.zeros((n_ops.value, n_ctas.value, 8), dtype=np.uint64)
+        _check(lib().dl_plan_trace(self._h, buf.ctypes.data, buf.nbytes, None, None))
+        return buf
 
     def logits_ptr(self) -> Optional[int]:
         return lib().dl_plan_logits(self._h)

@@ -35,6 +35,17 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------------------------------ trace
+// Trace build: %globaltimer stamp (or a value) of share c of the current op.
+__device__ __forceinline__ void trace_put(const KernelCtx& ctx, int c, int slot,
+                                          unsigned long long v) {
+  if (ctx.trace && c < ctx.trace_ctas)
+    ctx.trace[(static_cast<size_t>(ctx.op_id) * ctx.trace_ctas + c) * kTraceSlots + slot] = v;
+}
+__device__ __forceinline__ void trace_stamp(const KernelCtx& ctx, int c, int slot) {
+  if (ctx.trace) trace_put(ctx, c, slot, globaltimer());
+}
+
 // ------------------------------------------------------------- status word
 __device__ __forceinline__ void report_error(DevStatus* st, unsigned code,
                                              unsigned op, unsigned cta,

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -115,6 +116,8 @@ struct dl_plan {
   std::vector<void*> allocs;
   Binding* d_binding = nullptr;
   DevStatus* d_status = nullptr;
+  unsigned long long* d_trace = nullptr;  // trace build: [trace_ops][sms][kTraceSlots]
+  int trace_ops = 0;
   void *h1 = nullptr, *attn = nullptr, *h2 = nullptr, *act = nullptr;
   float *h1s = nullptr, *attns = nullptr, *h2s = nullptr, *acts = nullptr;
   void *r1 = nullptr, *r2 = nullptr, *o2 = nullptr, *y = nullptr, *q = nullptr;
@@ -192,6 +195,8 @@ static KernelCtx make_ctx(const dl_plan* p, int op_id) {
   c.status = p->d_status;
   c.budget_ns = p->budget_ns;
   c.op_id = op_id;
+  c.trace = p->d_trace;
+  c.trace_ctas = p->sms;
   return c;
 }
 
@@ -807,6 +812,15 @@ static dl_status build_plan(dl_plan* p) {
   CK(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
   CK(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
 
+  // trace build (DL_TRACE=1 in the environment at creation)
+  {
+    const char* tr = std::getenv("DL_TRACE");
+    if (tr && tr[0] == '1' && tr[1] == 0) {
+      p->trace_ops = static_cast<int>(std::max(p->lin.size(), p->dag.size()));
+      DA(p->d_trace, static_cast<size_t>(p->trace_ops) * p->sms * kTraceSlots * 8);
+    }
+  }
+
   // e2e staging buffers
   DA(p->st_x, MH2);
   DA(p->st_res, MH2);
@@ -969,6 +983,22 @@ extern "C" dl_status dl_plan_status(dl_plan* p) {
 }
 
 extern "C" const float* dl_plan_logits(dl_plan* p) { return p ? p->logits : nullptr; }
+
+extern "C" dl_status dl_plan_trace(dl_plan* p, void* host_buf, size_t bytes, int* n_ops,
+                                   int* n_ctas) {
+  if (!p) return fail(DL_ERR_INVALID_ARG, "plan is NULL");
+  if (!p->d_trace) return fail(DL_ERR_UNSUPPORTED, "plan was created without DL_TRACE=1");
+  if (n_ops) *n_ops = p->trace_ops;
+  if (n_ctas) *n_ctas = p->sms;
+  if (!host_buf) return DL_OK;
+  const size_t need = static_cast<size_t>(p->trace_ops) * p->sms * kTraceSlots * 8;
+  if (bytes < need) return fail(DL_ERR_INVALID_ARG, "trace buffer too small");
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(host_buf, p->d_trace, need, cudaMemcpyDeviceToHost));
+  CK(cudaMemset(p->d_trace, 0, need));
+  CK(cudaDeviceSynchronize());
+  return DL_OK;
+}
 
 extern "C" dl_status dl_plan_debug_buffer(dl_plan* p, int which, void** ptr, size_t* bytes) {
   if (!p || !ptr || !bytes) return fail(DL_ERR_INVALID_ARG, "NULL argument");

@@ -196,11 +196,25 @@ struct MegaArgs {
   unsigned* trace;            // optional [workers][qlen][4] (start, ready, done)
 };
 
+// Trace build: per (operation, CTA share) kTraceSlots u64 entries.
+enum TraceSlot : int {
+  TR_START = 0,       // the share's engine starts (after its barrier set-up)
+  TR_DEPS = 1,        // its inputs are ready (griddepcontrol / event counters)
+  TR_FIRST = 2,       // the first unit's data has reached the consumers
+  TR_LOOP_END = 3,    // the last unit of the last run has been consumed
+  TR_END = 4,         // the share is done (fix-up / combine / epilogue included)
+  TR_UNITS = 5,       // value: work units of the share
+  TR_REDUCE = 6,      // the last Stream-K fix-up / split-KV combine it ran ended
+  kTraceSlots = 8
+};
+
 struct KernelCtx {
   const Binding* binding;
   DevStatus* status;
   unsigned long long budget_ns;   // bounded-wait budget
-  int op_id;                      // for error reports
+  int op_id;                      // for error reports (and the trace row)
+  int trace_ctas = 0;             // shares per trace row
+  unsigned long long* trace = nullptr;  // [ops][trace_ctas][kTraceSlots] or NULL
 };
 
 }  // namespace dl

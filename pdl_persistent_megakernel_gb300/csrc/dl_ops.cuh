@@ -115,6 +115,7 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     return;
   }
   const int ct = tid - 32, lane = tid & 31, wc = ct >> 5;
+  if (ct == 0) trace_stamp(ctx, c, TR_START);
   float* red = reinterpret_cast<float*>(smem);     // [2][8]
   int* sflag = reinterpret_cast<int*>(smem + 128);
   const int H = a.H, nvec = H >> 3;
@@ -126,6 +127,7 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     wv[j] = (ct + j * 256 < nvec) ? __ldg(reinterpret_cast<const uint4*>(w + (ct + j * 256) * 8))
                                   : make_uint4(0, 0, 0, 0);
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag)) return;
+  if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
   const Binding* bd = ctx.binding;
   const uint16_t* x = resolve<const uint16_t>(a.x, bd);
   const uint16_t* res = resolve<const uint16_t>(a.res, bd);
@@ -212,6 +214,10 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
         }
       }
     }
+  }
+  if (ct == 0) {
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(m1 > m0 ? m1 - m0 : 0));
+    trace_stamp(ctx, c, TR_END);
   }
 }
 
@@ -557,7 +563,10 @@ __device__ void gemm_finish_tile(const GemmArgs& a, int c, long long u0, int tl,
     // CTA order: the sum does not depend on which CTA arrived last
     ordered_sum4(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb,
                  sh.flag[3], nel / 4, nthr, ct);
-    if (ct == 0) a.tile_cnt[tl] = 0u;
+    if (ct == 0) {
+      a.tile_cnt[tl] = 0u;
+      trace_stamp(ctx, c, TR_REDUCE);
+    }
     named_bar(bar, nthr);
   }
   const int tg = a.t_base + tl;
@@ -676,6 +685,8 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
     sh.flag[2] = 1;
     fence_barrier_init();
+    trace_stamp(ctx, c, TR_START);
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
   }
   __syncthreads();
 
@@ -701,6 +712,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
         tma_load_2d(st + 16384, a.tmap_w, &sh.full[i], kb * kel, a.up_row + t * 128, pw);
     }
     bool ok = single_wait(dep, ctx, 10);
+    trace_stamp(ctx, c, TR_DEPS);
     // activations of the prefetched stages (issued even after a failed wait
     // so that every armed stage completes and can be drained)
     for (int i = 0; i < pre; ++i) {
@@ -765,6 +777,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       for (int k = 0; k < run; ++k, ++i) {
         const int s = i % S;
         if (!dead) dead = !warp_wait(&sh.full[s], (i / S) & 1, ctx, 13);
+        if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
         const uint8_t* st = sh.stage0 + s * L.stage_bytes;
         const uint8_t* xs = st + npair * 16384;
@@ -830,9 +843,11 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
             if (c8 == 0 && m < a.M) sh.tout[(p * a.Mp + m) * 128 + r0 + 32 * j] = v;
           }
       }
+      if (ct == 0 && i == nunits) trace_stamp(ctx, c, TR_LOOP_END);
       if (named_bar_or(1, 256, dead)) return;
       gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 256, ct, 1, ctx, sh);
     }
+    if (ct == 0) trace_stamp(ctx, c, TR_END);
   } else {
     // --------------------------------------------- tcgen05 (M > 4, N = kMp)
     const int ncols = npair * kMp;  // TMEM columns per accumulator buffer
@@ -905,6 +920,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       for (int k = 0; k < run; ++k, ++i) {
         const int b = i % NTB;
         if (!dead) dead = !warp_wait(&sh.tfull[b], (i / NTB) & 1, ctx, 17);
+        if (i == 0 && et == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
         tc_fence_after();
 #pragma unroll
@@ -940,9 +956,11 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
         for (int m = 0; m < kMp; ++m)
           if (m < a.M) sh.tout[(p * a.Mp + m) * 128 + row] = acc[p][m];
       }
+      if (et == 0 && i == nunits) trace_stamp(ctx, c, TR_LOOP_END);
       if (named_bar_or(2, 128, dead)) return;
       gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, sh);
     }
+    if (et == 0) trace_stamp(ctx, c, TR_END);
   }
 }
 
@@ -1053,6 +1071,8 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     flag[0] = flag[1] = 0;
     flag[2] = 1;
     fence_barrier_init();
+    trace_stamp(ctx, c, TR_START);
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(u1 - u0));
   }
   __syncthreads();
 
@@ -1068,6 +1088,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0) {
+      trace_stamp(ctx, c, TR_DEPS);
       fence_tmap_acquire(kvm);
       prefetch_tmap(kvm);
     }
@@ -1201,6 +1222,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     for (int blk = blk_a; blk < min(blk_b, nvb); ++blk, ++i) {
       const int s = i % S;
       if (!dead) dead = !warp_wait(&full[s], (i / S) & 1, ctx, 35);
+      if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
       uint8_t* st = stage0 + s * L.stage_bytes;
       const uint32_t kb_u32 = smem_u32(st), vb_u32 = smem_u32(st + 2 * kAttnKeys * 128);
       const int k0 = blk * kAttnKeys;
@@ -1385,6 +1407,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       }
       named_bar(1, 256);
     }
+    if (ct == 0) trace_stamp(ctx, c, TR_LOOP_END);
     const bool whole = (blk_a == 0 && blk_b == a.NB);
     if (!whole) {
       const long long ps = static_cast<long long>(p) * a.NB;
@@ -1479,7 +1502,10 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
             }
           }
         }
-        if (ct == 0) a.pair_cnt[p] = 0u;
+        if (ct == 0) {
+          a.pair_cnt[p] = 0u;
+          trace_stamp(ctx, c, TR_REDUCE);
+        }
         named_bar(1, 256);
       }
     }
@@ -1508,6 +1534,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     named_bar(1, 256);
     u = run_end;
   }
+  if (ct == 0) trace_stamp(ctx, c, TR_END);
 }
 
 __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
