@@ -629,125 +629,105 @@ __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShar
   named_bar(bar, nthr);
 }
 
+// ------------------------------------------------------------ pipelines
+// Where the operands of a pipeline's units live and how they are handed
+// over.  A standalone kernel owns a ring of `ns` stages, one per unit (a
+// GEMM unit's weight tile(s) and activation slice side by side, an
+// attention block's K then V), spu = 1.  The streaming megakernel has one
+// ring of `ns` equal slots shared by all instructions of a worker and filled
+// in queue order by its producer warp: a GEMM unit takes npair slots (the
+// first one also holds the activation slice), an attention block two (K,
+// V), and seq0 is the ring sequence number of the share's first slot.
+struct Pipe {
+  uint8_t* base;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t slot_bytes;
+  uint32_t ns;
+  uint32_t seq0;
+  int spu;          // slots per unit
+  int empty_cnt;    // arrivals that free a slot (1: one MMA commit; 8: 8 warps)
+};
+
+__device__ __forceinline__ uint32_t pipe_seq(const Pipe& P, int i, int j) {
+  return P.seq0 + static_cast<uint32_t>(i * P.spu + j);
+}
+__device__ __forceinline__ uint8_t* pipe_slot(const Pipe& P, uint32_t q) {
+  return P.base + (q % P.ns) * P.slot_bytes;
+}
+__device__ __forceinline__ uint64_t* pipe_full(const Pipe& P, uint32_t q) { return P.full + q % P.ns; }
+__device__ __forceinline__ uint64_t* pipe_empty(const Pipe& P, uint32_t q) { return P.empty + q % P.ns; }
+__device__ __forceinline__ uint32_t pipe_par(const Pipe& P, uint32_t q) { return (q / P.ns) & 1u; }
+
+// GEMM unit i: weight tile p (gate / up, or the single tile) and the
+// activation slice.
+__device__ __forceinline__ uint8_t* gemm_w(const Pipe& P, int i, int p) {
+  return P.spu == 1 ? pipe_slot(P, pipe_seq(P, i, 0)) + p * 16384 : pipe_slot(P, pipe_seq(P, i, p));
+}
+__device__ __forceinline__ uint8_t* gemm_x(const Pipe& P, int i, int npair) {
+  return pipe_slot(P, pipe_seq(P, i, 0)) + (P.spu == 1 ? npair : 1) * 16384;
+}
+
+// A warp waits until every slot of unit i is full (all lanes poll, the warp
+// agrees); false if a wait gave up.
+__device__ __forceinline__ bool pipe_warp_wait(const Pipe& P, int i, const KernelCtx& ctx,
+                                               unsigned where) {
+  for (int j = 0; j < P.spu; ++j) {
+    const uint32_t q = pipe_seq(P, i, j);
+    if (!warp_wait(pipe_full(P, q), pipe_par(P, q), ctx, where)) return false;
+  }
+  return true;
+}
+
+// TMEM accumulator ring of the tcgen05 path: buffer b of nbuf at column
+// base + b * stride; seq0 counts the accumulations before this share.
+struct TmemRing {
+  uint32_t base;
+  int nbuf;
+  int stride;
+  uint32_t seq0;
+};
+
 // ------------------------------------------------------------ GEMM engine
 // kMG: GEMV token bound (1/2/4, CUDA cores); kMp: tcgen05 N (16/32/64).
 // Exactly one of them is non-zero.
 //
-// Roles.  Warp 0 lane 0 streams the weight tile(s) and the activation slice
-// of each unit into a ring of `stages` shared-memory stages (TMA, 128-byte
-// swizzle); before its first dependent read it issues the weights of the
-// first stages (they do not depend on the previous operation).
-//   GEMV (M <= 4): warps 1-8 each take 16 rows of a stage, 8 lanes per row.
+// Roles.  The producer (warp 0 lane 0 of a standalone kernel, or the
+// megakernel's producer warp) streams the weight tile(s) and the activation
+// slice of each unit into the pipeline (TMA, 128-byte swizzle); before its
+// first dependent read it issues the weights of the first units (they do not
+// depend on the previous operation).
+//   GEMV (M <= 4): warps 1-8 each take 16 rows of a unit, 8 lanes per row.
 //   tcgen05 (M > 4): warp 1 lane 0 issues 4 MMAs (K = 32 bytes each) per
-//   unit into a ring of TMEM accumulators; warps 5-8 read each unit's
+//   weight tile into a ring of TMEM accumulators; warps 5-8 read each unit's
 //   accumulator (TMEM lane quarter = warp % 4), apply the FP8 block scales
 //   and accumulate the tile in registers.
 // Waits are per warp (all lanes poll, the warp agrees); a failed wait marks
 // the warp dead, it skips work but keeps the barrier sequence, and the group
 // agrees on failure with one OR-barrier per tile run.
+//
+// gemm_consume_t is the consumer side (warps 1-8); gemm_op_t wraps it with
+// the standalone kernel's own stages and producer.
 template <int kMG, int kMp>
-__device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
-                          const KernelCtx& ctx, uint8_t* smem,
-                          uint32_t tmem_base) {
+__device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
+                               const KernelCtx& ctx, const GemmShared& sh,
+                               const Pipe& P, const TmemRing& TR) {
   constexpr bool kMMA = kMp > 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npair = a.pair ? 2 : 1;
-  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M);
-  GemmShared sh;
-  sh.stage0 = smem;
-  sh.tout = reinterpret_cast<float*>(smem + L.tile_off);
-  sh.sx = reinterpret_cast<float*>(smem + L.sx_off);
-  sh.sw = reinterpret_cast<float*>(smem + L.sw_off);
-  sh.tok_pos = reinterpret_cast<int*>(smem + L.epi_off);
-  sh.tok_row = sh.tok_pos + a.M;
-  sh.rope = reinterpret_cast<float2*>(smem + L.epi_off + a.M * 8);
-  sh.full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  sh.empty = sh.full + kMaxStages;
-  sh.tfull = sh.empty + kMaxStages;
-  sh.tempty = sh.tfull + kMaxTmemBufs;
-  sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
-  sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
   const long long U = static_cast<long long>(a.NT) * a.KB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const int nunits = static_cast<int>(u1 - u0);
-  const int S = a.stages;
-  const int NTB = kMMA ? a.tmem_bufs : 1;
-  const int kel = a.fp8 ? 128 : 64;  // elements per k-block
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], kMMA ? 1 : 8);
-    }
-    for (int b = 0; b < kMaxTmemBufs; ++b) {
-      mbar_init(&sh.tfull[b], 1);
-      mbar_init(&sh.tempty[b], 4);
-    }
-    sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
-    sh.flag[2] = 1;
-    fence_barrier_init();
-    trace_stamp(ctx, c, TR_START);
-    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    // ------------------------------------------------------- producer
-    if (lane != 0) {
-      idle_wait(dep);
-      return;
-    }
-    prefetch_tmap(a.tmap_w);
-    prefetch_tmap(a.tmap_x);
-    const uint32_t tx = npair * 16384 + a.Mp * 128;
-    const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-    const int pre = min(S, nunits);
-    // weights of the first stages do not depend on the previous op
-    for (int i = 0; i < pre; ++i) {
-      const long long u = u0 + i;
-      const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
-      uint8_t* st = sh.stage0 + i * L.stage_bytes;
-      mbar_arrive_expect_tx(&sh.full[i], tx);
-      tma_load_2d(st, a.tmap_w, &sh.full[i], kb * kel, t * 128, pw);
-      if (a.pair)
-        tma_load_2d(st + 16384, a.tmap_w, &sh.full[i], kb * kel, a.up_row + t * 128, pw);
-    }
-    bool ok = single_wait(dep, ctx, 10);
-    trace_stamp(ctx, c, TR_DEPS);
-    // activations of the prefetched stages (issued even after a failed wait
-    // so that every armed stage completes and can be drained)
-    for (int i = 0; i < pre; ++i) {
-      const int kb = static_cast<int>((u0 + i) % a.KB);
-      tma_load_2d(sh.stage0 + i * L.stage_bytes + npair * 16384, a.tmap_x, &sh.full[i],
-                  kb * kel, 0, px);
-    }
-    int issued = pre;
-    if (ok) {
-      for (int i = pre; i < nunits; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(&sh.empty[s], ((i / S) - 1) & 1, ctx, 11)) break;
-        const long long u = u0 + i;
-        const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
-        uint8_t* st = sh.stage0 + s * L.stage_bytes;
-        mbar_arrive_expect_tx(&sh.full[s], tx);
-        tma_load_2d(st, a.tmap_w, &sh.full[s], kb * kel, t * 128, pw);
-        if (a.pair)
-          tma_load_2d(st + 16384, a.tmap_w, &sh.full[s], kb * kel, a.up_row + t * 128, pw);
-        tma_load_2d(st + npair * 16384, a.tmap_x, &sh.full[s], kb * kel, 0, px);
-        issued = i + 1;
-      }
-    }
-    // no copy may be in flight when the CTA leaves
-    for (int s = 0; s < S && s < issued; ++s) {
-      const int last = s + ((issued - 1 - s) / S) * S;  // last unit issued to stage s
-      mbar_drain(&sh.full[s], (last / S) & 1, ctx.budget_ns);
-    }
-    return;
-  }
 
   if constexpr (!kMMA) {
     // ----------------------------------------------- CUDA-core GEMV (M <= 4)
     const int ct = tid - 32;
+    if (ct == 0) {
+      trace_stamp(ctx, c, TR_START);
+      trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
+    }
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
+    if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 256, ct, 1);
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
     const int c8 = ct & 7, r0 = ct >> 3;
@@ -775,12 +755,10 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
           for (int m = 0; m < kMG; ++m) acc[p][j][m] = 0.f;
       for (int k = 0; k < run; ++k, ++i) {
-        const int s = i % S;
-        if (!dead) dead = !warp_wait(&sh.full[s], (i / S) & 1, ctx, 13);
+        if (!dead) dead = !pipe_warp_wait(P, i, ctx, 13);
         if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
-        const uint8_t* st = sh.stage0 + s * L.stage_bytes;
-        const uint8_t* xs = st + npair * 16384;
+        const uint8_t* xs = gemm_x(P, i, npair);
         uint4 xv[kMG];
 #pragma unroll
         for (int m = 0; m < kMG; ++m)
@@ -789,11 +767,11 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             if (p >= npair) break;
+            const uint8_t* wt = gemm_w(P, i, p);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int r = r0 + 32 * j;
-              const uint4 wv = *reinterpret_cast<const uint4*>(
-                  st + p * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4));
+              const uint4 wv = *reinterpret_cast<const uint4*>(wt + r * 128 + ((c8 ^ (r & 7)) << 4));
 #pragma unroll
               for (int m = 0; m < kMG; ++m) acc[p][j][m] += dot8_bf16(wv, xv[m]);
             }
@@ -806,12 +784,12 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             if (p >= npair) break;
+            const uint8_t* wt = gemm_w(P, i, p);
             const float sw = sh.sw[p * run + k];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int r = r0 + 32 * j;
-              const uint4 wv = *reinterpret_cast<const uint4*>(
-                  st + p * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4));
+              const uint4 wv = *reinterpret_cast<const uint4*>(wt + r * 128 + ((c8 ^ (r & 7)) << 4));
               float wf[16];
               unpack_e4m3x16(wv, wf);
 #pragma unroll
@@ -826,7 +804,8 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.empty[s]);
+        if (lane == 0)
+          for (int j = 0; j < P.spu; ++j) mbar_arrive(pipe_empty(P, pipe_seq(P, i, j)));
       }
       // reduce the 8 lanes that share a row, store the tile sum
 #pragma unroll
@@ -850,38 +829,52 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     if (ct == 0) trace_stamp(ctx, c, TR_END);
   } else {
     // --------------------------------------------- tcgen05 (M > 4, N = kMp)
-    const int ncols = npair * kMp;  // TMEM columns per accumulator buffer
     if (warp == 1) {
       idle_wait(dep);
       if (lane == 0) {
+        trace_stamp(ctx, c, TR_START);
+        trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
         int issued = 0;
         for (int i = 0; i < nunits; ++i) {
-          const int s = i % S, b = i % NTB;
-          if (!mbar_wait(&sh.full[s], (i / S) & 1, ctx, 14)) break;
-          if (i >= NTB && !mbar_wait(&sh.tempty[b], ((i / NTB) - 1) & 1, ctx, 15)) break;
+          bool ok = true;
+          for (int j = 0; j < P.spu && ok; ++j) {
+            const uint32_t q = pipe_seq(P, i, j);
+            ok = mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 14);
+          }
+          if (!ok) break;
+          const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
+          const int b = static_cast<int>(tq % TR.nbuf);
+          if (tq >= static_cast<uint32_t>(TR.nbuf) &&
+              !mbar_wait(&sh.tempty[b], ((tq / TR.nbuf) - 1) & 1, ctx, 15))
+            break;
           tc_fence_after();
-          const uint32_t sa = smem_u32(sh.stage0 + s * L.stage_bytes);
+          const uint32_t sb = smem_u32(gemm_x(P, i, npair));
           for (int p = 0; p < npair; ++p) {
-            const uint32_t d = tmem_base + b * ncols + p * kMp;
+            const uint32_t d = TR.base + b * TR.stride + p * kMp;
+            const uint32_t sa = smem_u32(gemm_w(P, i, p));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = umma_desc_sw128(sa + p * 16384 + k * 32);
-              const uint64_t bd = umma_desc_sw128(sa + npair * 16384 + k * 32);
+              const uint64_t ad = umma_desc_sw128(sa + k * 32);
+              const uint64_t bd = umma_desc_sw128(sb + k * 32);
               if (a.fp8)
                 umma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
               else
                 umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
             }
           }
-          umma_commit(&sh.empty[s]);
+          for (int j = 0; j < P.spu; ++j) {
+            uint64_t* e = pipe_empty(P, pipe_seq(P, i, j));
+            umma_commit(e);
+            if (P.empty_cnt > 1) mbar_arrive_cnt(e, static_cast<uint32_t>(P.empty_cnt - 1));
+          }
           umma_commit(&sh.tfull[b]);
           issued = i + 1;
         }
         // no MMA may still read shared memory or write TMEM when we leave
         if (issued > 0) {
-          const int l = issued - 1;
-          mbar_drain(&sh.tfull[l % NTB], (l / NTB) & 1, ctx.budget_ns);
+          const uint32_t l = TR.seq0 + static_cast<uint32_t>(issued - 1);
+          mbar_drain(&sh.tfull[l % TR.nbuf], (l / TR.nbuf) & 1, ctx.budget_ns);
         }
       }
       return;
@@ -895,6 +888,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     const int q = warp & 3;
     const int row = q * 32 + lane;
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
+    if (et == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
     bool dead = false;
@@ -918,8 +912,9 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
         for (int m = 0; m < kMp; ++m) acc[p][m] = 0.f;
       for (int k = 0; k < run; ++k, ++i) {
-        const int b = i % NTB;
-        if (!dead) dead = !warp_wait(&sh.tfull[b], (i / NTB) & 1, ctx, 17);
+        const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
+        const int b = static_cast<int>(tq % TR.nbuf);
+        if (!dead) dead = !warp_wait(&sh.tfull[b], (tq / TR.nbuf) & 1, ctx, 17);
         if (i == 0 && et == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
         tc_fence_after();
@@ -930,7 +925,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 #pragma unroll
           for (int c16 = 0; c16 < kMp / 16; ++c16) {
             float v[16];
-            tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * ncols + p * kMp + c16 * 16, v);
+            tmem_ld16(TR.base + (static_cast<uint32_t>(q * 32) << 16) + b * TR.stride + p * kMp + c16 * 16, v);
             tmem_wait_ld();
             if (a.fp8) {
 #pragma unroll
@@ -962,6 +957,127 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     }
     if (et == 0) trace_stamp(ctx, c, TR_END);
   }
+}
+
+// Shared-memory pointers of a GEMM share: operand stages at smem (standalone,
+// `stages` of them) and the private area after them.
+__device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* smem, int stages) {
+  const int npair = a.pair ? 2 : 1;
+  const GemmSmem L = gemm_smem_layout(npair, a.Mp, stages, a.KB, a.fp8, a.epi, a.M);
+  GemmShared sh;
+  sh.stage0 = smem;
+  sh.tout = reinterpret_cast<float*>(smem + L.tile_off);
+  sh.sx = reinterpret_cast<float*>(smem + L.sx_off);
+  sh.sw = reinterpret_cast<float*>(smem + L.sw_off);
+  sh.tok_pos = reinterpret_cast<int*>(smem + L.epi_off);
+  sh.tok_row = sh.tok_pos + a.M;
+  sh.rope = reinterpret_cast<float2*>(smem + L.epi_off + a.M * 8);
+  sh.full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  sh.empty = sh.full + kMaxStages;
+  sh.tfull = sh.empty + kMaxStages;
+  sh.tempty = sh.tfull + kMaxTmemBufs;
+  sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
+  sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
+  return sh;
+}
+
+// Standalone GEMM share: its own stages, barriers and producer (warp 0).
+template <int kMG, int kMp>
+__device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
+                          const KernelCtx& ctx, uint8_t* smem,
+                          uint32_t tmem_base) {
+  constexpr bool kMMA = kMp > 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int npair = a.pair ? 2 : 1;
+  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M);
+  const GemmShared sh = gemm_shared(a, smem, a.stages);
+  const long long U = static_cast<long long>(a.NT) * a.KB;
+  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int nunits = static_cast<int>(u1 - u0);
+  const int S = a.stages;
+  const int kel = a.fp8 ? 128 : 64;  // elements per k-block
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kMMA ? 1 : 8);
+    }
+    for (int b = 0; b < kMaxTmemBufs; ++b) {
+      mbar_init(&sh.tfull[b], 1);
+      mbar_init(&sh.tempty[b], 4);
+    }
+    sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
+    sh.flag[2] = 1;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------- producer
+    if (lane != 0) {
+      idle_wait(dep);
+      return;
+    }
+    prefetch_tmap(a.tmap_w);
+    prefetch_tmap(a.tmap_x);
+    const uint32_t tx = npair * 16384 + a.Mp * 128;
+    const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+    const int pre = min(S, nunits);
+    // weights of the first stages do not depend on the previous op
+    for (int i = 0; i < pre; ++i) {
+      const long long u = u0 + i;
+      const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
+      uint8_t* st = sh.stage0 + i * L.stage_bytes;
+      mbar_arrive_expect_tx(&sh.full[i], tx);
+      tma_load_2d(st, a.tmap_w, &sh.full[i], kb * kel, t * 128, pw);
+      if (a.pair)
+        tma_load_2d(st + 16384, a.tmap_w, &sh.full[i], kb * kel, a.up_row + t * 128, pw);
+    }
+    bool ok = single_wait(dep, ctx, 10);
+    // activations of the prefetched stages (issued even after a failed wait
+    // so that every armed stage completes and can be drained)
+    for (int i = 0; i < pre; ++i) {
+      const int kb = static_cast<int>((u0 + i) % a.KB);
+      tma_load_2d(sh.stage0 + i * L.stage_bytes + npair * 16384, a.tmap_x, &sh.full[i],
+                  kb * kel, 0, px);
+    }
+    int issued = pre;
+    if (ok) {
+      for (int i = pre; i < nunits; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&sh.empty[s], ((i / S) - 1) & 1, ctx, 11)) break;
+        const long long u = u0 + i;
+        const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
+        uint8_t* st = sh.stage0 + s * L.stage_bytes;
+        mbar_arrive_expect_tx(&sh.full[s], tx);
+        tma_load_2d(st, a.tmap_w, &sh.full[s], kb * kel, t * 128, pw);
+        if (a.pair)
+          tma_load_2d(st + 16384, a.tmap_w, &sh.full[s], kb * kel, a.up_row + t * 128, pw);
+        tma_load_2d(st + npair * 16384, a.tmap_x, &sh.full[s], kb * kel, 0, px);
+        issued = i + 1;
+      }
+    }
+    // no copy may be in flight when the CTA leaves
+    for (int s = 0; s < S && s < issued; ++s) {
+      const int last = s + ((issued - 1 - s) / S) * S;  // last unit issued to stage s
+      mbar_drain(&sh.full[s], (last / S) & 1, ctx.budget_ns);
+    }
+    return;
+  }
+  Pipe P;
+  P.base = sh.stage0;
+  P.full = sh.full;
+  P.empty = sh.empty;
+  P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
+  P.ns = static_cast<uint32_t>(S);
+  P.seq0 = 0;
+  P.spu = 1;
+  P.empty_cnt = kMMA ? 1 : 8;
+  TmemRing TR;
+  TR.base = tmem_base;
+  TR.nbuf = kMMA ? a.tmem_bufs : 1;
+  TR.stride = npair * (kMMA ? kMp : 0);
+  TR.seq0 = 0;
+  gemm_consume_t<kMG, kMp>(a, c, dep, ctx, sh, P, TR);
 }
 
 // ============================================================== ATTENTION
@@ -1034,15 +1150,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // and lse_i, and the last CTA of the pair combines
 //   lse = log sum_i e^{lse_i},  O = sum_i e^{lse_i - lse} O_i
 // over the partials in CTA order (deterministic).
+// Attention block i of a pipeline: K (d 0-63 | d 64-127), then V.
+__device__ __forceinline__ uint8_t* attn_k(const Pipe& P, int i) {
+  return pipe_slot(P, pipe_seq(P, i, 0));
+}
+__device__ __forceinline__ uint8_t* attn_v(const Pipe& P, int i) {
+  return P.spu == 1 ? attn_k(P, i) + 2 * kAttnKeys * 128 : pipe_slot(P, pipe_seq(P, i, 1));
+}
+
+// Consumer side of an attention share (warps 1-8): `priv` is the share's
+// private shared memory (layout attn_smem_layout(QRp, 0)).  Returns the
+// number of key blocks it consumed (the blocks below each pair's context),
+// or -1 after a failed wait.
 template <int kNMT>
-__device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
-                          const KernelCtx& ctx, uint8_t* smem) {
+__device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
+                              const KernelCtx& ctx, uint8_t* priv, const Pipe& P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QRp = a.QRp, G = a.Hq / a.Hkv;
   constexpr int nmt = kNMT;
   constexpr int kXS = nmt * 8;   // partial-score floats per thread
-  const AttnSmem L = attn_smem_layout(QRp, a.stages);
-  uint8_t* stage0 = smem;
+  const AttnSmem L = attn_smem_layout(QRp, 0);
+  uint8_t* smem = priv;
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q_off);
   float* Ob = reinterpret_cast<float*>(smem + L.o_off);
   float* xs = reinterpret_cast<float*>(smem + L.xs_off);
@@ -1051,126 +1179,21 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   float* row_lse = kg_l + 4 * QRp;
   float* row_w = row_lse + QRp;
   int* row_pos = reinterpret_cast<int*>(row_w + QRp);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* empty = full + kMaxStages;
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
-  int* pgbuf = flag + 16;                 // [32][4] pages of the producer's batch
-  int* ppos = pgbuf + 32 * 4;             // [64] token positions (producer)
-  int* ctb = ppos + 64;                   // [kMaxContrib] combine contributors
+  int* ctb = flag + 16 + 32 * 4 + 64;     // [kMaxContrib] combine contributors
   float* cw = reinterpret_cast<float*>(ctb + kMaxContrib);  // [kMaxContrib] weights
-  const int S = a.stages;
   const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
-  const CUtensorMap* kvm = &bd->kv_map;
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
-    }
-    flag[0] = flag[1] = 0;
-    flag[2] = 1;
-    fence_barrier_init();
-    trace_stamp(ctx, c, TR_START);
-    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(u1 - u0));
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    // ------------------------------------------ producer (warp 0, lane 0 issues)
-    bool ok = true;
-    if (dep.mode == 0) {
-      gdc_wait();
-      gdc_launch_dependents();
-      ok = !aborted(ctx.status);
-    } else {
-      if (lane == 0) ok = poll_deps(dep, ctx, 30);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    }
-    if (lane == 0) {
-      trace_stamp(ctx, c, TR_DEPS);
-      fence_tmap_acquire(kvm);
-      prefetch_tmap(kvm);
-    }
-    const int* pos = resolve<const int>(a.pos, bd);
-    const int* bt = resolve<const int>(a.bt, bd);
-    const int M = a.R * a.T;
-    for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
-    __syncwarp();
-    const uint64_t pol = policy_evict_first();
-    const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
-    const int npg = kAttnKeys / box;                      // boxes per 64-key unit
-    const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
-    int i = 0;
-    for (long long ub = u0; ok && ub < u1; ub += 32) {
-      const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
-      // the batch's page numbers, loaded by the whole warp
-      for (int e = lane; e < nb * npg; e += 32) {
-        const int j = e / npg, q = e % npg;
-        const long long u = ub + j;
-        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
-        const int r = p / a.Hkv;
-        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
-        const int key = blk * kAttnKeys + q * box;
-        const int lp = key / a.P;
-        pgbuf[j * 4 + q] = (key < ctxr && lp < a.max_pages)
-                               ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        for (int j = 0; j < nb && ok; ++j) {
-          const long long u = ub + j;
-          const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
-          const int r = p / a.Hkv, h = p % a.Hkv;
-          const int ctxr = ppos[r * a.T + a.T - 1] + 1;
-          const int k0 = blk * kAttnKeys;
-          if (k0 >= ctxr) continue;
-          const int s = i % S;
-          if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = stage0 + s * L.stage_bytes;
-          const int nk = min(kAttnKeys, ctxr - k0);
-          const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
-          mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
-          for (int q = 0; q < nbox; ++q) {
-            const int key = k0 + q * box;
-            int page = pgbuf[j * 4 + q];
-            if (page < 0 || page >= a.num_pages) {
-              report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, key / a.P);
-              page = 0;
-            }
-            const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
-            const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
-            uint8_t* dq = st + q * box * 128;
-            tma_load_2d(dq, kvm, &full[s], 0, rk, pol);
-            tma_load_2d(dq + half, kvm, &full[s], 64, rk, pol);
-            tma_load_2d(dq + 2 * half, kvm, &full[s], 0, rv, pol);
-            tma_load_2d(dq + 3 * half, kvm, &full[s], 64, rv, pol);
-          }
-          ++i;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      i = __shfl_sync(0xffffffffu, i, 0);
-      __syncwarp();
-    }
-    if (lane == 0) {
-      const int issued = i;
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / S) * S;
-        mbar_drain(&full[s], (last / S) & 1, ctx.budget_ns);
-      }
-    }
-    return;
-  }
-
-  // ---------------------------------------------------------- consumers
   const int ct = tid - 32, wc = warp - 1;  // wc: 0..7
   const int kg = wc & 3, dh = wc >> 2;     // key group, head-dim half
   const int partner = kg + 4 * (1 - dh);
-  if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return;
+  if (ct == 0) {
+    trace_stamp(ctx, c, TR_START);
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(u1 - u0));
+  }
+  if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return -1;
+  if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
   const int* pos = resolve<const int>(a.pos, bd);
   const uint16_t* qg = static_cast<const uint16_t*>(a.q);
   const uint32_t qs_u32 = smem_u32(Qs);
@@ -1220,11 +1243,11 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     }
     const int nvb = (ctxr + kAttnKeys - 1) / kAttnKeys;   // valid blocks
     for (int blk = blk_a; blk < min(blk_b, nvb); ++blk, ++i) {
-      const int s = i % S;
-      if (!dead) dead = !warp_wait(&full[s], (i / S) & 1, ctx, 35);
+      if (!dead) dead = !pipe_warp_wait(P, i, ctx, 35);
       if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
-      uint8_t* st = stage0 + s * L.stage_bytes;
-      const uint32_t kb_u32 = smem_u32(st), vb_u32 = smem_u32(st + 2 * kAttnKeys * 128);
+      uint8_t* kst = attn_k(P, i);
+      uint8_t* vst = attn_v(P, i);
+      const uint32_t kb_u32 = smem_u32(kst), vb_u32 = smem_u32(vst);
       const int k0 = blk * kAttnKeys;
       const int nk = min(kAttnKeys, ctxr - k0);
       float* xbuf = xs + (i & 1) * (8 * kXS * 32);
@@ -1239,7 +1262,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
         if (nk < kAttnKeys) {
           // keys past the context were not loaded (or hold stale data): zero
           // this warp's V rows so that 0-probability keys contribute exactly 0
-          uint8_t* vh = st + (2 + dh) * kAttnKeys * 128;
+          uint8_t* vh = vst + dh * kAttnKeys * 128;
           for (int e = lane; e < 16 * 8; e += 32) {
             const int key = kg * 16 + (e >> 3);
             if (key >= nk) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
@@ -1342,11 +1365,12 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
         }
         if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0)
+          for (int j = 0; j < P.spu; ++j) mbar_arrive(pipe_empty(P, pipe_seq(P, i, j)));
       }
     }
     // ---- merge the four key groups (fixed order) into Ob, then lse
-    if (named_bar_or(1, 256, dead)) return;
+    if (named_bar_or(1, 256, dead)) return -1;
     if (dh == 0 && qc == 0) {
 #pragma unroll
       for (int mt = 0; mt < kNMT; ++mt) {
@@ -1535,6 +1559,150 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     u = run_end;
   }
   if (ct == 0) trace_stamp(ctx, c, TR_END);
+  return i;
+}
+
+
+template <int kNMT>
+__device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
+                          const KernelCtx& ctx, uint8_t* smem) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int QRp = a.QRp, G = a.Hq / a.Hkv;
+  constexpr int nmt = kNMT;
+  constexpr int kXS = nmt * 8;   // partial-score floats per thread
+  const AttnSmem L = attn_smem_layout(QRp, a.stages);
+  uint8_t* stage0 = smem;
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q_off);
+  float* Ob = reinterpret_cast<float*>(smem + L.o_off);
+  float* xs = reinterpret_cast<float*>(smem + L.xs_off);
+  float* kg_m = reinterpret_cast<float*>(smem + L.stat_off);   // [4][QRp]
+  float* kg_l = kg_m + 4 * QRp;                                 // [4][QRp]
+  float* row_lse = kg_l + 4 * QRp;
+  float* row_w = row_lse + QRp;
+  int* row_pos = reinterpret_cast<int*>(row_w + QRp);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + kMaxStages;
+  int* flag = reinterpret_cast<int*>(smem + L.misc_off);
+  int* pgbuf = flag + 16;                 // [32][4] pages of the producer's batch
+  int* ppos = pgbuf + 32 * 4;             // [64] token positions (producer)
+  int* ctb = ppos + 64;                   // [kMaxContrib] combine contributors
+  float* cw = reinterpret_cast<float*>(ctb + kMaxContrib);  // [kMaxContrib] weights
+  const int S = a.stages;
+  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
+  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const Binding* bd = ctx.binding;
+  const CUtensorMap* kvm = &bd->kv_map;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 8);
+    }
+    flag[0] = flag[1] = 0;
+    flag[2] = 1;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------ producer (warp 0, lane 0 issues)
+    bool ok = true;
+    if (dep.mode == 0) {
+      gdc_wait();
+      gdc_launch_dependents();
+      ok = !aborted(ctx.status);
+    } else {
+      if (lane == 0) ok = poll_deps(dep, ctx, 30);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
+      fence_tmap_acquire(kvm);
+      prefetch_tmap(kvm);
+    }
+    const int* pos = resolve<const int>(a.pos, bd);
+    const int* bt = resolve<const int>(a.bt, bd);
+    const int M = a.R * a.T;
+    for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
+    const int npg = kAttnKeys / box;                      // boxes per 64-key unit
+    const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
+    int i = 0;
+    for (long long ub = u0; ok && ub < u1; ub += 32) {
+      const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
+      // the batch's page numbers, loaded by the whole warp
+      for (int e = lane; e < nb * npg; e += 32) {
+        const int j = e / npg, q = e % npg;
+        const long long u = ub + j;
+        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+        const int r = p / a.Hkv;
+        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+        const int key = blk * kAttnKeys + q * box;
+        const int lp = key / a.P;
+        pgbuf[j * 4 + q] = (key < ctxr && lp < a.max_pages)
+                               ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        for (int j = 0; j < nb && ok; ++j) {
+          const long long u = ub + j;
+          const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+          const int r = p / a.Hkv, h = p % a.Hkv;
+          const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+          const int k0 = blk * kAttnKeys;
+          if (k0 >= ctxr) continue;
+          const int s = i % S;
+          if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = stage0 + s * L.stage_bytes;
+          const int nk = min(kAttnKeys, ctxr - k0);
+          const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
+          mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
+          for (int q = 0; q < nbox; ++q) {
+            const int key = k0 + q * box;
+            int page = pgbuf[j * 4 + q];
+            if (page < 0 || page >= a.num_pages) {
+              report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, key / a.P);
+              page = 0;
+            }
+            const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
+            const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
+            uint8_t* dq = st + q * box * 128;
+            tma_load_2d(dq, kvm, &full[s], 0, rk, pol);
+            tma_load_2d(dq + half, kvm, &full[s], 64, rk, pol);
+            tma_load_2d(dq + 2 * half, kvm, &full[s], 0, rv, pol);
+            tma_load_2d(dq + 3 * half, kvm, &full[s], 64, rv, pol);
+          }
+          ++i;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      i = __shfl_sync(0xffffffffu, i, 0);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      const int issued = i;
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / S) * S;
+        mbar_drain(&full[s], (last / S) & 1, ctx.budget_ns);
+      }
+    }
+    return;
+  }
+
+
+  Pipe P;
+  P.base = stage0;
+  P.full = full;
+  P.empty = empty;
+  P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
+  P.ns = static_cast<uint32_t>(S);
+  P.seq0 = 0;
+  P.spu = 1;
+  P.empty_cnt = 8;
+  attn_consume_t<kNMT>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
 }
 
 __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
