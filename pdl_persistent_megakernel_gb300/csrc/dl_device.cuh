@@ -108,20 +108,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// How often a waiting thread looks at the abort flag and the budget.  The
+// flag lives in global memory: reading it on every pass would make the wait
+// return no sooner than one memory round trip after the phase completes,
+// which under a saturated HBM is a microsecond or more.
+constexpr unsigned long long kCheckNs = 20000;
+
 // Wait for the phase with the given parity to complete; false on timeout or
 // when another thread raised the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const KernelCtx& ctx, unsigned where) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
+  unsigned long long check = t0 + kCheckNs;
   for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (aborted(ctx.status)) return false;
-    if (globaltimer() - t0 > ctx.budget_ns) {
-      report_error(ctx.status, DERR_TIMEOUT, ctx.op_id, blockIdx.x, where,
-                   parity);
-      return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t = globaltimer();
+    if (t >= check) {
+      if (aborted(ctx.status)) return false;
+      if (t - t0 > ctx.budget_ns) {
+        report_error(ctx.status, DERR_TIMEOUT, ctx.op_id, blockIdx.x, where, parity);
+        return false;
+      }
+      check = t + kCheckNs;
     }
   }
 }
@@ -262,16 +271,17 @@ __device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned value,
                                              unsigned where) {
   if (ld_acquire_gpu(p) >= value) return true;
   const unsigned long long t0 = globaltimer();
+  unsigned long long check = t0 + kCheckNs;
   for (;;) {
-    for (int i = 0; i < 8; ++i) {
-      __nanosleep(32);
-      if (ld_acquire_gpu(p) >= value) return true;
-    }
-    if (aborted(ctx.status)) return false;
-    if (globaltimer() - t0 > ctx.budget_ns) {
-      report_error(ctx.status, DERR_TIMEOUT, ctx.op_id, blockIdx.x, where,
-                   value);
-      return false;
+    if (ld_acquire_gpu(p) >= value) return true;
+    const unsigned long long t = globaltimer();
+    if (t >= check) {
+      if (aborted(ctx.status)) return false;
+      if (t - t0 > ctx.budget_ns) {
+        report_error(ctx.status, DERR_TIMEOUT, ctx.op_id, blockIdx.x, where, value);
+        return false;
+      }
+      check = t + kCheckNs;
     }
   }
 }

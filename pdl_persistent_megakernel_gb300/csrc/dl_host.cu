@@ -142,6 +142,7 @@ struct dl_plan {
   unsigned* d_finish = nullptr;
   std::vector<Instr> queues;
   int qlen = 0, workers = 0, n_events = 0, mega_smem = 0;
+  int mega_ns = 0, mega_slot = 0, mega_priv_off = 0;
 
   cudaGraphExec_t exec[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   cudaStream_t cap = nullptr, side = nullptr;
@@ -269,10 +270,13 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   const long long U = static_cast<long long>(a.NT) * a.KB;
   a.G = static_cast<int>(std::min<long long>(p->sms, U));
   const int npair = s.pair ? 2 : 1;
-  const int stage_bytes = npair * 16384 + ((a.Mp * 128 + 1023) / 1024) * 1024;
+  // a stage: 32 KiB of tiles (gate + up, or two consecutive units) and one
+  // activation slice per unit
+  const int stage_bytes = 32768 + (npair == 1 ? 2 : 1) * (((a.Mp * 128 + 1023) / 1024) * 1024);
   const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0, a.KB, a.fp8, s.epi, a.M);
-  // one CTA per SM: a deep ring keeps ~200 KB of weights in flight per SM
-  a.stages = choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget);
+  // one CTA per SM; 3-4 stages of 32 KiB in flight per SM already reach the
+  // HBM copy rate, a few more absorb jitter
+  a.stages = std::min(5, choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget));
   a.tmem_bufs = a.mma ? std::min(4, 512 / (npair * a.Mp)) : 1;
   a.epi = s.epi;
   a.ws = p->ws_gemm[s.ws_slot];
@@ -554,6 +558,9 @@ static cudaError_t launch_mega(dl_plan* p, cudaStream_t s) {
   m.num_events = p->n_events;
   m.budget_ns = p->budget_ns;
   m.trace = nullptr;
+  m.ns = p->mega_ns;
+  m.slot_bytes = p->mega_slot;
+  m.priv_off = p->mega_priv_off;
   KernelCtx ctx = make_ctx(p, -1);
   void* args[] = {&m, &ctx};
   return cudaLaunchKernelExC(&lc, mega_kernel(), args);
@@ -832,7 +839,30 @@ static dl_status build_plan(dl_plan* p) {
   if (c.modes_mask & (1u << DL_MODE_MEGAKERNEL)) {
     if ((s = build_mega(p)) != DL_OK) return s;
     if ((s = validate_mega(p)) != DL_OK) return s;
-    p->mega_smem = max_smem;
+    // the worker's ring of equal operand slots (32 KiB of weight tiles or
+    // K/V plus the activation slices) and the largest private area
+    int slot = 32768, priv = norm_smem_bytes();
+    for (const LaunchOp& op : p->lin) {
+      if (op.args.kind == OP_GEMM) {
+        const GemmArgs& a = op.args.gemm;
+        slot = std::max(slot, 32768 + (a.pair ? 1 : 2) * (((a.Mp * 128 + 1023) / 1024) * 1024));
+        priv = std::max(priv, gemm_smem_bytes(a.pair ? 2 : 1, a.Mp, 0, a.KB, a.fp8, a.epi, a.M));
+      } else if (op.args.kind == OP_ATTN) {
+        priv = std::max(priv, attn_smem_bytes(op.args.attn.QRp, 0));
+      }
+    }
+    priv = (priv + 1023) & ~1023;
+    cudaFuncAttributes fa;
+    CK(cudaFuncGetAttributes(&fa, mega_kernel()));
+    int optin = 0;
+    CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->dev));
+    const int avail = optin - static_cast<int>(fa.sharedSizeBytes) - 1024 - priv;
+    p->mega_ns = std::min(kMaxSlots, avail / slot);
+    if (p->mega_ns < 4) return fail(DL_ERR_PLAN_INVALID, "megakernel ring has fewer than 4 slots");
+    p->mega_slot = slot;
+    p->mega_priv_off = p->mega_ns * slot;
+    p->mega_smem = 1024 + p->mega_priv_off + priv;
+    (void)max_smem;
     CK(cudaFuncSetAttribute(mega_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                             p->mega_smem));
     int per_sm = 0;

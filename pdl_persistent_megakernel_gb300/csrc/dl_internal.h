@@ -25,6 +25,7 @@ constexpr int kMaxM = 64;            // tokens per step
 constexpr int kAttnKeys = 64;        // keys per attention pipeline stage
 constexpr int kMaxQRows = 64;        // query rows per (request, kv head)
 constexpr int kMaxStages = 12;
+constexpr int kMaxSlots = 16;        // operand slots of a megakernel worker's ring
 
 // ----------------------------------------------------- runtime bindings
 // Pointers supplied per decode call (the caller's tensors).  Kernels read
@@ -194,6 +195,12 @@ struct MegaArgs {
   int num_events;
   unsigned long long budget_ns;
   unsigned* trace;            // optional [workers][qlen][4] (start, ready, done)
+  // the worker's shared memory: a ring of `ns` slots of `slot_bytes` at
+  // offset 0 (operands, filled by the producer warp in queue order), then
+  // the consumers' private area at `priv_off`
+  int ns;
+  int slot_bytes;
+  int priv_off;
 };
 
 // Trace build: per (operation, CTA share) kTraceSlots u64 entries.
@@ -205,6 +212,7 @@ enum TraceSlot : int {
   TR_END = 4,         // the share is done (fix-up / combine / epilogue included)
   TR_UNITS = 5,       // value: work units of the share
   TR_REDUCE = 6,      // the last Stream-K fix-up / split-KV combine it ran ended
+  TR_PDEPS = 7,       // megakernel: its producer warp saw the inputs ready
   kTraceSlots = 8
 };
 

@@ -104,42 +104,43 @@ __global__ void k_test_kv_gather(const uint16_t* kv, const int* bt, uint16_t* ds
 }
 
 // ------------------------------------------------------------ megakernel
-// Runs one GEMM instruction with the variant its arguments call for.
-__device__ void mega_gemm(const GemmArgs& a, int c, const Dep& dep,
-                          const KernelCtx& ctx, uint8_t* smem, uint32_t tmem) {
-  if (!a.mma) {
-    if (a.M <= 1)
-      gemm_op_t<1, 0>(a, c, dep, ctx, smem, tmem);
-    else if (a.M <= 2)
-      gemm_op_t<2, 0>(a, c, dep, ctx, smem, tmem);
-    else
-      gemm_op_t<4, 0>(a, c, dep, ctx, smem, tmem);
-  } else {
-    if (a.Mp <= 16)
-      gemm_op_t<0, 16>(a, c, dep, ctx, smem, tmem);
-    else if (a.Mp <= 32)
-      gemm_op_t<0, 32>(a, c, dep, ctx, smem, tmem);
-    else
-      gemm_op_t<0, 64>(a, c, dep, ctx, smem, tmem);
-  }
-}
-
-// One worker CTA per SM walks its host-built queue.  Before an instruction's
-// dependent reads it acquire-polls the event counters the instruction names
-// (weights are prefetched first); after it, thread 0 publishes with a
-// release add.  Instructions only wait on earlier instructions of a global
-// topological order and all workers are co-resident (cooperative launch), so
-// the earliest unfinished instruction can always run.
+// One worker CTA per SM walks its host-built queue.  Warp 0 is the producer:
+// it runs ahead of the other warps across instruction boundaries and fills
+// the worker's ring of operand slots in the order they will be consumed
+// (weights at once, dependent data once the instruction's event counters
+// are reached).  Warps 1-8 consume instruction after instruction: before
+// an instruction's dependent reads they acquire-poll the event counters it
+// names; after it, one thread publishes with a release add.  Instructions
+// only wait on earlier instructions of a global topological order and all
+// workers are co-resident (cooperative launch), so the earliest unfinished
+// instruction can always run; the producer never blocks on a slot that only
+// the consumption of its own pending (dependent) loads could free.
 __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(16) Instr ins;
   __shared__ __align__(16) OpArgs op;
   __shared__ int stop;
+  __shared__ __align__(8) uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
+  __shared__ __align__(8) uint64_t tm_full[4], tm_empty[4];
+  __shared__ int p_pgbuf[32 * 4], p_ppos[kMaxM];
   uint8_t* smem = align1024(smem_raw);
-  const int tid = threadIdx.x;
+  uint8_t* priv = smem + m.priv_off;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kTmemCols = 512;   // one worker per SM owns all of TMEM
-  if ((tid >> 5) == 1) {
+  if (tid == 0) {
+    for (int s = 0; s < m.ns; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 8);
+    }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&tm_full[b], 1);
+      mbar_init(&tm_empty[b], 4);
+    }
+    stop = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
     tmem_alloc(&tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -147,61 +148,141 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  Pipe R;
+  R.base = smem;
+  R.full = ring_full;
+  R.empty = ring_empty;
+  R.slot_bytes = static_cast<uint32_t>(m.slot_bytes);
+  R.ns = static_cast<uint32_t>(m.ns);
+  R.seq0 = 0;
+  R.ups = 1;
+  R.x_bytes = 0;
+  R.empty_cnt = 8;
   const Instr* q = m.queues + static_cast<size_t>(blockIdx.x) * m.qlen;
-  for (int pc = 0; pc < m.qlen; ++pc) {
-    if (tid < 32) reinterpret_cast<uint32_t*>(&ins)[tid] = __ldg(reinterpret_cast<const uint32_t*>(q + pc) + tid);
-    __syncthreads();
-    if (ins.op_row == 0xffffffffu) break;   // NoOp padding: the queue is done
-    for (int i = tid; i < static_cast<int>(sizeof(OpArgs) / 4); i += kThreads)
-      reinterpret_cast<uint32_t*>(&op)[i] = __ldg(reinterpret_cast<const uint32_t*>(m.ops + ins.op_row) + i);
-    __syncthreads();
-    Dep dep{};
-    dep.mode = 1;
-    dep.n = static_cast<int>(ins.n_wait);
-    for (int i = 0; i < dep.n && i < 4; ++i) {
-      dep.ev[i] = m.events + ins.wait_event[i];
-      dep.val[i] = ins.wait_value[i];
-    }
-    KernelCtx c2 = ctx;
-    c2.op_id = static_cast<int>(ins.op_row);
-    if (m.trace && tid == 0)
-      m.trace[(static_cast<size_t>(blockIdx.x) * m.qlen + pc) * 4 + 0] =
-          static_cast<unsigned>(globaltimer());
-    switch (op.kind) {
-      case OP_NORM:
-        norm_op(op.norm, static_cast<int>(ins.cta), dep, c2, smem);
-        break;
-      case OP_GEMM:
-        mega_gemm(op.gemm, static_cast<int>(ins.cta), dep, c2, smem, tmem);
-        break;
-      case OP_ATTN:
-        attn_op(op.attn, static_cast<int>(ins.cta), dep, c2, smem);
-        break;
-      default:
-        if (tid == 0) report_error(ctx.status, DERR_BAD_OP, ins.op_row, blockIdx.x, 40, op.kind);
-        break;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const bool ab = aborted(ctx.status);
-      if (!ab) {
-        fence_proxy_async_global();
-        __threadfence();
-        for (uint32_t s = 0; s < ins.n_signal && s < 2; ++s)
-          red_release_gpu_add(m.events + ins.signal_event[s], ins.signal_inc[s]);
+
+  if (warp == 0) {
+    // --------------------------------------------------------- producer
+    uint32_t seq = 0, hi = 0;
+    bool ok = true;
+    for (int pc = 0; pc < m.qlen && ok; ++pc) {
+      const Instr* in = q + pc;
+      const uint32_t row = __ldg(&in->op_row);
+      if (row == 0xffffffffu) break;
+      const OpArgs* oa = m.ops + row;
+      const int kind = __ldg(&oa->kind);
+      Dep dep{};
+      dep.mode = 1;
+      dep.n = static_cast<int>(__ldg(&in->n_wait));
+      for (int i = 0; i < dep.n && i < 4; ++i) {
+        dep.ev[i] = m.events + __ldg(&in->wait_event[i]);
+        dep.val[i] = __ldg(&in->wait_value[i]);
       }
-      stop = ab ? 1 : 0;
-      if (m.trace)
-        m.trace[(static_cast<size_t>(blockIdx.x) * m.qlen + pc) * 4 + 2] =
-            static_cast<unsigned>(globaltimer());
+      KernelCtx c2 = ctx;
+      c2.op_id = static_cast<int>(row);
+      const int cta = static_cast<int>(__ldg(&in->cta));
+      if (kind == OP_GEMM) {
+        const GemmArgs& ga = oa->gemm;
+        if (lane == 0) ok = mk_produce_gemm(ga, cta, dep, c2, R, seq, &hi);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int ups = ga.pair ? 1 : 2;
+        seq += static_cast<uint32_t>((gemm_share_units(ga, cta) + ups - 1) / ups);
+      } else if (kind == OP_ATTN) {
+        int nv = 0;
+        ok = mk_produce_attn(oa->attn, cta, dep, c2, R, seq, p_pgbuf, p_ppos, &nv, &hi);
+        seq += static_cast<uint32_t>(nv);
+      }
+      if (aborted(ctx.status)) ok = false;
+      __syncwarp();
     }
-    __syncthreads();
-    if (stop) break;
+    // no copy may be in flight when the worker leaves
+    if (lane == 0) {
+      const uint32_t lo = hi > R.ns ? hi - R.ns : 0u;
+      for (uint32_t s = lo; s < hi; ++s)
+        mbar_drain(pipe_full(R, s), pipe_par(R, s), ctx.budget_ns);
+    }
+  } else {
+    // ------------------------------------------------------- consumers
+    const int ct = tid - 32;
+    uint32_t seq = 0, tseq = 0;
+    for (int pc = 0; pc < m.qlen; ++pc) {
+      if (ct < 32) reinterpret_cast<uint32_t*>(&ins)[ct] = __ldg(reinterpret_cast<const uint32_t*>(q + pc) + ct);
+      named_bar(1, 256);
+      if (ins.op_row == 0xffffffffu) break;   // NoOp padding: the queue is done
+      for (int i = ct; i < static_cast<int>(sizeof(OpArgs) / 4); i += 256)
+        reinterpret_cast<uint32_t*>(&op)[i] = __ldg(reinterpret_cast<const uint32_t*>(m.ops + ins.op_row) + i);
+      named_bar(1, 256);
+      Dep dep{};
+      dep.mode = 1;
+      dep.n = static_cast<int>(ins.n_wait);
+      for (int i = 0; i < dep.n && i < 4; ++i) {
+        dep.ev[i] = m.events + ins.wait_event[i];
+        dep.val[i] = ins.wait_value[i];
+      }
+      KernelCtx c2 = ctx;
+      c2.op_id = static_cast<int>(ins.op_row);
+      const int cta = static_cast<int>(ins.cta);
+      if (m.trace && ct == 0)
+        m.trace[(static_cast<size_t>(blockIdx.x) * m.qlen + pc) * 4 + 0] =
+            static_cast<unsigned>(globaltimer());
+      bool fail = false;
+      switch (op.kind) {
+        case OP_NORM:
+          mk_norm(op.norm, cta, dep, c2, priv);
+          break;
+        case OP_GEMM: {
+          const int ups = op.gemm.pair ? 1 : 2;
+          Pipe P = R;
+          P.seq0 = seq;
+          P.ups = ups;
+          P.x_bytes = ((op.gemm.Mp * 128 + 1023) / 1024) * 1024;
+          TmemRing TR;
+          TR.base = tmem;
+          TR.nbuf = 4;
+          TR.stride = 128;
+          TR.seq0 = tseq;
+          mk_gemm(op.gemm, cta, dep, c2, priv, P, TR, tm_full, tm_empty);
+          const int n = gemm_share_units(op.gemm, cta);
+          seq += static_cast<uint32_t>((n + ups - 1) / ups);
+          if (op.gemm.mma) tseq += static_cast<uint32_t>(n);
+          break;
+        }
+        case OP_ATTN: {
+          Pipe P = R;
+          P.seq0 = seq;
+          P.ups = 1;
+          const int nv = mk_attn(op.attn, cta, dep, c2, priv, P);
+          if (nv < 0)
+            fail = true;
+          else
+            seq += static_cast<uint32_t>(nv);
+          break;
+        }
+        default:
+          if (ct == 0) report_error(ctx.status, DERR_BAD_OP, ins.op_row, blockIdx.x, 40, op.kind);
+          break;
+      }
+      named_bar(1, 256);
+      if (ct == 0) {
+        const bool ab = fail || aborted(ctx.status);
+        if (!ab) {
+          fence_proxy_async_global();
+          __threadfence();
+          for (uint32_t s = 0; s < ins.n_signal && s < 2; ++s)
+            red_release_gpu_add(m.events + ins.signal_event[s], ins.signal_inc[s]);
+        }
+        stop = ab ? 1 : 0;
+        if (m.trace)
+          m.trace[(static_cast<size_t>(blockIdx.x) * m.qlen + pc) * 4 + 2] =
+              static_cast<unsigned>(globaltimer());
+      }
+      named_bar(1, 256);
+      if (stop) break;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if ((tid >> 5) == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   // the last worker out zeroes the event counters for the next step
   if (tid == 0) {
     __threadfence();

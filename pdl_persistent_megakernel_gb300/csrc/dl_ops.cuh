@@ -240,7 +240,9 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   GemmSmem L;
   L.w_bytes = 16384;
   L.x_bytes = ((Mp * 128 + 1023) / 1024) * 1024;
-  L.stage_bytes = npair * L.w_bytes + L.x_bytes;
+  // 32 KiB of tiles (gate + up, or two consecutive units), then one
+  // activation slice per unit
+  L.stage_bytes = 2 * L.w_bytes + (npair == 1 ? 2 : 1) * L.x_bytes;
   L.tile_off = stages * L.stage_bytes;
   L.sx_off = L.tile_off + npair * Mp * 128 * 4;
   L.sw_off = L.sx_off + (fp8 ? KB * Mp * 4 : 0);
@@ -631,13 +633,16 @@ __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShar
 
 // ------------------------------------------------------------ pipelines
 // Where the operands of a pipeline's units live and how they are handed
-// over.  A standalone kernel owns a ring of `ns` stages, one per unit (a
-// GEMM unit's weight tile(s) and activation slice side by side, an
-// attention block's K then V), spu = 1.  The streaming megakernel has one
-// ring of `ns` equal slots shared by all instructions of a worker and filled
-// in queue order by its producer warp: a GEMM unit takes npair slots (the
-// first one also holds the activation slice), an attention block two (K,
-// V), and seq0 is the ring sequence number of the share's first slot.
+// over.  Every slot holds 32 KiB of weight tiles or K/V, then activation
+// slices: a GEMM slot holds the gate and up tiles of one unit, or, without
+// gate/up pairing, the tiles of two consecutive units (ups = 2), each with
+// its activation slice; an attention slot holds one 64-key block (K, then
+// V).  Streaming two adjacent 128-byte k-blocks of the same weight rows at
+// once runs near the HBM copy rate, one at a time about a quarter slower.
+// A standalone kernel owns a ring of `ns` slots; the streaming megakernel
+// has one ring for all instructions of a worker, filled in queue order by
+// its producer warp, and seq0 is the ring sequence number of the share's
+// first slot.
 struct Pipe {
   uint8_t* base;
   uint64_t* full;
@@ -645,12 +650,15 @@ struct Pipe {
   uint32_t slot_bytes;
   uint32_t ns;
   uint32_t seq0;
-  int spu;          // slots per unit
+  int ups;          // units per slot
+  int x_bytes;      // bytes of one unit's activation slice (after the tiles)
   int empty_cnt;    // arrivals that free a slot (1: one MMA commit; 8: 8 warps)
 };
 
-__device__ __forceinline__ uint32_t pipe_seq(const Pipe& P, int i, int j) {
-  return P.seq0 + static_cast<uint32_t>(i * P.spu + j);
+constexpr int kSlotTiles = 32768;   // bytes of weight tiles / K+V per slot
+
+__device__ __forceinline__ uint32_t pipe_q(const Pipe& P, int i) {
+  return P.seq0 + static_cast<uint32_t>(i / P.ups);
 }
 __device__ __forceinline__ uint8_t* pipe_slot(const Pipe& P, uint32_t q) {
   return P.base + (q % P.ns) * P.slot_bytes;
@@ -658,25 +666,26 @@ __device__ __forceinline__ uint8_t* pipe_slot(const Pipe& P, uint32_t q) {
 __device__ __forceinline__ uint64_t* pipe_full(const Pipe& P, uint32_t q) { return P.full + q % P.ns; }
 __device__ __forceinline__ uint64_t* pipe_empty(const Pipe& P, uint32_t q) { return P.empty + q % P.ns; }
 __device__ __forceinline__ uint32_t pipe_par(const Pipe& P, uint32_t q) { return (q / P.ns) & 1u; }
+// unit i of n is the last one of its slot: the slot is released after it
+__device__ __forceinline__ bool pipe_last(const Pipe& P, int i, int n) {
+  return (i % P.ups) == P.ups - 1 || i == n - 1;
+}
 
 // GEMM unit i: weight tile p (gate / up, or the single tile) and the
 // activation slice.
 __device__ __forceinline__ uint8_t* gemm_w(const Pipe& P, int i, int p) {
-  return P.spu == 1 ? pipe_slot(P, pipe_seq(P, i, 0)) + p * 16384 : pipe_slot(P, pipe_seq(P, i, p));
+  return pipe_slot(P, pipe_q(P, i)) + ((i % P.ups) + p) * 16384;
 }
-__device__ __forceinline__ uint8_t* gemm_x(const Pipe& P, int i, int npair) {
-  return pipe_slot(P, pipe_seq(P, i, 0)) + (P.spu == 1 ? npair : 1) * 16384;
+__device__ __forceinline__ uint8_t* gemm_x(const Pipe& P, int i) {
+  return pipe_slot(P, pipe_q(P, i)) + kSlotTiles + (i % P.ups) * P.x_bytes;
 }
 
-// A warp waits until every slot of unit i is full (all lanes poll, the warp
-// agrees); false if a wait gave up.
+// A warp waits until unit i's slot is full (all lanes poll, the warp agrees);
+// false if the wait gave up.
 __device__ __forceinline__ bool pipe_warp_wait(const Pipe& P, int i, const KernelCtx& ctx,
                                                unsigned where) {
-  for (int j = 0; j < P.spu; ++j) {
-    const uint32_t q = pipe_seq(P, i, j);
-    if (!warp_wait(pipe_full(P, q), pipe_par(P, q), ctx, where)) return false;
-  }
-  return true;
+  const uint32_t q = pipe_q(P, i);
+  return warp_wait(pipe_full(P, q), pipe_par(P, q), ctx, where);
 }
 
 // TMEM accumulator ring of the tcgen05 path: buffer b of nbuf at column
@@ -726,10 +735,12 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       trace_stamp(ctx, c, TR_START);
       trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
     }
+    // the QKV epilogue's operands (positions, cache rows, RoPE rows) are
+    // step inputs: load them before the dependency wait
+    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
     if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 256, ct, 1);
-    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
     const int c8 = ct & 7, r0 = ct >> 3;
     bool dead = false;
     int i = 0;
@@ -758,7 +769,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         if (!dead) dead = !pipe_warp_wait(P, i, ctx, 13);
         if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
-        const uint8_t* xs = gemm_x(P, i, npair);
+        const uint8_t* xs = gemm_x(P, i);
         uint4 xv[kMG];
 #pragma unroll
         for (int m = 0; m < kMG; ++m)
@@ -804,8 +815,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           }
         }
         __syncwarp();
-        if (lane == 0)
-          for (int j = 0; j < P.spu; ++j) mbar_arrive(pipe_empty(P, pipe_seq(P, i, j)));
+        if (lane == 0 && pipe_last(P, i, nunits)) mbar_arrive(pipe_empty(P, pipe_q(P, i)));
       }
       // reduce the 8 lanes that share a row, store the tile sum
 #pragma unroll
@@ -829,53 +839,62 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     if (ct == 0) trace_stamp(ctx, c, TR_END);
   } else {
     // --------------------------------------------- tcgen05 (M > 4, N = kMp)
-    if (warp == 1) {
+    // Two issuing threads (warps 1 and 2, lane 0) take alternate slots: one
+    // tcgen05.mma costs the issuing thread about 90 ns, and one thread alone
+    // would fall behind the weight stream.  Each commits the accumulators of
+    // its units and, after a slot's last unit, the slot's release; the
+    // epilogue takes the accumulators in unit order.
+    if (warp == 1 || warp == 2) {
       idle_wait(dep);
+      const int w = warp - 1;
       if (lane == 0) {
-        trace_stamp(ctx, c, TR_START);
-        trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
+        if (w == 0) {
+          trace_stamp(ctx, c, TR_START);
+          trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
+        }
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
-        int issued = 0;
-        for (int i = 0; i < nunits; ++i) {
+        const int nslots = (nunits + P.ups - 1) / P.ups;
+        long long last_tq = -1;
+        for (int j = w; j < nslots; j += 2) {
+          const uint32_t q = P.seq0 + static_cast<uint32_t>(j);
+          if (!mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 14)) break;
+          const int i0 = j * P.ups, i1 = min(nunits, i0 + P.ups);
           bool ok = true;
-          for (int j = 0; j < P.spu && ok; ++j) {
-            const uint32_t q = pipe_seq(P, i, j);
-            ok = mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 14);
+          for (int i = i0; i < i1; ++i) {
+            const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
+            const int b = static_cast<int>(tq % TR.nbuf);
+            if (tq >= static_cast<uint32_t>(TR.nbuf) &&
+                !mbar_wait(&sh.tempty[b], ((tq / TR.nbuf) - 1) & 1, ctx, 15)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sb = smem_u32(gemm_x(P, i));
+            for (int p = 0; p < npair; ++p) {
+              const uint32_t d = TR.base + b * TR.stride + p * kMp;
+              const uint32_t sa = smem_u32(gemm_w(P, i, p));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = umma_desc_sw128(sa + k * 32);
+                const uint64_t bd = umma_desc_sw128(sb + k * 32);
+                if (a.fp8)
+                  umma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                else
+                  umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+              }
+            }
+            umma_commit(&sh.tfull[b]);
+            last_tq = tq;
           }
           if (!ok) break;
-          const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
-          const int b = static_cast<int>(tq % TR.nbuf);
-          if (tq >= static_cast<uint32_t>(TR.nbuf) &&
-              !mbar_wait(&sh.tempty[b], ((tq / TR.nbuf) - 1) & 1, ctx, 15))
-            break;
-          tc_fence_after();
-          const uint32_t sb = smem_u32(gemm_x(P, i, npair));
-          for (int p = 0; p < npair; ++p) {
-            const uint32_t d = TR.base + b * TR.stride + p * kMp;
-            const uint32_t sa = smem_u32(gemm_w(P, i, p));
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = umma_desc_sw128(sa + k * 32);
-              const uint64_t bd = umma_desc_sw128(sb + k * 32);
-              if (a.fp8)
-                umma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-              else
-                umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-            }
-          }
-          for (int j = 0; j < P.spu; ++j) {
-            uint64_t* e = pipe_empty(P, pipe_seq(P, i, j));
-            umma_commit(e);
-            if (P.empty_cnt > 1) mbar_arrive_cnt(e, static_cast<uint32_t>(P.empty_cnt - 1));
-          }
-          umma_commit(&sh.tfull[b]);
-          issued = i + 1;
+          uint64_t* e = pipe_empty(P, q);
+          umma_commit(e);
+          if (P.empty_cnt > 1) mbar_arrive_cnt(e, static_cast<uint32_t>(P.empty_cnt - 1));
         }
         // no MMA may still read shared memory or write TMEM when we leave
-        if (issued > 0) {
-          const uint32_t l = TR.seq0 + static_cast<uint32_t>(issued - 1);
-          mbar_drain(&sh.tfull[l % TR.nbuf], (l / TR.nbuf) & 1, ctx.budget_ns);
-        }
+        if (last_tq >= 0)
+          mbar_drain(&sh.tfull[last_tq % TR.nbuf], static_cast<uint32_t>(last_tq / TR.nbuf) & 1u,
+                     ctx.budget_ns);
       }
       return;
     }
@@ -887,10 +906,10 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     const int et = tid - 160;
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
     if (et == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
-    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
     bool dead = false;
     int i = 0;
     while (i < nunits) {
@@ -1011,6 +1030,8 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   }
   __syncthreads();
 
+  const int ups = npair == 1 ? 2 : 1;
+  const int nslots = (nunits + ups - 1) / ups;
   if (warp == 0) {
     // ------------------------------------------------------- producer
     if (lane != 0) {
@@ -1019,46 +1040,53 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     }
     prefetch_tmap(a.tmap_w);
     prefetch_tmap(a.tmap_x);
-    const uint32_t tx = npair * 16384 + a.Mp * 128;
+    const uint32_t ub = npair * 16384 + a.Mp * 128;   // bytes of one unit
     const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-    const int pre = min(S, nunits);
+    // the weight tiles / activation slices of the units of slot j
+    auto load_w = [&](int j, int s) {
+      uint8_t* st = sh.stage0 + s * L.stage_bytes;
+      for (int i = j * ups; i < nunits && i < (j + 1) * ups; ++i) {
+        const long long u = u0 + i;
+        const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
+        const int sub = i - j * ups;
+        tma_load_2d(st + sub * 16384, a.tmap_w, &sh.full[s], kb * kel, t * 128, pw);
+        if (a.pair)
+          tma_load_2d(st + 16384, a.tmap_w, &sh.full[s], kb * kel, a.up_row + t * 128, pw);
+      }
+    };
+    auto load_x = [&](int j, int s) {
+      uint8_t* st = sh.stage0 + s * L.stage_bytes;
+      for (int i = j * ups; i < nunits && i < (j + 1) * ups; ++i) {
+        const int kb = static_cast<int>((u0 + i) % a.KB);
+        tma_load_2d(st + kSlotTiles + (i - j * ups) * L.x_bytes, a.tmap_x, &sh.full[s], kb * kel,
+                    0, px);
+      }
+    };
+    auto units_in = [&](int j) { return min(ups, nunits - j * ups); };
+    const int pre = min(S, nslots);
     // weights of the first stages do not depend on the previous op
-    for (int i = 0; i < pre; ++i) {
-      const long long u = u0 + i;
-      const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
-      uint8_t* st = sh.stage0 + i * L.stage_bytes;
-      mbar_arrive_expect_tx(&sh.full[i], tx);
-      tma_load_2d(st, a.tmap_w, &sh.full[i], kb * kel, t * 128, pw);
-      if (a.pair)
-        tma_load_2d(st + 16384, a.tmap_w, &sh.full[i], kb * kel, a.up_row + t * 128, pw);
+    for (int j = 0; j < pre; ++j) {
+      mbar_arrive_expect_tx(&sh.full[j], ub * units_in(j));
+      load_w(j, j);
     }
     bool ok = single_wait(dep, ctx, 10);
     // activations of the prefetched stages (issued even after a failed wait
     // so that every armed stage completes and can be drained)
-    for (int i = 0; i < pre; ++i) {
-      const int kb = static_cast<int>((u0 + i) % a.KB);
-      tma_load_2d(sh.stage0 + i * L.stage_bytes + npair * 16384, a.tmap_x, &sh.full[i],
-                  kb * kel, 0, px);
-    }
+    for (int j = 0; j < pre; ++j) load_x(j, j);
     int issued = pre;
     if (ok) {
-      for (int i = pre; i < nunits; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(&sh.empty[s], ((i / S) - 1) & 1, ctx, 11)) break;
-        const long long u = u0 + i;
-        const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
-        uint8_t* st = sh.stage0 + s * L.stage_bytes;
-        mbar_arrive_expect_tx(&sh.full[s], tx);
-        tma_load_2d(st, a.tmap_w, &sh.full[s], kb * kel, t * 128, pw);
-        if (a.pair)
-          tma_load_2d(st + 16384, a.tmap_w, &sh.full[s], kb * kel, a.up_row + t * 128, pw);
-        tma_load_2d(st + npair * 16384, a.tmap_x, &sh.full[s], kb * kel, 0, px);
-        issued = i + 1;
+      for (int j = pre; j < nslots; ++j) {
+        const int s = j % S;
+        if (!mbar_wait(&sh.empty[s], ((j / S) - 1) & 1, ctx, 11)) break;
+        mbar_arrive_expect_tx(&sh.full[s], ub * units_in(j));
+        load_w(j, s);
+        load_x(j, s);
+        issued = j + 1;
       }
     }
     // no copy may be in flight when the CTA leaves
     for (int s = 0; s < S && s < issued; ++s) {
-      const int last = s + ((issued - 1 - s) / S) * S;  // last unit issued to stage s
+      const int last = s + ((issued - 1 - s) / S) * S;  // last slot issued to stage s
       mbar_drain(&sh.full[s], (last / S) & 1, ctx.budget_ns);
     }
     return;
@@ -1070,7 +1098,8 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
   P.ns = static_cast<uint32_t>(S);
   P.seq0 = 0;
-  P.spu = 1;
+  P.ups = ups;
+  P.x_bytes = L.x_bytes;
   P.empty_cnt = kMMA ? 1 : 8;
   TmemRing TR;
   TR.base = tmem_base;
@@ -1152,10 +1181,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // over the partials in CTA order (deterministic).
 // Attention block i of a pipeline: K (d 0-63 | d 64-127), then V.
 __device__ __forceinline__ uint8_t* attn_k(const Pipe& P, int i) {
-  return pipe_slot(P, pipe_seq(P, i, 0));
+  return pipe_slot(P, pipe_q(P, i));
 }
 __device__ __forceinline__ uint8_t* attn_v(const Pipe& P, int i) {
-  return P.spu == 1 ? attn_k(P, i) + 2 * kAttnKeys * 128 : pipe_slot(P, pipe_seq(P, i, 1));
+  return attn_k(P, i) + 2 * kAttnKeys * 128;
 }
 
 // Consumer side of an attention share (warps 1-8): `priv` is the share's
@@ -1365,8 +1394,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
         }
         if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
         __syncwarp();
-        if (lane == 0)
-          for (int j = 0; j < P.spu; ++j) mbar_arrive(pipe_empty(P, pipe_seq(P, i, j)));
+        if (lane == 0) mbar_arrive(pipe_empty(P, pipe_q(P, i)));
       }
     }
     // ---- merge the four key groups (fixed order) into Ob, then lse
@@ -1700,7 +1728,8 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
   P.ns = static_cast<uint32_t>(S);
   P.seq0 = 0;
-  P.spu = 1;
+  P.ups = 1;
+  P.x_bytes = 0;
   P.empty_cnt = 8;
   attn_consume_t<kNMT>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
 }
@@ -1713,6 +1742,273 @@ __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCt
     attn_op_t<2>(a, c, dep, ctx, smem);
   else
     attn_op_t<4>(a, c, dep, ctx, smem);
+}
+
+// ========================================================= MEGAKERNEL
+// Streaming megakernel: one worker CTA per SM walks its host-built queue of
+// instructions.  Its producer warp runs ahead of the consumer warps and
+// fills one ring of equal slots in exactly the order the consumers will
+// take them, across instruction boundaries: the weights of the next
+// projection stream in while the current instruction is still computing,
+// fixing up and signalling (the overlap of instruction i + 1's load with
+// instruction i's compute on page "Kernel-Mega-PDL", megakernel section).
+// Dependent data (activations, KV blocks that hold this step's new keys) is
+// issued only after the instruction's event counters are reached.
+// GEMM share c: its units fill slots seq, seq + 1, ... (two units per slot
+// without gate/up pairing, one otherwise), each unit's activation slice
+// after the slot's tiles.  Weights go out as soon as a slot is free;
+// activation slices once the share's inputs are ready, and before the
+// producer would block on a slot that only the consumption of a pending
+// unit can free.  Every armed slot completes even after a failed wait (so
+// the ring can be drained).
+__device__ __noinline__ bool mk_produce_gemm(const GemmArgs& a_, int c, const Dep& dep_,
+                                             const KernelCtx& ctx_, const Pipe& R_, uint32_t seq,
+                                             uint32_t* hi) {
+  const GemmArgs a = a_;
+  const Dep dep = dep_;
+  const KernelCtx ctx = ctx_;
+  const Pipe R = R_;
+  const int npair = a.pair ? 2 : 1;
+  const int ups = npair == 1 ? 2 : 1;
+  const long long U = static_cast<long long>(a.NT) * a.KB;
+  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int n = static_cast<int>(u1 - u0);
+  const int nslots = (n + ups - 1) / ups;
+  const int kel = a.fp8 ? 128 : 64;
+  const uint32_t ub = static_cast<uint32_t>(npair * 16384 + a.Mp * 128);
+  const int xbytes = ((a.Mp * 128 + 1023) / 1024) * 1024;
+  const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+  prefetch_tmap(a.tmap_w);
+  prefetch_tmap(a.tmap_x);
+  bool deps_ok = false, ok = true;
+  int pend = 0;    // first unit whose activation slice is not issued yet
+  int armed = 0;   // units whose slot is armed
+  auto load_x = [&](int i) {
+    const int kb = static_cast<int>((u0 + i) % a.KB);
+    const uint32_t q = seq + static_cast<uint32_t>(i / ups);
+    tma_load_2d(pipe_slot(R, q) + kSlotTiles + (i % ups) * xbytes, a.tmap_x, pipe_full(R, q),
+                kb * kel, 0, px);
+  };
+  for (int j = 0; j < nslots && ok; ++j) {
+    const uint32_t q = seq + static_cast<uint32_t>(j);
+    if (q >= R.ns) {
+      uint64_t* e = pipe_empty(R, q);
+      const uint32_t par = ((q / R.ns) - 1) & 1u;
+      if (!deps_ok && pend < armed && !mbar_try_wait(e, par)) {
+        deps_ok = poll_deps(dep, ctx, 60);
+        trace_stamp(ctx, c, TR_PDEPS);
+        for (; pend < armed; ++pend) load_x(pend);
+        if (!deps_ok) {
+          ok = false;
+          break;
+        }
+      }
+      if (!mbar_wait(e, par, ctx, 61)) {
+        ok = false;
+        break;
+      }
+    }
+    const int i0 = j * ups, i1 = min(n, i0 + ups);
+    mbar_arrive_expect_tx(pipe_full(R, q), ub * static_cast<uint32_t>(i1 - i0));
+    *hi = q + 1;
+    for (int i = i0; i < i1; ++i) {
+      const long long u = u0 + i;
+      const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
+      tma_load_2d(pipe_slot(R, q) + (i - i0) * 16384, a.tmap_w, pipe_full(R, q), kb * kel,
+                  t * 128, pw);
+      if (a.pair)
+        tma_load_2d(pipe_slot(R, q) + 16384, a.tmap_w, pipe_full(R, q), kb * kel,
+                    a.up_row + t * 128, pw);
+    }
+    armed = i1;
+    if (deps_ok)
+      for (; pend < armed; ++pend) load_x(pend);
+  }
+  if (!deps_ok && armed > 0) {
+    deps_ok = poll_deps(dep, ctx, 62);
+    trace_stamp(ctx, c, TR_PDEPS);
+  }
+  for (; pend < armed; ++pend) load_x(pend);
+  return ok && (deps_ok || armed == 0);
+}
+
+// Attention share c (whole warp; lane 0 issues): valid block i (keys below
+// its pair's context) takes slot seq + i (K, then V).
+// Blocks that hold none of this step's new keys are independent of the
+// previous instructions and go out at once; the first block that holds a
+// new key waits for the share's inputs.  Returns the valid blocks issued
+// (through *nvalid) and false after a failed wait.
+__device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const Dep& dep_,
+                                             const KernelCtx& ctx_, const Pipe& R_, uint32_t seq,
+                                             int* pgbuf, int* ppos, int* nvalid, uint32_t* hi) {
+  const AttnArgs a = a_;
+  const Dep dep = dep_;
+  const KernelCtx ctx = ctx_;
+  const Pipe R = R_;
+  const int lane = threadIdx.x & 31;
+  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
+  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const Binding* bd = ctx.binding;
+  const CUtensorMap* kvm = &bd->kv_map;
+  if (lane == 0) {
+    fence_tmap_acquire(kvm);
+    prefetch_tmap(kvm);
+  }
+  const int* pos = resolve<const int>(a.pos, bd);
+  const int* bt = resolve<const int>(a.bt, bd);
+  const int M = a.R * a.T;
+  for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
+  __syncwarp();
+  const uint64_t pol = policy_evict_first();
+  const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
+  const int npg = kAttnKeys / box;                      // boxes per 64-key block
+  const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
+  bool ok = true, deps_ok = dep.n == 0;
+  int i = 0;
+  for (long long ub = u0; ok && ub < u1; ub += 32) {
+    const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
+    for (int e = lane; e < nb * npg; e += 32) {
+      const int j = e / npg, qq = e % npg;
+      const long long u = ub + j;
+      const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+      const int r = p / a.Hkv;
+      const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+      const int key = blk * kAttnKeys + qq * box;
+      const int lp = key / a.P;
+      pgbuf[j * 4 + qq] = (key < ctxr && lp < a.max_pages)
+                              ? bt[static_cast<size_t>(r) * a.max_pages + lp] : -1;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int j = 0; j < nb && ok; ++j) {
+        const long long u = ub + j;
+        const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
+        const int r = p / a.Hkv, h = p % a.Hkv;
+        const int ctxr = ppos[r * a.T + a.T - 1] + 1;
+        const int k0 = blk * kAttnKeys;
+        if (k0 >= ctxr) continue;
+        const int nk = min(kAttnKeys, ctxr - k0);
+        if (!deps_ok && k0 + nk > ppos[r * a.T]) {
+          deps_ok = poll_deps(dep, ctx, 63);
+          trace_stamp(ctx, c, TR_PDEPS);
+          if (!deps_ok) {
+            ok = false;
+            break;
+          }
+        }
+        const int nbox = (nk + box - 1) / box;
+        const uint32_t q = seq + static_cast<uint32_t>(i);
+        if (q >= R.ns && !mbar_wait(pipe_empty(R, q), ((q / R.ns) - 1) & 1u, ctx, 64)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(pipe_full(R, q), static_cast<uint32_t>(nbox * box * 128 * 4));
+        *hi = q + 1;
+        uint8_t* dst = pipe_slot(R, q);
+        for (int qq = 0; qq < nbox; ++qq) {
+          const int key = k0 + qq * box;
+          int page = pgbuf[j * 4 + qq];
+          if (page < 0 || page >= a.num_pages) {
+            report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 65, key / a.P);
+            page = 0;
+          }
+          const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, key % a.P));
+          const int rv = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 1, h, key % a.P));
+          uint8_t* dq = dst + qq * box * 128;
+          tma_load_2d(dq, kvm, pipe_full(R, q), 0, rk, pol);
+          tma_load_2d(dq + half, kvm, pipe_full(R, q), 64, rk, pol);
+          tma_load_2d(dq + 2 * half, kvm, pipe_full(R, q), 0, rv, pol);
+          tma_load_2d(dq + 3 * half, kvm, pipe_full(R, q), 64, rv, pol);
+        }
+        ++i;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    i = __shfl_sync(0xffffffffu, i, 0);
+    deps_ok = __shfl_sync(0xffffffffu, deps_ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+  }
+  *nvalid = i;
+  return ok;
+}
+
+// Consumer side of one GEMM instruction with the variant its arguments call
+// for, over the worker's ring and TMEM accumulator ring.
+// Each consumer variant is a separate, non-inlined function (the megakernel
+// then allocates registers per variant, as the standalone kernels do, not
+// for the union of all of them), and it works on private copies of its
+// arguments: the instruction's arguments sit in shared memory and the
+// descriptors in the caller's frame, and every inline-asm memory clobber
+// (barrier waits, MMAs, fences) would otherwise force the compiler to load
+// each field again; the standalone kernels read them from parameter space,
+// which never changes.
+template <int kMG, int kMp>
+__device__ __noinline__ void mk_gemm_v(const GemmArgs& a_, int c, const Dep& dep_,
+                                       const KernelCtx& ctx_, const GemmShared& sh_,
+                                       const Pipe& P_, const TmemRing& TR_) {
+  const GemmArgs a = a_;
+  const Dep dep = dep_;
+  const KernelCtx ctx = ctx_;
+  const GemmShared sh = sh_;
+  const Pipe P = P_;
+  const TmemRing TR = TR_;
+  gemm_consume_t<kMG, kMp>(a, c, dep, ctx, sh, P, TR);
+}
+
+template <int kNMT>
+__device__ __noinline__ int mk_attn_v(const AttnArgs& a_, int c, const Dep& dep_,
+                                      const KernelCtx& ctx_, uint8_t* priv, const Pipe& P_) {
+  const AttnArgs a = a_;
+  const Dep dep = dep_;
+  const KernelCtx ctx = ctx_;
+  const Pipe P = P_;
+  return attn_consume_t<kNMT>(a, c, dep, ctx, priv, P);
+}
+
+__device__ __noinline__ void mk_norm(const NormArgs& a_, int c, const Dep& dep_,
+                                     const KernelCtx& ctx_, uint8_t* priv) {
+  const NormArgs a = a_;
+  const Dep dep = dep_;
+  const KernelCtx ctx = ctx_;
+  norm_op(a, c, dep, ctx, priv);
+}
+
+__device__ void mk_gemm(const GemmArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
+                        uint8_t* priv, const Pipe& P, const TmemRing& TR, uint64_t* tfull,
+                        uint64_t* tempty) {
+  GemmShared sh = gemm_shared(a, priv, 0);
+  sh.tfull = tfull;
+  sh.tempty = tempty;
+  if (!a.mma) {
+    if (a.M <= 1)
+      mk_gemm_v<1, 0>(a, c, dep, ctx, sh, P, TR);
+    else if (a.M <= 2)
+      mk_gemm_v<2, 0>(a, c, dep, ctx, sh, P, TR);
+    else
+      mk_gemm_v<4, 0>(a, c, dep, ctx, sh, P, TR);
+  } else {
+    if (a.Mp <= 16)
+      mk_gemm_v<0, 16>(a, c, dep, ctx, sh, P, TR);
+    else if (a.Mp <= 32)
+      mk_gemm_v<0, 32>(a, c, dep, ctx, sh, P, TR);
+    else
+      mk_gemm_v<0, 64>(a, c, dep, ctx, sh, P, TR);
+  }
+}
+
+// Consumer side of one attention instruction; returns the key blocks it
+// consumed, or -1 after a failed wait.
+__device__ int mk_attn(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
+                       uint8_t* priv, const Pipe& P) {
+  if (a.QRp <= 16) return mk_attn_v<1>(a, c, dep, ctx, priv, P);
+  if (a.QRp <= 32) return mk_attn_v<2>(a, c, dep, ctx, priv, P);
+  return mk_attn_v<4>(a, c, dep, ctx, priv, P);
+}
+
+// Units of GEMM share c (its Stream-K range).
+__device__ __forceinline__ int gemm_share_units(const GemmArgs& a, int c) {
+  const long long U = static_cast<long long>(a.NT) * a.KB;
+  return static_cast<int>(sk_begin(U, a.G, c + 1) - sk_begin(U, a.G, c));
 }
 
 }  // namespace dl
