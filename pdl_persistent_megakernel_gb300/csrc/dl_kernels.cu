@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
   __shared__ __align__(16) OpArgs op;
   __shared__ int stop;
   __shared__ __align__(8) uint64_t ring_full[kMaxSlots], ring_empty[kMaxSlots];
-  __shared__ __align__(8) uint64_t tm_full[4], tm_empty[4];
+  __shared__ __align__(8) uint64_t tbars[12];   // TMEM full[4], empty[4]; tile ready[2], free[2]
   __shared__ int p_pgbuf[32 * 4], p_ppos[kMaxM];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* priv = smem + m.priv_off;
@@ -134,8 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
       mbar_init(&ring_empty[s], 8);
     }
     for (int b = 0; b < 4; ++b) {
-      mbar_init(&tm_full[b], 1);
-      mbar_init(&tm_empty[b], 4);
+      mbar_init(&tbars[b], 1);
+      mbar_init(&tbars[4 + b], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tbars[8 + b], 4);
+      mbar_init(&tbars[10 + b], 2);
     }
     stop = 0;
     fence_barrier_init();
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
   } else {
     // ------------------------------------------------------- consumers
     const int ct = tid - 32;
-    uint32_t seq = 0, tseq = 0;
+    uint32_t seq = 0, tseq = 0, rseq = 0;
     for (int pc = 0; pc < m.qlen; ++pc) {
       if (ct < 32) reinterpret_cast<uint32_t*>(&ins)[ct] = __ldg(reinterpret_cast<const uint32_t*>(q + pc) + ct);
       named_bar(1, 256);
@@ -240,10 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
           TR.nbuf = 4;
           TR.stride = 128;
           TR.seq0 = tseq;
-          mk_gemm(op.gemm, cta, dep, c2, priv, P, TR, tm_full, tm_empty);
+          TR.rseq0 = rseq;
+          mk_gemm(op.gemm, cta, dep, c2, priv, P, TR, tbars);
           const int n = gemm_share_units(op.gemm, cta);
           seq += static_cast<uint32_t>((n + ups - 1) / ups);
-          if (op.gemm.mma) tseq += static_cast<uint32_t>(n);
+          if (op.gemm.mma) {
+            tseq += static_cast<uint32_t>(n);
+            rseq += static_cast<uint32_t>(gemm_share_runs(op.gemm, cta));
+          }
           break;
         }
         case OP_ATTN: {

@@ -231,6 +231,13 @@ struct GemmSmem {
 
 constexpr int kMaxContrib = 256;  // CTAs that may share one tile / KV pair
 
+// Finished-tile buffers of the tcgen05 path: two (the epilogue warps fill
+// one while the fix-up warps finish the other) when a tile takes at most 16
+// KiB, else one.
+__host__ __device__ inline int gemm_ntout(int npair, int Mp) {
+  return npair * Mp * 128 * 4 <= 16384 ? 2 : 1;
+}
+
 // Shared-memory layout of one GEMM CTA: the operand ring, the finished tile,
 // the FP8 scales of the current tile run (staged once per run), the QKV
 // epilogue's per-token positions / cache rows / RoPE rows, barriers and a
@@ -244,12 +251,12 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   // activation slice per unit
   L.stage_bytes = 2 * L.w_bytes + (npair == 1 ? 2 : 1) * L.x_bytes;
   L.tile_off = stages * L.stage_bytes;
-  L.sx_off = L.tile_off + npair * Mp * 128 * 4;
+  L.sx_off = L.tile_off + gemm_ntout(npair, Mp) * npair * Mp * 128 * 4;
   L.sw_off = L.sx_off + (fp8 ? KB * Mp * 4 : 0);
   L.epi_off = ((L.sw_off + (fp8 ? 2 * KB * 4 : 0)) + 15) & ~15;
   L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) : 0);
   L.bar_off = (L.bar_off + 15) & ~15;
-  L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs) * 8;
+  L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 4) * 8;
   L.total = L.misc_off + 256 + kMaxContrib * 4;
   return L;
 }
@@ -266,6 +273,8 @@ struct GemmShared {
   uint64_t* empty;
   uint64_t* tfull;
   uint64_t* tempty;
+  uint64_t* tready;  // [2] finished tile buffer b written (4 epilogue warps)
+  uint64_t* tfree;   // [2] tile buffer b finished and free (2 fix-up warps)
   int* flag;      // [4]
   int* ctb;       // [kMaxContrib] contributor list of a fix-up
 };
@@ -695,6 +704,7 @@ struct TmemRing {
   int nbuf;
   int stride;
   uint32_t seq0;
+  uint32_t rseq0;   // tile runs handed to the fix-up warps before this share
 };
 
 // ------------------------------------------------------------ GEMM engine
@@ -898,6 +908,33 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       }
       return;
     }
+    const int ntb = gemm_ntout(npair, kMp);
+    const int tile_floats = npair * a.Mp * 128;
+    if (warp == 3 || warp == 4) {
+      // fix-up warps: the Stream-K fix-up and epilogue of each finished
+      // tile, while the epilogue warps already accumulate the next one
+      idle_wait(dep);
+      const int ft = tid - 96;
+      int i = 0;
+      uint32_t rq = TR.rseq0;
+      while (i < nunits) {
+        const long long u = u0 + i;
+        const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
+        const int run = min(nunits - i, a.KB - kb0);
+        const int b = static_cast<int>(rq % ntb);
+        if (!warp_wait(&sh.tready[b], (rq / ntb) & 1, ctx, 18)) return;
+        if (aborted(ctx.status)) return;
+        GemmShared shb = sh;
+        shb.tout = sh.tout + b * tile_floats;
+        gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 64, ft, 3, ctx, shb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.tfree[b]);
+        i += run;
+        ++rq;
+      }
+      if (ft == 0) trace_stamp(ctx, c, TR_END);
+      return;
+    }
     if (warp < 5) {
       idle_wait(dep);
       return;
@@ -912,6 +949,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
     bool dead = false;
     int i = 0;
+    uint32_t rq = TR.rseq0;
     while (i < nunits) {
       const long long u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
@@ -963,18 +1001,25 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.tempty[b]);
       }
+      // hand the tile to the fix-up warps through buffer b
+      const int b = static_cast<int>(rq % ntb);
+      if (rq >= static_cast<uint32_t>(ntb) && !dead)
+        dead = !warp_wait(&sh.tfree[b], ((rq / ntb) - 1) & 1, ctx, 19);
+      if (named_bar_or(2, 128, dead)) return;
+      float* tout = sh.tout + b * tile_floats;
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         if (p >= npair) break;
 #pragma unroll
         for (int m = 0; m < kMp; ++m)
-          if (m < a.M) sh.tout[(p * a.Mp + m) * 128 + row] = acc[p][m];
+          if (m < a.M) tout[(p * a.Mp + m) * 128 + row] = acc[p][m];
       }
       if (et == 0 && i == nunits) trace_stamp(ctx, c, TR_LOOP_END);
-      if (named_bar_or(2, 128, dead)) return;
-      gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, sh);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.tready[b]);
+      ++rq;
     }
-    if (et == 0) trace_stamp(ctx, c, TR_END);
+    // the fix-up warps finish the last tile; the share ends when they do
   }
 }
 
@@ -995,6 +1040,8 @@ __device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* sm
   sh.empty = sh.full + kMaxStages;
   sh.tfull = sh.empty + kMaxStages;
   sh.tempty = sh.tfull + kMaxTmemBufs;
+  sh.tready = sh.tempty + kMaxTmemBufs;
+  sh.tfree = sh.tready + 2;
   sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
   sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
   return sh;
@@ -1023,6 +1070,10 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     for (int b = 0; b < kMaxTmemBufs; ++b) {
       mbar_init(&sh.tfull[b], 1);
       mbar_init(&sh.tempty[b], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.tready[b], 4);
+      mbar_init(&sh.tfree[b], 2);
     }
     sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
     sh.flag[2] = 1;
@@ -1106,6 +1157,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   TR.nbuf = kMMA ? a.tmem_bufs : 1;
   TR.stride = npair * (kMMA ? kMp : 0);
   TR.seq0 = 0;
+  TR.rseq0 = 0;
   gemm_consume_t<kMG, kMp>(a, c, dep, ctx, sh, P, TR);
 }
 
@@ -1974,11 +2026,12 @@ __device__ __noinline__ void mk_norm(const NormArgs& a_, int c, const Dep& dep_,
 }
 
 __device__ void mk_gemm(const GemmArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
-                        uint8_t* priv, const Pipe& P, const TmemRing& TR, uint64_t* tfull,
-                        uint64_t* tempty) {
+                        uint8_t* priv, const Pipe& P, const TmemRing& TR, uint64_t* tbars) {
   GemmShared sh = gemm_shared(a, priv, 0);
-  sh.tfull = tfull;
-  sh.tempty = tempty;
+  sh.tfull = tbars;            // [4]
+  sh.tempty = tbars + 4;       // [4]
+  sh.tready = tbars + 8;       // [2]
+  sh.tfree = tbars + 10;       // [2]
   if (!a.mma) {
     if (a.M <= 1)
       mk_gemm_v<1, 0>(a, c, dep, ctx, sh, P, TR);
@@ -2009,6 +2062,13 @@ __device__ int mk_attn(const AttnArgs& a, int c, const Dep& dep, const KernelCtx
 __device__ __forceinline__ int gemm_share_units(const GemmArgs& a, int c) {
   const long long U = static_cast<long long>(a.NT) * a.KB;
   return static_cast<int>(sk_begin(U, a.G, c + 1) - sk_begin(U, a.G, c));
+}
+
+// Tile runs of GEMM share c (tiles its range touches).
+__device__ __forceinline__ int gemm_share_runs(const GemmArgs& a, int c) {
+  const long long U = static_cast<long long>(a.NT) * a.KB;
+  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  return u1 > u0 ? static_cast<int>((u1 - 1) / a.KB - u0 / a.KB + 1) : 0;
 }
 
 }  // namespace dl
