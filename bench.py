@@ -190,7 +190,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="q8_layer_m16_ctx8192_fp8")
-    ap.add_argument("--modes", default="serial,pdl_graph,megakernel")
+    ap.add_argument("--modes", default="serial,graph_linear,graph_linear_pdl,pdl_graph,megakernel")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--per-kernel", action="store_true", default=True)
