@@ -1267,7 +1267,17 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
   const int ct = tid - 32, wc = warp - 1;  // wc: 0..7
-  const int kg = wc & 3, dh = wc >> 2;     // key group, head-dim half
+  // Warp wc works on key group kg = wc % 4 (16 keys of every 64-key block).
+  // With two 16-row m-tiles (kMS) the pair of a key group splits the query
+  // rows: each warp takes one m-tile over the whole head dim, so no partial
+  // scores are exchanged; otherwise it splits the head dim (dh), takes every
+  // m-tile and the pair exchanges partial scores.
+  constexpr bool kMS = (kNMT == 2);
+  constexpr int kMT = kMS ? 1 : kNMT;      // m-tiles per warp
+  constexpr int kND = kMS ? 16 : 8;        // 8-column d tiles per warp
+  const int kg = wc & 3, dh = wc >> 2;     // key group; d-half or m-tile
+  const int mtb = kMS ? dh : 0;            // first m-tile of this warp
+  const int dlo = kMS ? 0 : dh;            // first d-half of this warp
   const int partner = kg + 4 * (1 - dh);
   if (ct == 0) {
     trace_stamp(ctx, c, TR_START);
@@ -1303,22 +1313,22 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
     }
     for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
     named_bar(1, 256);
-    int lim[kNMT][2];
+    int lim[kMT][2];
 #pragma unroll
-    for (int mt = 0; mt < kNMT; ++mt) {
-      lim[mt][0] = row_pos[mt * 16 + qr];
-      lim[mt][1] = row_pos[mt * 16 + qr + 8];
+    for (int mt = 0; mt < kMT; ++mt) {
+      lim[mt][0] = row_pos[(mtb + mt) * 16 + qr];
+      lim[mt][1] = row_pos[(mtb + mt) * 16 + qr + 8];
     }
-    float o[kNMT][8][4];
+    float o[kMT][kND][4];
 #pragma unroll
-    for (int mt = 0; mt < kNMT; ++mt)
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+      for (int nt = 0; nt < kND; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-    float mrow[kNMT][2], lrow[kNMT][2];
+    float mrow[kMT][2], lrow[kMT][2];
 #pragma unroll
-    for (int mt = 0; mt < kNMT; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
       mrow[mt][0] = mrow[mt][1] = -INFINITY;
       lrow[mt][0] = lrow[mt][1] = 0.f;
     }
@@ -1332,9 +1342,9 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       const int k0 = blk * kAttnKeys;
       const int nk = min(kAttnKeys, ctxr - k0);
       float* xbuf = xs + (i & 1) * (8 * kXS * 32);
-      float sc[kNMT][2][4];
+      float sc[kMT][2][4];
 #pragma unroll
-      for (int mt = 0; mt < kNMT; ++mt)
+      for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -1342,7 +1352,8 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       if (!dead) {
         if (nk < kAttnKeys) {
           // keys past the context were not loaded (or hold stale data): zero
-          // this warp's V rows so that 0-probability keys contribute exactly 0
+          // this key group's V rows (the pair splits them by d-half) so that
+          // 0-probability keys contribute exactly 0
           uint8_t* vh = vst + dh * kAttnKeys * 128;
           for (int e = lane; e < 16 * 8; e += 32) {
             const int key = kg * 16 + (e >> 3);
@@ -1350,44 +1361,53 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
           }
           __syncwarp();
         }
-        // partial S over this warp's half of d
+        // S over this warp's d range (both halves with kMS)
 #pragma unroll
-        for (int ks4 = 0; ks4 < 4; ++ks4) {
-          const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
-          const int ch = ks4 * 2 + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        for (int dd = 0; dd < (kMS ? 2 : 1); ++dd) {
+          const int dhh = dlo + dd;
 #pragma unroll
-          for (int mt = 0; mt < kNMT; ++mt) {
-            const int qrow = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int qch = (dh * 4 + ks4) * 2 + (lane >> 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
-            mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
+          for (int ks4 = 0; ks4 < 4; ++ks4) {
+            const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int ch = ks4 * 2 + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kb_u32 + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+              const int qrow = (mtb + mt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+              const int qch = (dhh * 4 + ks4) * 2 + (lane >> 4);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
+              mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
+              mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
+            }
           }
         }
-        float* mine = xbuf + wc * (kXS * 32);
+        if constexpr (!kMS) {
+          float* mine = xbuf + wc * (kXS * 32);
 #pragma unroll
-        for (int mt = 0; mt < kNMT; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mine[((mt * 2 + nt) * 4 + e) * 32 + lane] = sc[mt][nt][e];
+              for (int e = 0; e < 4; ++e) mine[((mt * 2 + nt) * 4 + e) * 32 + lane] = sc[mt][nt][e];
+        }
       }
       // the two d-half warps of this key group exchange partial scores
-      named_bar(2 + kg, 64);
+      // (with kMS: the pair only waits for each other's V zeroing)
+      if (!kMS || nk < kAttnKeys) named_bar(2 + kg, 64);
       if (!dead) {
-        const float* other = xbuf + partner * (kXS * 32);
+        if constexpr (!kMS) {
+          const float* other = xbuf + partner * (kXS * 32);
 #pragma unroll
-        for (int mt = 0; mt < kNMT; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[mt][nt][e] += other[((mt * 2 + nt) * 4 + e) * 32 + lane];
+              for (int e = 0; e < 4; ++e) sc[mt][nt][e] += other[((mt * 2 + nt) * 4 + e) * 32 + lane];
+        }
         // scale, mask, online softmax on this key group's 16 keys
 #pragma unroll
-        for (int mt = 0; mt < kNMT; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             float mx = -INFINITY;
@@ -1420,28 +1440,38 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             mrow[mt][hr] = mnew;
             lrow[mt][hr] = lrow[mt][hr] * alpha + sum;
+            // after the first blocks a row's maximum rarely moves: skip the
+            // rescale (a multiply by exactly 1) unless some row of the warp's
+            // 8-row group changed
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-              o[mt][nt][hr * 2] *= alpha;
-              o[mt][nt][hr * 2 + 1] *= alpha;
+              for (int nt = 0; nt < kND; ++nt) {
+                o[mt][nt][hr * 2] *= alpha;
+                o[mt][nt][hr * 2 + 1] *= alpha;
+              }
             }
           }
         }
-        // O += P V for columns [64 dh, 64 dh + 64)
+        // O += P V over this warp's d range (columns [64 dh, 64 dh + 64), or
+        // all 128 with kMS)
 #pragma unroll
-        for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
-          const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int ch = cp * 2 + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb_u32 + dh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        for (int dd = 0; dd < (kMS ? 2 : 1); ++dd) {
+          const int dhh = dlo + dd;
 #pragma unroll
-          for (int mt = 0; mt < kNMT; ++mt) {
-            const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-            const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-            const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-            const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
-            mma_bf16_16816(o[mt][cp * 2], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(o[mt][cp * 2 + 1], a0, a1, a2, a3, b2, b3);
+          for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
+            const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int ch = cp * 2 + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vb_u32 + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+              const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+              const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+              const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+              const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+              mma_bf16_16816(o[mt][dd * 8 + cp * 2], a0, a1, a2, a3, b0, b1);
+              mma_bf16_16816(o[mt][dd * 8 + cp * 2 + 1], a0, a1, a2, a3, b2, b3);
+            }
           }
         }
         if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
@@ -1451,13 +1481,14 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
     }
     // ---- merge the four key groups (fixed order) into Ob, then lse
     if (named_bar_or(1, 256, dead)) return -1;
-    if (dh == 0 && qc == 0) {
+    if ((kMS || dh == 0) && qc == 0) {
 #pragma unroll
-      for (int mt = 0; mt < kNMT; ++mt) {
-        kg_m[kg * QRp + mt * 16 + qr] = mrow[mt][0];
-        kg_m[kg * QRp + mt * 16 + qr + 8] = mrow[mt][1];
-        kg_l[kg * QRp + mt * 16 + qr] = lrow[mt][0];
-        kg_l[kg * QRp + mt * 16 + qr + 8] = lrow[mt][1];
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int r0 = (mtb + mt) * 16 + qr;
+        kg_m[kg * QRp + r0] = mrow[mt][0];
+        kg_m[kg * QRp + r0 + 8] = mrow[mt][1];
+        kg_l[kg * QRp + r0] = lrow[mt][0];
+        kg_l[kg * QRp + r0 + 8] = lrow[mt][1];
       }
     }
     named_bar(1, 256);
@@ -1472,41 +1503,47 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       kg_l[rr] = l;   // slot 0 now holds the merged row sum (read after the barrier)
     }
     named_bar(1, 256);
-    float fac[kNMT][2];
+    float fac[kMT][2];
 #pragma unroll
-    for (int mt = 0; mt < kNMT; ++mt)
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int rr = mt * 16 + qr + hr * 8;
+        const int rr = (mtb + mt) * 16 + qr + hr * 8;
         const float l = kg_l[rr];
         fac[mt][hr] = (l > 0.f && mrow[mt][hr] != -INFINITY) ? exp2f(mrow[mt][hr] - row_w[rr]) / l : 0.f;
       }
+    const int col0 = (kMS ? 0 : dh * 64) + qc * 2;
     for (int g4 = 0; g4 < 4; ++g4) {
       if (kg == g4) {
-        // per m-tile: load the running sum first (no store -> load chains),
-        // add this key group's scaled slice, store
+        // per m-tile and 8 d tiles: load the running sum first (no store ->
+        // load chains), add this key group's scaled slice, store
 #pragma unroll
-        for (int mt = 0; mt < kNMT; ++mt) {
-          float2 prev[2][8];
-          if (g4 > 0) {
+        for (int mt = 0; mt < kMT; ++mt) {
+#pragma unroll
+          for (int n0 = 0; n0 < kND; n0 += 8) {
+            float2 prev[2][8];
+            if (g4 > 0) {
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+                  prev[hr][nt] = *reinterpret_cast<const float2*>(
+                      Ob + ((mtb + mt) * 16 + qr + hr * 8) * kOP + col0 + (n0 + nt) * 8);
+            }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-              for (int nt = 0; nt < 8; ++nt)
-                prev[hr][nt] = *reinterpret_cast<const float2*>(
-                    Ob + (mt * 16 + qr + hr * 8) * kOP + dh * 64 + nt * 8 + qc * 2);
-          }
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-              float2 v = make_float2(o[mt][nt][hr * 2] * fac[mt][hr], o[mt][nt][hr * 2 + 1] * fac[mt][hr]);
-              if (g4 > 0) {
-                v.x += prev[hr][nt].x;
-                v.y += prev[hr][nt].y;
+              for (int nt = 0; nt < 8; ++nt) {
+                float2 v = make_float2(o[mt][n0 + nt][hr * 2] * fac[mt][hr],
+                                       o[mt][n0 + nt][hr * 2 + 1] * fac[mt][hr]);
+                if (g4 > 0) {
+                  v.x += prev[hr][nt].x;
+                  v.y += prev[hr][nt].y;
+                }
+                *reinterpret_cast<float2*>(Ob + ((mtb + mt) * 16 + qr + hr * 8) * kOP + col0 +
+                                           (n0 + nt) * 8) = v;
               }
-              *reinterpret_cast<float2*>(Ob + (mt * 16 + qr + hr * 8) * kOP + dh * 64 + nt * 8 + qc * 2) = v;
-            }
+          }
         }
       }
       named_bar(1, 256);
