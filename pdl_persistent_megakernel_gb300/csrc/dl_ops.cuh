@@ -279,10 +279,10 @@ struct GemmShared {
   int* ctb;       // [kMaxContrib] contributor list of a fix-up
 };
 
-// Sum of `nc` fp32 partials (float4 granular, nel4 float4s each) listed in
-// ctb as workspace slot indices, in list order, into dst.  Each thread owns
-// up to 8 float4s per pass and loads them for two contributors at a time,
-// so a pass costs about nc / 2 L2 round trips.
+// dst (the first partial) plus `nc` fp32 partials (float4 granular, nel4
+// float4s each) listed in ctb as workspace slot indices, in list order, into
+// dst.  Each thread owns up to 8 float4s per pass and loads them for two
+// contributors at a time, so a pass costs about nc / 2 L2 round trips.
 __device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_t part,
                                              const int* ctb, int nc, int nel4, int nthr,
                                              int ct) {
@@ -291,7 +291,10 @@ __device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_
   for (int q0 = 0; q0 * nthr < nel4; q0 += kQ) {
     float4 acc[kQ];
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) acc[q] = z;
+    for (int q = 0; q < kQ; ++q) {
+      const int e4 = ct + (q0 + q) * nthr;
+      acc[q] = e4 < nel4 ? dst[e4] : z;
+    }
     for (int j = 0; j < nc; j += 2) {
       const float4* s0 = reinterpret_cast<const float4*>(ws + static_cast<size_t>(ctb[j]) * part);
       const float4* s1 = j + 1 < nc
@@ -556,28 +559,33 @@ __device__ void gemm_finish_tile(const GemmArgs& a, int c, long long u0, int tl,
   if (!full_tile) {
     const long long U = static_cast<long long>(a.NT) * a.KB;
     const long long ts = static_cast<long long>(tl) * a.KB;
-    const int slot = (u0 >= ts) ? 0 : 1;
-    float4* mine = reinterpret_cast<float4*>(a.ws + static_cast<size_t>(c * 2 + slot) * nel);
-    for (int e4 = ct; e4 < nel / 4; e4 += nthr) mine[e4] = reinterpret_cast<const float4*>(tout)[e4];
-    __threadfence();
-    named_bar(bar, nthr);
+    // The CTA whose range holds the tile's first unit reaches its part of
+    // the tile last (that part ends its range): it finishes the tile.  The
+    // others publish their partial early and add an arrival.
+    if (u0 > ts) {
+      float4* mine = reinterpret_cast<float4*>(a.ws + static_cast<size_t>(c * 2) * nel);
+      for (int e4 = ct; e4 < nel / 4; e4 += nthr) mine[e4] = reinterpret_cast<const float4*>(tout)[e4];
+      __threadfence();
+      named_bar(bar, nthr);
+      if (ct == 0) atomicAdd(a.tile_cnt + tl, 1u);
+      named_bar(bar, nthr);  // tout is reused by the next tile
+      return;
+    }
     if (ct == 0) {
       const int n = sk_contributors(U, a.G, ts, a.KB, sh.ctb);
       sh.flag[3] = n;
-      const unsigned old = atomicAdd(a.tile_cnt + tl, 1u);
-      sh.flag[0] = (old + 1 == static_cast<unsigned>(n)) ? 1 : 0;
+      const bool ok = n <= 1 || wait_counter(a.tile_cnt + tl, static_cast<unsigned>(n - 1), ctx, 23);
+      sh.flag[0] = ok ? 1 : 0;
+      a.tile_cnt[tl] = 0u;
     }
     named_bar(bar, nthr);
     if (!sh.flag[0]) return;
     __threadfence();
-    // every partial, this CTA's included, is read back from the workspace in
-    // CTA order: the sum does not depend on which CTA arrived last
-    ordered_sum4(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb,
-                 sh.flag[3], nel / 4, nthr, ct);
-    if (ct == 0) {
-      a.tile_cnt[tl] = 0u;
-      trace_stamp(ctx, c, TR_REDUCE);
-    }
+    // this CTA's partial (first in CTA order) plus the others' in CTA order:
+    // the sum does not depend on which CTA finished when
+    ordered_sum4(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb + 1,
+                 sh.flag[3] - 1, nel / 4, nthr, ct);
+    if (ct == 0) trace_stamp(ctx, c, TR_REDUCE);
     named_bar(bar, nthr);
   }
   const int tg = a.t_base + tl;
@@ -1552,34 +1560,43 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
     const bool whole = (blk_a == 0 && blk_b == a.NB);
     if (!whole) {
       const long long ps = static_cast<long long>(p) * a.NB;
-      // slot 0: the pair where this CTA's range begins; slot 1: a later pair
-      // (the range's last one), matching sk_contributors
-      const int slot = (u0 >= ps) ? 0 : 1;
       const size_t part = static_cast<size_t>(QRp) * 129;
-      float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
-      for (int e4 = ct; e4 < QRp * 32; e4 += 256)
-        reinterpret_cast<float4*>(mine)[e4] =
-            *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
-      for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
-      __threadfence();
-      named_bar(1, 256);
-      if (ct == 0) {
+      // The CTA whose range holds the pair's first block reaches its part of
+      // the pair last (that part ends its range): it combines.  The others
+      // publish their partial (slot 0: it is the first segment of their
+      // range) and add an arrival.
+      if (u0 > ps) {
+        float* mine = a.ws + static_cast<size_t>(c * 2) * part;
+        for (int e4 = ct; e4 < QRp * 32; e4 += 256)
+          reinterpret_cast<float4*>(mine)[e4] =
+              *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
+        for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
+        __threadfence();
+        named_bar(1, 256);
+        if (ct == 0) {
+          atomicAdd(a.pair_cnt + p, 1u);
+          flag[0] = 0;
+        }
+      } else if (ct == 0) {
         const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
         flag[1] = n;
-        const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
-        flag[0] = (old + 1 == static_cast<unsigned>(n)) ? 1 : 0;
+        const bool ok = n <= 1 || wait_counter(a.pair_cnt + p, static_cast<unsigned>(n - 1), ctx, 36);
+        a.pair_cnt[p] = 0u;
+        flag[0] = ok ? 1 : -1;
       }
       named_bar(1, 256);
+      if (flag[0] < 0) return -1;
       if (flag[0]) {
         __threadfence();
         const int nc = flag[1];
-        // lse table [nc][QRp] of every partial (this CTA's included), loaded
-        // cooperatively into the idle Q buffer (one round trip), then per-row
-        // weights w_j = 2^(lse_j - max) and 1 / sum_j w_j
+        // lse table [nc][QRp] of every partial (this CTA's first, from shared
+        // memory), loaded cooperatively into the idle Q buffer (one round
+        // trip), then per-row weights w_j = 2^(lse_j - max) and 1 / sum_j w_j
         float* wt = reinterpret_cast<float*>(Qs);
         for (int e = ct; e < nc * QRp; e += 256) {
           const int j = e / QRp, rr = e % QRp;
-          wt[e] = __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
+          wt[e] = j == 0 ? row_lse[rr]
+                         : __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
         }
         named_bar(1, 256);
         for (int rr = ct; rr < QRp; rr += 256) {
@@ -1610,12 +1627,16 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
             float4 v[4][4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
+              const int j = j0 + jj;
               const float4* src = reinterpret_cast<const float4*>(
-                  a.ws + static_cast<size_t>(ctb[j0 + jj < nc ? j0 + jj : 0]) * part);
+                  a.ws + static_cast<size_t>(ctb[j > 0 && j < nc ? j : 1 % nc]) * part);
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const int e4 = ct + (q0 + q) * 256;
-                v[jj][q] = (j0 + jj < nc && e4 < nel4) ? __ldcg(src + e4) : z;
+                if (j == 0)
+                  v[jj][q] = e4 < nel4 ? *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4) : z;
+                else
+                  v[jj][q] = (j < nc && e4 < nel4) ? __ldcg(src + e4) : z;
               }
             }
 #pragma unroll
@@ -1643,10 +1664,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
             }
           }
         }
-        if (ct == 0) {
-          a.pair_cnt[p] = 0u;
-          trace_stamp(ctx, c, TR_REDUCE);
-        }
+        if (ct == 0) trace_stamp(ctx, c, TR_REDUCE);
         named_bar(1, 256);
       }
     }
