@@ -289,6 +289,17 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   return op;
 }
 
+// CTAs of the split-KV attention: a whole number of CTAs per (request, kv
+// head) pair when the pairs are fewer than the SMs, so that no CTA's range
+// straddles two pairs (a straddling CTA merges and publishes mid-range and
+// holds up both pairs' combines); at most 62 per pair (the combine's weights
+// sit in two lanes of a warp); never more than the units.
+int dl::attn_ctas(int pairs, int nb, int sms) {
+  const long long U = static_cast<long long>(pairs) * nb;
+  long long g = pairs <= sms ? static_cast<long long>(pairs) * std::min(62, sms / pairs) : sms;
+  return static_cast<int>(std::max(1LL, std::min(g, U)));
+}
+
 static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   LaunchOp op;
   std::memset(&op.args, 0, sizeof(op.args));
@@ -313,11 +324,7 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.QR = p->T * (p->Hq / p->Hkv);
   a.QRp = a.QR <= 16 ? 16 : (a.QR <= 32 ? 32 : 64);
   a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
-  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  // at most ~62 CTAs may share one (request, kv head) stream: the combine's
-  // weight table holds 64 contributors
-  a.G = static_cast<int>(std::min<long long>(std::min<long long>(p->sms, U),
-                                             62LL * a.R * a.Hkv));
+  a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms);
   // 4 stages of 32 KiB keep the KV stream at full rate (more adds nothing)
   a.stages = std::max(2, std::min(4, (kGemmSmemTarget - attn_smem_bytes(a.QRp, 0)) /
                                          (4 * kAttnKeys * 128)));

@@ -41,7 +41,7 @@ enum BindingSlot : int {
   NUM_SLOTS = 8
 };
 
-struct alignas(64) Binding {
+struct alignas(128) Binding {
   void* p[NUM_SLOTS];
   // TMA descriptor of the bound KV cache viewed as [rows, head_dim] bf16
   // (rows = layers * pages * 2 * kv_heads * page_size), 128-byte swizzle,

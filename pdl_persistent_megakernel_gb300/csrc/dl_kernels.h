@@ -14,6 +14,9 @@ const void* mega_kernel();
 cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s);
 int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M);
 int attn_smem_bytes(int QRp, int stages);
+// CTAs of a split-KV attention over `pairs` (request, kv head) streams of
+// `nb` 64-key blocks on `sms` SMs (dl_host.cu).
+int attn_ctas(int pairs, int nb, int sms);
 int norm_smem_bytes();
 cudaError_t launch_test_kv_write(const void* src, void* kv, const int* bt, const int* pos,
                                  int layer, int M, int T, int Hkv, int d, int P,

@@ -179,8 +179,7 @@ extern "C" dl_status dl_attention_noalloc(const dl_config* c, int layer, const v
   a.QRp = QR <= 16 ? 16 : (QR <= 32 ? 32 : 64);
   a.NB = (c->max_context + kAttnKeys - 1) / kAttnKeys;
   const int sms = c->num_sms > 0 ? std::min(c->num_sms, d->sms) : d->sms;
-  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  a.G = static_cast<int>(std::min<long long>(std::min<long long>(sms, U), 62LL * pairs));
+  a.G = attn_ctas(pairs, a.NB, sms);
   a.stages = attn_stages(a.QRp);
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.d)));
   const size_t need = kPartialOff + static_cast<size_t>(a.G) * 2 * a.QRp * 129 * sizeof(float);

@@ -1247,6 +1247,29 @@ __device__ __forceinline__ uint8_t* attn_v(const Pipe& P, int i) {
   return attn_k(P, i) + 2 * kAttnKeys * 128;
 }
 
+// One query row of the attention output (warp-wide: lane l holds columns
+// 4 l .. 4 l + 3): bf16, or e4m3 codes with the row's scale (the O
+// projection's input quantised per token per 128-group).
+__device__ __forceinline__ void attn_write_row(const AttnArgs& a, int r, int h, int G, int rr,
+                                               float4 v, int lane) {
+  const int t = rr / G, g = rr % G;
+  const size_t m = static_cast<size_t>(r) * a.T + t;
+  const int hq = h * G + g;
+  if (!a.fp8) {
+    uint16_t* out = static_cast<uint16_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+  } else {
+    const float am = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    const float sc = am > 0.f ? am / 448.f : 1.f;
+    const uint32_t code = static_cast<uint32_t>(f2e4m3(v.x / sc)) |
+                          (static_cast<uint32_t>(f2e4m3(v.y / sc)) << 8) |
+                          (static_cast<uint32_t>(f2e4m3(v.z / sc)) << 16) |
+                          (static_cast<uint32_t>(f2e4m3(v.w / sc)) << 24);
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4) = code;
+    if (lane == 0) a.out_scale[m * a.Hq + hq] = sc;
+  }
+}
+
 // Consumer side of an attention share (warps 1-8): `priv` is the share's
 // private shared memory (layout attn_smem_layout(QRp, 0)).  Returns the
 // number of key blocks it consumed (the blocks below each pair's context),
@@ -1270,7 +1293,6 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   int* row_pos = reinterpret_cast<int*>(row_w + QRp);
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
   int* ctb = flag + 16 + 32 * 4 + 64;     // [kMaxContrib] combine contributors
-  float* cw = reinterpret_cast<float*>(ctb + kMaxContrib);  // [kMaxContrib] weights
   const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
@@ -1299,6 +1321,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   const int qr = lane >> 2, qc = lane & 3;  // fragment row / column pair
   bool dead = false;
   int i = 0;                               // valid-unit counter (matches producer)
+  int pend[2], npend = 0;                  // pairs this CTA shares (first / last)
   long long u = u0;
   while (u < u1) {
     const int p = static_cast<int>(u / a.NB);
@@ -1556,142 +1579,97 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       }
       named_bar(1, 256);
     }
-    if (ct == 0) trace_stamp(ctx, c, TR_LOOP_END);
     const bool whole = (blk_a == 0 && blk_b == a.NB);
     if (!whole) {
+      // publish this pair's partial (slot 0: the pair where this CTA's range
+      // begins; slot 1: a later pair, the range's last one) and an arrival;
+      // the pair is combined once this CTA's range is done (below)
       const long long ps = static_cast<long long>(p) * a.NB;
+      const int slot = (u0 >= ps) ? 0 : 1;
       const size_t part = static_cast<size_t>(QRp) * 129;
-      // The CTA whose range holds the pair's first block reaches its part of
-      // the pair last (that part ends its range): it combines.  The others
-      // publish their partial (slot 0: it is the first segment of their
-      // range) and add an arrival.
-      if (u0 > ps) {
-        float* mine = a.ws + static_cast<size_t>(c * 2) * part;
-        for (int e4 = ct; e4 < QRp * 32; e4 += 256)
-          reinterpret_cast<float4*>(mine)[e4] =
-              *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
-        for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
-        __threadfence();
-        named_bar(1, 256);
-        if (ct == 0) {
-          atomicAdd(a.pair_cnt + p, 1u);
-          flag[0] = 0;
-        }
-      } else if (ct == 0) {
-        const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
-        flag[1] = n;
-        const bool ok = n <= 1 || wait_counter(a.pair_cnt + p, static_cast<unsigned>(n - 1), ctx, 36);
-        a.pair_cnt[p] = 0u;
-        flag[0] = ok ? 1 : -1;
-      }
+      float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
+      for (int e4 = ct; e4 < QRp * 32; e4 += 256)
+        reinterpret_cast<float4*>(mine)[e4] =
+            *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
+      for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
+      __threadfence();
       named_bar(1, 256);
-      if (flag[0] < 0) return -1;
-      if (flag[0]) {
-        __threadfence();
-        const int nc = flag[1];
-        // lse table [nc][QRp] of every partial (this CTA's first, from shared
-        // memory), loaded cooperatively into the idle Q buffer (one round
-        // trip), then per-row weights w_j = 2^(lse_j - max) and 1 / sum_j w_j
-        float* wt = reinterpret_cast<float*>(Qs);
-        for (int e = ct; e < nc * QRp; e += 256) {
-          const int j = e / QRp, rr = e % QRp;
-          wt[e] = j == 0 ? row_lse[rr]
-                         : __ldcg(a.ws + static_cast<size_t>(ctb[j]) * part + QRp * 128 + rr);
-        }
-        named_bar(1, 256);
-        for (int rr = ct; rr < QRp; rr += 256) {
-          float mx = -INFINITY;
-          for (int j = 0; j < nc; ++j) mx = fmaxf(mx, wt[j * QRp + rr]);
-          row_w[rr] = mx;
-        }
-        named_bar(1, 256);
-        for (int e = ct; e < nc * QRp; e += 256) {
-          const float mx = row_w[e % QRp];
-          wt[e] = (mx == -INFINITY) ? 0.f : exp2f(wt[e] - mx);
-        }
-        named_bar(1, 256);
-        for (int rr = ct; rr < QRp; rr += 256) {
-          float den = 0.f;
-          for (int j = 0; j < nc; ++j) den += wt[j * QRp + rr];
-          cw[rr] = den > 0.f ? 1.f / den : 0.f;
-        }
-        named_bar(1, 256);
-        // O = sum_j w_j O_j / sum_j w_j: 4 contributors x 4 float4s in flight
-        const int nel4 = QRp * 32;
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = 0; q0 * 256 < nel4; q0 += 4) {
-          float4 acc[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[q] = z;
-          for (int j0 = 0; j0 < nc; j0 += 4) {
-            float4 v[4][4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int j = j0 + jj;
-              const float4* src = reinterpret_cast<const float4*>(
-                  a.ws + static_cast<size_t>(ctb[j > 0 && j < nc ? j : 1 % nc]) * part);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int e4 = ct + (q0 + q) * 256;
-                if (j == 0)
-                  v[jj][q] = e4 < nel4 ? *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4) : z;
-                else
-                  v[jj][q] = (j < nc && e4 < nel4) ? __ldcg(src + e4) : z;
-              }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              if (j0 + jj >= nc) break;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int e4 = ct + (q0 + q) * 256;
-                const int rr = (e4 < nel4 ? e4 : 0) >> 5;
-                const float wgt = wt[(j0 + jj) * QRp + rr];
-                acc[q].x = fmaf(wgt, v[jj][q].x, acc[q].x);
-                acc[q].y = fmaf(wgt, v[jj][q].y, acc[q].y);
-                acc[q].z = fmaf(wgt, v[jj][q].z, acc[q].z);
-                acc[q].w = fmaf(wgt, v[jj][q].w, acc[q].w);
-              }
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int e4 = ct + (q0 + q) * 256;
-            if (e4 < nel4) {
-              const float inv = cw[e4 >> 5];
-              *reinterpret_cast<float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4) =
-                  make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
-            }
-          }
-        }
-        if (ct == 0) trace_stamp(ctx, c, TR_REDUCE);
-        named_bar(1, 256);
-      }
-    }
-    if (whole || flag[0]) {
-      // write the attention output, one warp per query row
-      for (int rr = wc; rr < a.QR; rr += 8) {
-        const int t = rr / G, g = rr % G;
-        const size_t m = static_cast<size_t>(r) * a.T + t;
-        const int hq = h * G + g;
-        const float4 v = *reinterpret_cast<const float4*>(Ob + rr * kOP + lane * 4);
-        if (!a.fp8) {
-          uint16_t* out = static_cast<uint16_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4;
-          *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
-        } else {
-          const float am = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-          const float sc = am > 0.f ? am / 448.f : 1.f;
-          const uint32_t code = static_cast<uint32_t>(f2e4m3(v.x / sc)) |
-                                (static_cast<uint32_t>(f2e4m3(v.y / sc)) << 8) |
-                                (static_cast<uint32_t>(f2e4m3(v.z / sc)) << 16) |
-                                (static_cast<uint32_t>(f2e4m3(v.w / sc)) << 24);
-          *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out) + (m * a.Hq + hq) * 128 + lane * 4) = code;
-          if (lane == 0) a.out_scale[m * a.Hq + hq] = sc;
-        }
-      }
+      if (ct == 0) atomicAdd(a.pair_cnt + p, 1u);
+      pend[npend++] = p;
+    } else {
+      // the whole pair is this CTA's: write the attention output, one warp
+      // per query row
+      for (int rr = wc; rr < a.QR; rr += 8)
+        attn_write_row(a, r, h, G, rr, *reinterpret_cast<const float4*>(Ob + rr * kOP + lane * 4), lane);
     }
     named_bar(1, 256);
     u = run_end;
+  }
+  if (ct == 0) trace_stamp(ctx, c, TR_LOOP_END);
+  // ---- split-KV combine, shared by all CTAs of a pair: once every partial
+  // of the pair is published, contributor j (CTA order) combines query rows
+  // [j * per, (j + 1) * per) by their log-sum-exp weights, in CTA order, and
+  // writes them (one warp per row).  The pair's counter counts the n
+  // publications, then the n finished slices; the last slice resets it.
+  for (int k = 0; k < npend; ++k) {
+    const int p = pend[k];
+    const long long ps = static_cast<long long>(p) * a.NB;
+    const int r = p / a.Hkv, h = p % a.Hkv;
+    const size_t part = static_cast<size_t>(QRp) * 129;
+    if (ct == 0) {
+      const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
+      int j = 0;
+      while (j < n && (ctb[j] >> 1) != c) ++j;
+      flag[1] = n;
+      flag[3] = j;
+      flag[0] = wait_counter(a.pair_cnt + p, static_cast<unsigned>(n), ctx, 36) ? 1 : -1;
+    }
+    named_bar(1, 256);
+    if (flag[0] < 0) return -1;
+    __threadfence();
+    const int n = flag[1], jme = flag[3];
+    const int per = (a.QR + n - 1) / n;
+    const int r1 = min(a.QR, (jme + 1) * per);
+    for (int rr = jme * per + wc; rr < r1; rr += 8) {
+      // lane j holds contributor j's weight (j < 32, then j + 32)
+      float l0 = -INFINITY, l1 = -INFINITY;
+      if (lane < n) l0 = __ldcg(a.ws + static_cast<size_t>(ctb[lane]) * part + QRp * 128 + rr);
+      if (lane + 32 < n) l1 = __ldcg(a.ws + static_cast<size_t>(ctb[lane + 32]) * part + QRp * 128 + rr);
+      const float mx = warp_max(fmaxf(l0, l1));
+      const float w0 = (mx == -INFINITY || lane >= n) ? 0.f : exp2f(l0 - mx);
+      const float w1 = (mx == -INFINITY || lane + 32 >= n) ? 0.f : exp2f(l1 - mx);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj < n ? j0 + jj : 0;
+          v[jj] = __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<size_t>(ctb[j]) * part +
+                                                          static_cast<size_t>(rr) * 128) + lane);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const float wsrc = __shfl_sync(0xffffffffu, j < 32 ? w0 : w1, j & 31);
+          if (j < n) {
+            den += wsrc;
+            acc.x = fmaf(wsrc, v[jj].x, acc.x);
+            acc.y = fmaf(wsrc, v[jj].y, acc.y);
+            acc.z = fmaf(wsrc, v[jj].z, acc.z);
+            acc.w = fmaf(wsrc, v[jj].w, acc.w);
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      attn_write_row(a, r, h, G, rr, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv), lane);
+    }
+    named_bar(1, 256);
+    if (ct == 0) {
+      const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
+      if (old + 1 == 2u * static_cast<unsigned>(n)) a.pair_cnt[p] = 0u;
+      trace_stamp(ctx, c, TR_REDUCE);
+    }
   }
   if (ct == 0) trace_stamp(ctx, c, TR_END);
   return i;
@@ -1702,26 +1680,14 @@ template <int kNMT>
 __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
                           const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int QRp = a.QRp, G = a.Hq / a.Hkv;
-  constexpr int nmt = kNMT;
-  constexpr int kXS = nmt * 8;   // partial-score floats per thread
+  const int QRp = a.QRp;
   const AttnSmem L = attn_smem_layout(QRp, a.stages);
   uint8_t* stage0 = smem;
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem + L.q_off);
-  float* Ob = reinterpret_cast<float*>(smem + L.o_off);
-  float* xs = reinterpret_cast<float*>(smem + L.xs_off);
-  float* kg_m = reinterpret_cast<float*>(smem + L.stat_off);   // [4][QRp]
-  float* kg_l = kg_m + 4 * QRp;                                 // [4][QRp]
-  float* row_lse = kg_l + 4 * QRp;
-  float* row_w = row_lse + QRp;
-  int* row_pos = reinterpret_cast<int*>(row_w + QRp);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kMaxStages;
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
   int* pgbuf = flag + 16;                 // [32][4] pages of the producer's batch
   int* ppos = pgbuf + 32 * 4;             // [64] token positions (producer)
-  int* ctb = ppos + 64;                   // [kMaxContrib] combine contributors
-  float* cw = reinterpret_cast<float*>(ctb + kMaxContrib);  // [kMaxContrib] weights
   const int S = a.stages;
   const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
