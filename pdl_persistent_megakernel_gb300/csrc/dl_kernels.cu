@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
           seq += static_cast<uint32_t>((n + ups - 1) / ups);
           if (op.gemm.mma) {
             tseq += static_cast<uint32_t>(n);
-            rseq += static_cast<uint32_t>(gemm_share_runs(op.gemm, cta));
+            rseq += static_cast<uint32_t>(gemm_share_handoffs(op.gemm, cta));
           }
           break;
         }

@@ -257,7 +257,9 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) : 0);
   L.bar_off = (L.bar_off + 15) & ~15;
   L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 4) * 8;
-  L.total = L.misc_off + 256 + kMaxContrib * 4;
+  // two control areas (flags + contributor list): the fix-up warps' and the
+  // epilogue warps' (which finish the last tile themselves)
+  L.total = L.misc_off + 2 * (256 + kMaxContrib * 4);
   return L;
 }
 
@@ -277,6 +279,8 @@ struct GemmShared {
   uint64_t* tfree;   // [2] tile buffer b finished and free (2 fix-up warps)
   int* flag;      // [4]
   int* ctb;       // [kMaxContrib] contributor list of a fix-up
+  int* flag2;     // the epilogue warps' own control area (last tile)
+  int* ctb2;
 };
 
 // dst (the first partial) plus `nc` fp32 partials (float4 granular, nel4
@@ -929,6 +933,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         const long long u = u0 + i;
         const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
         const int run = min(nunits - i, a.KB - kb0);
+        if (i + run == nunits) break;   // the epilogue warps finish the last tile
         const int b = static_cast<int>(rq % ntb);
         if (!warp_wait(&sh.tready[b], (rq / ntb) & 1, ctx, 18)) return;
         if (aborted(ctx.status)) return;
@@ -940,7 +945,6 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         i += run;
         ++rq;
       }
-      if (ft == 0) trace_stamp(ctx, c, TR_END);
       return;
     }
     if (warp < 5) {
@@ -1023,11 +1027,22 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           if (m < a.M) tout[(p * a.Mp + m) * 128 + row] = acc[p][m];
       }
       if (et == 0 && i == nunits) trace_stamp(ctx, c, TR_LOOP_END);
+      if (i == nunits) {
+        // the last tile: finished here, 128 threads, own control area (the
+        // fix-up warps may still be on the previous one)
+        named_bar(2, 128);
+        GemmShared shl = sh;
+        shl.tout = tout;
+        shl.flag = sh.flag2;
+        shl.ctb = sh.ctb2;
+        gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, shl);
+        break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.tready[b]);
       ++rq;
     }
-    // the fix-up warps finish the last tile; the share ends when they do
+    if (et == 0) trace_stamp(ctx, c, TR_END);
   }
 }
 
@@ -1052,6 +1067,8 @@ __device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* sm
   sh.tfree = sh.tready + 2;
   sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
   sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
+  sh.flag2 = reinterpret_cast<int*>(smem + L.misc_off + 256 + kMaxContrib * 4);
+  sh.ctb2 = sh.flag2 + 64;
   return sh;
 }
 
@@ -2085,11 +2102,12 @@ __device__ __forceinline__ int gemm_share_units(const GemmArgs& a, int c) {
   return static_cast<int>(sk_begin(U, a.G, c + 1) - sk_begin(U, a.G, c));
 }
 
-// Tile runs of GEMM share c (tiles its range touches).
-__device__ __forceinline__ int gemm_share_runs(const GemmArgs& a, int c) {
+// Tiles GEMM share c hands to its fix-up warps: every tile its range
+// touches but the last (which the epilogue warps finish themselves).
+__device__ __forceinline__ int gemm_share_handoffs(const GemmArgs& a, int c) {
   const long long U = static_cast<long long>(a.NT) * a.KB;
   const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
-  return u1 > u0 ? static_cast<int>((u1 - 1) / a.KB - u0 / a.KB + 1) : 0;
+  return u1 > u0 ? static_cast<int>((u1 - 1) / a.KB - u0 / a.KB) : 0;
 }
 
 }  // namespace dl
