@@ -865,7 +865,10 @@ static dl_status build_plan(dl_plan* p) {
     CK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->dev));
     const int avail = optin - static_cast<int>(fa.sharedSizeBytes) - 1024 - priv;
     p->mega_ns = std::min(kMaxSlots, avail / slot);
-    if (p->mega_ns < 4) return fail(DL_ERR_PLAN_INVALID, "megakernel ring has fewer than 4 slots");
+    // two slots suffice for progress (the producer issues every pending
+    // activation slice before it waits for a slot); fewer cannot hold a unit
+    // while the next one streams in
+    if (p->mega_ns < 2) return fail(DL_ERR_PLAN_INVALID, "megakernel ring has fewer than 2 slots");
     p->mega_slot = slot;
     p->mega_priv_off = p->mega_ns * slot;
     p->mega_smem = 1024 + p->mega_priv_off + priv;

@@ -76,6 +76,28 @@ def as_u8_np(u8, shape):
     return u8.numpy()[:int(np.prod(shape))].reshape(shape)
 
 
+def check_mlp_stagewise(case, plan, out, what=""):
+    """bf16 layer: the gate/up + SiLU*mul and down projections, each given
+    the GPU's own input (the oracle's operations applied to the GPU's h2 and
+    SiLU*mul output), element-wise within the bf16 tolerance.  End to end the
+    two chains differ by one-ulp bf16 rounding flips (fp32 versus fp64
+    accumulation next to a rounding boundary), and a K = 12288 down
+    projection sums a thousand of them; per operation no such flip exists."""
+    cfg = case.cfg
+    M, H, I = cfg.M, cfg.hidden, cfg.inter
+    lw = case.w["layers"][cfg.n_layers - 1]
+    h2 = as_bf16_np(read_debug(plan, "h2"), (M, H))
+    act = as_bf16_np(read_debug(plan, "act"), (M, I))
+    gu = oracle.gemm_bf16(f64(h2), synth.as_u16(lw["w_gate_up"]))
+    g = f64(oracle.bf16_from_double(gu[:, :I]))
+    u = f64(oracle.bf16_from_double(gu[:, I:]))
+    act_want = oracle.bf16_from_double(oracle.silu(g) * u)
+    bf16_close(act, act_want, f"{what} silu*mul given the GPU's h2")
+    y = out[0].view(torch.int16).cpu().numpy().view(np.uint16)
+    y_want = oracle.bf16_from_double(oracle.gemm_bf16(f64(act), synth.as_u16(lw["w_down"])))
+    bf16_close(y, y_want, f"{what} down projection given the GPU's act")
+
+
 class Case:
     """Inputs + oracle result of one configuration (computed once)."""
 
