@@ -194,6 +194,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--per-kernel", action="store_true", default=True)
+    ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
+                    help="flush: a 256 MiB write before every step; stream: steps back to "
+                         "back (each step reads more bytes than the 129 MB L2 holds)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
@@ -238,13 +241,15 @@ def main():
     def timed_steps(mode, k, w_):
         with torch.cuda.stream(stream):
             for _ in range(w_):
-                flush.zero_()
+                if args.l2 == "flush":
+                    flush.zero_()
                 plan.step(x, res, kv, bt, pos, out, mode, stream)
             barrier()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(k)]
             for a, b in evs:
-                flush.zero_()
+                if args.l2 == "flush":
+                    flush.zero_()
                 a.record(stream)
                 plan.step(x, res, kv, bt, pos, out, mode, stream)
                 b.record(stream)
@@ -364,7 +369,8 @@ def main():
                        "tokens_per_request": cfg.tokens_per_request, "context": cfg.context,
                        "page_size": cfg.page_size,
                        "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16",
-                       "algorithmic_bytes": algo, "l2": "256 MiB write between timed steps",
+                       "algorithmic_bytes": algo, "l2": ("256 MiB write between timed steps" if args.l2 == "flush" else
+                              "no flush: each step reads more than L2 holds"),
                        "replicas": ws},
             "us_per_layer": r["us"] / cfg.n_layers,
             "frac_of_8TBs": r["frac_of_8TBs"],

@@ -192,6 +192,12 @@ __device__ __forceinline__ void fence_tmap_acquire(const CUtensorMap* m) {
                : "memory");
 }
 
+// Prefetch one box of a tensor map into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(map), "r"(c0), "r"(c1) : "memory");
+}
+
 // 2-D tiled load: box at element coordinates (c0 inner, c1 outer).  c0 * the
 // element size is always a multiple of 128 bytes here (one swizzle atom).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,

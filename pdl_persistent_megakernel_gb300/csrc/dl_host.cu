@@ -111,6 +111,7 @@ struct dl_plan {
   int dev = 0, sms = 0, M = 0, Mp = 0, Mrows = 0, H = 0, I = 0, Hq = 0, Hkv = 0, d = 0;
   int L = 0, V = 0, R = 0, T = 0, P = 0;
   bool fp8 = false, full = false, mma = false;
+  int pf_units = 4;    // L2 prefetch units per share (DL_L2_PREFETCH_UNITS; 0: off)
   unsigned long long budget_ns = 1000000000ull;
 
   std::vector<void*> allocs;
@@ -800,6 +801,48 @@ static dl_status build_plan(dl_plan* p) {
     p->dag.push_back(lop);
   }
   if (cpos > p->n_counters) return fail(DL_ERR_CUDA, "counter pool overflow");
+
+  // the kernels split units with 32-bit arithmetic: units x CTAs < 2^32
+  for (const auto* list : {&p->lin, &p->dag})
+    for (const LaunchOp& op : *list) {
+      long long U = 0, G = 1;
+      if (op.args.kind == OP_GEMM) {
+        U = static_cast<long long>(op.args.gemm.NT) * op.args.gemm.KB;
+        G = op.args.gemm.G;
+      } else if (op.args.kind == OP_ATTN) {
+        U = static_cast<long long>(op.args.attn.R) * op.args.attn.Hkv * op.args.attn.NB;
+        G = op.args.attn.G;
+      }
+      if (U * G >= (1LL << 32)) return fail(DL_ERR_PLAN_INVALID, "too many work units for one op");
+    }
+  if (const char* e = std::getenv("DL_L2_PREFETCH_UNITS")) p->pf_units = std::atoi(e);
+  // L2 prefetch: a norm, an attention or a projection directly followed (on
+  // the same stream) by a projection warms L2 with the weight tiles that
+  // projection's first stages load, once its own loads are out
+  for (auto* list : {&p->lin, &p->dag})
+    for (size_t i = 0; i + 1 < list->size(); ++i) {
+      LaunchOp& cur = (*list)[i];
+      const LaunchOp& nx = (*list)[i + 1];
+      if (nx.args.kind != OP_GEMM || nx.branch != 0 || cur.branch != 0) continue;
+      const GemmArgs& g = nx.args.gemm;
+      PrefetchSpec pf;
+      pf.tmap = g.tmap_w;
+      pf.NT = g.NT;
+      pf.KB = g.KB;
+      pf.G = g.G;
+      pf.t_base = g.t_base;
+      pf.pair = g.pair;
+      pf.up_row = g.up_row;
+      pf.kel = 128 / (g.fp8 ? 1 : 2);
+      // 4 units (64 KiB, or 128 KiB of gate + up) per share measured best:
+      // enough to cover the hand-over, little enough not to queue ahead of
+      // the boundary's own latency-bound reads
+      pf.units = std::max(0, p->pf_units);
+      if (pf.units == 0) pf.tmap = nullptr;
+      if (cur.args.kind == OP_NORM) cur.args.norm.pf = pf;
+      else if (cur.args.kind == OP_ATTN) cur.args.attn.pf = pf;
+      else if (cur.args.kind == OP_GEMM) cur.args.gemm.pf = pf;
+    }
 
   // kernel attributes: dynamic shared memory (the largest user of each kernel)
   int max_smem = 0;

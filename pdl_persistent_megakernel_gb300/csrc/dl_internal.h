@@ -89,6 +89,15 @@ enum Epilogue : int {
   EPI_LOGITS = 3,     // fp32 logits + greedy argmax (lowest index on ties)
 };
 
+// L2 prefetch of the first weight tiles the next projection's share with a
+// given CTA index will stream (tmap == NULL: none).  Issued by the current
+// kernel once its own loads are out, so that the next kernel's first loads
+// hit L2.
+struct PrefetchSpec {
+  const CUtensorMap* tmap;    // the next projection's weights
+  int NT, KB, G, t_base, pair, up_row, kel, units;
+};
+
 struct NormArgs {
   DPtr x, res;        // bf16 [M, H]
   DPtr r_out;         // bf16 [M, H] new residual
@@ -97,6 +106,7 @@ struct NormArgs {
   float* h_scale;     // FP8: [M, H/128]
   int fp8, M, H, rows_per_cta;
   float eps;
+  PrefetchSpec pf;
 };
 
 struct GemmArgs {
@@ -140,6 +150,7 @@ struct GemmArgs {
   float* best_val;            // [NT][M]
   int* best_idx;              // [NT][M]
   DPtr ids;                   // int32 [M]
+  PrefetchSpec pf;
 };
 
 struct AttnArgs {
@@ -156,6 +167,7 @@ struct AttnArgs {
   float scale_log2;           // log2(e) / sqrt(d)
   float* ws;                  // partials [G][2][QRp][d] + lse [G][2][QRp]
   unsigned* pair_cnt;         // [R * Hkv]
+  PrefetchSpec pf;
 };
 
 struct OpArgs {

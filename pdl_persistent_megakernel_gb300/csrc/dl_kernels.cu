@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
   R.full = ring_full;
   R.empty = ring_empty;
   R.slot_bytes = static_cast<uint32_t>(m.slot_bytes);
-  R.ns = static_cast<uint32_t>(m.ns);
+  pipe_set_ns(R, static_cast<uint32_t>(m.ns));
   R.seq0 = 0;
   R.ups = 1;
   R.x_bytes = 0;
@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
           TmemRing TR;
           TR.base = tmem;
           TR.nbuf = 4;
+          TR.nbuf_magic = fdiv_magic(4u);
           TR.stride = 128;
           TR.seq0 = tseq;
           TR.rseq0 = rseq;

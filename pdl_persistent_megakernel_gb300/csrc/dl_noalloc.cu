@@ -180,6 +180,8 @@ extern "C" dl_status dl_attention_noalloc(const dl_config* c, int layer, const v
   a.NB = (c->max_context + kAttnKeys - 1) / kAttnKeys;
   const int sms = c->num_sms > 0 ? std::min(c->num_sms, d->sms) : d->sms;
   a.G = attn_ctas(pairs, a.NB, sms);
+  if (static_cast<long long>(pairs) * a.NB * a.G >= (1LL << 32))
+    return err(DL_ERR_UNSUPPORTED, "num_requests * n_kv_heads * blocks * CTAs >= 2^32");
   a.stages = attn_stages(a.QRp);
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.d)));
   const size_t need = kPartialOff + static_cast<size_t>(a.G) * 2 * a.QRp * 129 * sizeof(float);

@@ -89,17 +89,34 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ------------------------------------------------------ Stream-K ranges
-__device__ __forceinline__ long long sk_begin(long long U, int G, int c) {
-  return (U * c) / G;
+// Unit counts stay below 2^32 / G (checked when a plan is made), so the
+// range arithmetic is 32-bit: 64-bit division is a long emulated sequence.
+__device__ __forceinline__ int sk_begin(int U, int G, int c) {
+  return static_cast<int>((static_cast<unsigned>(U) * static_cast<unsigned>(c)) /
+                          static_cast<unsigned>(G));
 }
 
 // The CTA whose range holds unit x (the last CTA whose range starts <= x).
-__device__ __forceinline__ int sk_owner(long long U, int G, long long x) {
-  int c = static_cast<int>((x * G) / U);
+__device__ __forceinline__ int sk_owner(int U, int G, int x) {
+  int c = static_cast<int>((static_cast<unsigned>(x) * static_cast<unsigned>(G)) /
+                           static_cast<unsigned>(U));
   if (c >= G) c = G - 1;
   while (c > 0 && sk_begin(U, G, c) > x) --c;
   while (c + 1 < G && sk_begin(U, G, c + 1) <= x) ++c;
   return c;
+}
+
+// L2 prefetch of the first `pf.units` units of the next projection's share
+// c (its weight tiles; the activations do not exist yet).  One thread.
+__device__ __forceinline__ void prefetch_next_share(const PrefetchSpec& pf, int c) {
+  if (!pf.tmap || c >= pf.G) return;
+  const int U = pf.NT * pf.KB;
+  const int u0 = sk_begin(U, pf.G, c), u1 = sk_begin(U, pf.G, c + 1);
+  for (int u = u0; u < u1 && u < u0 + pf.units; ++u) {
+    const int t = pf.t_base + u / pf.KB, kb = u % pf.KB;
+    tma_prefetch_l2_2d(pf.tmap, kb * pf.kel, t * 128);
+    if (pf.pair) tma_prefetch_l2_2d(pf.tmap, kb * pf.kel, pf.up_row + t * 128);
+  }
 }
 
 // =================================================================== NORM
@@ -111,6 +128,13 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
                         const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x;
   if (tid < 32) {
+    // the next projection's first weight tiles (independent of everything)
+    // stream into L2 while this short op runs: share c' is prefetched by
+    // lane (c' / norm CTAs) % 32 of norm CTA c' mod (norm CTAs)
+    if (a.pf.tmap && dep.mode == 0) {
+      const int nc = static_cast<int>(gridDim.x);
+      for (int c2 = c + tid * nc; c2 < a.pf.G; c2 += 32 * nc) prefetch_next_share(a.pf, c2);
+    }
     idle_wait(dep);
     return;
   }
@@ -135,7 +159,8 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   const int m0 = c * a.rows_per_cta;
   const int m1 = min(a.M, m0 + a.rows_per_cta);
   for (int m = m0; m < m1; ++m) {
-    float r[4][8];
+    // r = bf16(x + res), kept as packed bf16 (exact)
+    uint32_t rp[4][4];
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -146,18 +171,18 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
         const uint4 rv = __ldcg(reinterpret_cast<const uint4*>(res + off));
         const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
         const uint32_t rs[4] = {rv.x, rv.y, rv.z, rv.w};
-        uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float a0 = bfround(bf16_lo(xs[e]) + bf16_lo(rs[e]));
           const float a1 = bfround(bf16_hi(xs[e]) + bf16_hi(rs[e]));
-          r[j][2 * e] = a0;
-          r[j][2 * e + 1] = a1;
           ss += a0 * a0 + a1 * a1;
-          o[e] = static_cast<uint32_t>(f2bf(a0)) |
-                 (static_cast<uint32_t>(f2bf(a1)) << 16);
+          rp[j][e] = static_cast<uint32_t>(f2bf(a0)) |
+                     (static_cast<uint32_t>(f2bf(a1)) << 16);
         }
-        *reinterpret_cast<uint4*>(rout + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rout + off) = make_uint4(rp[j][0], rp[j][1], rp[j][2], rp[j][3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rp[j][e] = 0u;
       }
     }
     ss = warp_sum(ss);
@@ -176,8 +201,8 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
         const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          h[2 * e] = r[j][2 * e] * inv * bf16_lo(ws[e]);
-          h[2 * e + 1] = r[j][2 * e + 1] * inv * bf16_hi(ws[e]);
+          h[2 * e] = bf16_lo(rp[j][e]) * inv * bf16_lo(ws[e]);
+          h[2 * e + 1] = bf16_hi(rp[j][e]) * inv * bf16_hi(ws[e]);
         }
       } else {
 #pragma unroll
@@ -335,12 +360,12 @@ __device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_
 // Stream-K bookkeeping shared by the GEMM fix-up and the attention combine:
 // write the list of CTAs whose ranges intersect units [ts, ts + len) (in
 // CTA order, as workspace slot indices c * 2 + slot) and return its size.
-__device__ __forceinline__ int sk_contributors(long long U, int G, long long ts, int len,
+__device__ __forceinline__ int sk_contributors(int U, int G, int ts, int len,
                                                int* ctb) {
   const int cf = sk_owner(U, G, ts), cl = sk_owner(U, G, ts + len - 1);
   int n = 0;
   for (int cc = cf; cc <= cl && n < kMaxContrib; ++cc) {
-    const long long b0 = sk_begin(U, G, cc);
+    const int b0 = sk_begin(U, G, cc);
     if (sk_begin(U, G, cc + 1) <= b0) continue;
     ctb[n++] = cc * 2 + ((b0 >= ts) ? 0 : 1);
   }
@@ -554,15 +579,15 @@ __device__ void epi_logits(const GemmArgs& a, int tg, int tl, const float* tout,
 
 // Finish tile tl (local index; global tg = t_base + tl): Stream-K fix-up,
 // then the epilogue.  tout holds this CTA's sum over its k-blocks.
-__device__ void gemm_finish_tile(const GemmArgs& a, int c, long long u0, int tl,
+__device__ void gemm_finish_tile(const GemmArgs& a, int c, int u0, int tl,
                                  bool full_tile, int npair, int nthr, int ct,
                                  int bar, const KernelCtx& ctx,
                                  const GemmShared& sh) {
   float* tout = sh.tout;
   const int nel = npair * a.Mp * 128;
   if (!full_tile) {
-    const long long U = static_cast<long long>(a.NT) * a.KB;
-    const long long ts = static_cast<long long>(tl) * a.KB;
+    const int U = a.NT * a.KB;
+    const int ts = tl * a.KB;
     // The CTA whose range holds the tile's first unit reaches its part of
     // the tile last (that part ends its range): it finishes the tile.  The
     // others publish their partial early and add an arrival.
@@ -664,41 +689,56 @@ __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShar
 // has one ring for all instructions of a worker, filled in queue order by
 // its producer warp, and seq0 is the ring sequence number of the share's
 // first slot.
+// q / d for q < 2^28 and 2 <= d <= 16: the high word of q * ceil(2^32 / d)
+// (the error q * (ceil(2^32 / d) - 2^32 / d) / 2^32 stays below 1 / d), so
+// the rings never divide by a runtime value.
+__host__ __device__ constexpr uint32_t fdiv_magic(uint32_t d) { return 0xFFFFFFFFu / d + 1u; }
+__device__ __forceinline__ uint32_t fdiv(uint32_t q, uint32_t magic) { return __umulhi(q, magic); }
+
 struct Pipe {
   uint8_t* base;
   uint64_t* full;
   uint64_t* empty;
   uint32_t slot_bytes;
-  uint32_t ns;
+  uint32_t ns;      // slots, >= 2
+  uint32_t ns_magic;
   uint32_t seq0;
-  int ups;          // units per slot
+  int ups;          // units per slot: 1 or 2
   int x_bytes;      // bytes of one unit's activation slice (after the tiles)
   int empty_cnt;    // arrivals that free a slot (1: one MMA commit; 8: 8 warps)
 };
 
 constexpr int kSlotTiles = 32768;   // bytes of weight tiles / K+V per slot
 
+__device__ __forceinline__ void pipe_set_ns(Pipe& P, uint32_t ns) {
+  P.ns = ns;
+  P.ns_magic = fdiv_magic(ns);
+}
+__device__ __forceinline__ int pipe_sub(const Pipe& P, int i) { return i & (P.ups - 1); }
 __device__ __forceinline__ uint32_t pipe_q(const Pipe& P, int i) {
-  return P.seq0 + static_cast<uint32_t>(i / P.ups);
+  return P.seq0 + static_cast<uint32_t>(i >> (P.ups - 1));
+}
+__device__ __forceinline__ uint32_t pipe_idx(const Pipe& P, uint32_t q) {
+  return q - fdiv(q, P.ns_magic) * P.ns;
 }
 __device__ __forceinline__ uint8_t* pipe_slot(const Pipe& P, uint32_t q) {
-  return P.base + (q % P.ns) * P.slot_bytes;
+  return P.base + pipe_idx(P, q) * P.slot_bytes;
 }
-__device__ __forceinline__ uint64_t* pipe_full(const Pipe& P, uint32_t q) { return P.full + q % P.ns; }
-__device__ __forceinline__ uint64_t* pipe_empty(const Pipe& P, uint32_t q) { return P.empty + q % P.ns; }
-__device__ __forceinline__ uint32_t pipe_par(const Pipe& P, uint32_t q) { return (q / P.ns) & 1u; }
+__device__ __forceinline__ uint64_t* pipe_full(const Pipe& P, uint32_t q) { return P.full + pipe_idx(P, q); }
+__device__ __forceinline__ uint64_t* pipe_empty(const Pipe& P, uint32_t q) { return P.empty + pipe_idx(P, q); }
+__device__ __forceinline__ uint32_t pipe_par(const Pipe& P, uint32_t q) { return fdiv(q, P.ns_magic) & 1u; }
 // unit i of n is the last one of its slot: the slot is released after it
 __device__ __forceinline__ bool pipe_last(const Pipe& P, int i, int n) {
-  return (i % P.ups) == P.ups - 1 || i == n - 1;
+  return pipe_sub(P, i) == P.ups - 1 || i == n - 1;
 }
 
 // GEMM unit i: weight tile p (gate / up, or the single tile) and the
 // activation slice.
 __device__ __forceinline__ uint8_t* gemm_w(const Pipe& P, int i, int p) {
-  return pipe_slot(P, pipe_q(P, i)) + ((i % P.ups) + p) * 16384;
+  return pipe_slot(P, pipe_q(P, i)) + (pipe_sub(P, i) + p) * 16384;
 }
 __device__ __forceinline__ uint8_t* gemm_x(const Pipe& P, int i) {
-  return pipe_slot(P, pipe_q(P, i)) + kSlotTiles + (i % P.ups) * P.x_bytes;
+  return pipe_slot(P, pipe_q(P, i)) + kSlotTiles + pipe_sub(P, i) * P.x_bytes;
 }
 
 // A warp waits until unit i's slot is full (all lanes poll, the warp agrees);
@@ -713,7 +753,8 @@ __device__ __forceinline__ bool pipe_warp_wait(const Pipe& P, int i, const Kerne
 // base + b * stride; seq0 counts the accumulations before this share.
 struct TmemRing {
   uint32_t base;
-  int nbuf;
+  int nbuf;         // >= 2
+  uint32_t nbuf_magic;
   int stride;
   uint32_t seq0;
   uint32_t rseq0;   // tile runs handed to the fix-up warps before this share
@@ -746,8 +787,8 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
   constexpr bool kMMA = kMp > 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npair = a.pair ? 2 : 1;
-  const long long U = static_cast<long long>(a.NT) * a.KB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.NT * a.KB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const int nunits = static_cast<int>(u1 - u0);
 
   if constexpr (!kMMA) {
@@ -767,7 +808,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     bool dead = false;
     int i = 0;
     while (i < nunits) {
-      const long long u = u0 + i;
+      const int u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
       const int tg = a.t_base + tl;
@@ -876,7 +917,8 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         }
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
         const int nslots = (nunits + P.ups - 1) / P.ups;
-        long long last_tq = -1;
+        uint32_t last_tq = 0;
+        bool any_tq = false;
         for (int j = w; j < nslots; j += 2) {
           const uint32_t q = P.seq0 + static_cast<uint32_t>(j);
           if (!mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 14)) break;
@@ -884,9 +926,10 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           bool ok = true;
           for (int i = i0; i < i1; ++i) {
             const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
-            const int b = static_cast<int>(tq % TR.nbuf);
+            const uint32_t tqd = fdiv(tq, TR.nbuf_magic);
+            const int b = static_cast<int>(tq - tqd * TR.nbuf);
             if (tq >= static_cast<uint32_t>(TR.nbuf) &&
-                !mbar_wait(&sh.tempty[b], ((tq / TR.nbuf) - 1) & 1, ctx, 15)) {
+                !mbar_wait(&sh.tempty[b], (tqd - 1) & 1, ctx, 15)) {
               ok = false;
               break;
             }
@@ -907,6 +950,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
             }
             umma_commit(&sh.tfull[b]);
             last_tq = tq;
+            any_tq = true;
           }
           if (!ok) break;
           uint64_t* e = pipe_empty(P, q);
@@ -914,8 +958,8 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           if (P.empty_cnt > 1) mbar_arrive_cnt(e, static_cast<uint32_t>(P.empty_cnt - 1));
         }
         // no MMA may still read shared memory or write TMEM when we leave
-        if (last_tq >= 0)
-          mbar_drain(&sh.tfull[last_tq % TR.nbuf], static_cast<uint32_t>(last_tq / TR.nbuf) & 1u,
+        if (any_tq)
+          mbar_drain(&sh.tfull[last_tq % TR.nbuf], (last_tq / TR.nbuf) & 1u,
                      ctx.budget_ns);
       }
       return;
@@ -930,7 +974,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       int i = 0;
       uint32_t rq = TR.rseq0;
       while (i < nunits) {
-        const long long u = u0 + i;
+        const int u = u0 + i;
         const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
         const int run = min(nunits - i, a.KB - kb0);
         if (i + run == nunits) break;   // the epilogue warps finish the last tile
@@ -963,7 +1007,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     int i = 0;
     uint32_t rq = TR.rseq0;
     while (i < nunits) {
-      const long long u = u0 + i;
+      const int u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
       const int tg = a.t_base + tl;
@@ -982,8 +1026,9 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         for (int m = 0; m < kMp; ++m) acc[p][m] = 0.f;
       for (int k = 0; k < run; ++k, ++i) {
         const uint32_t tq = TR.seq0 + static_cast<uint32_t>(i);
-        const int b = static_cast<int>(tq % TR.nbuf);
-        if (!dead) dead = !warp_wait(&sh.tfull[b], (tq / TR.nbuf) & 1, ctx, 17);
+        const uint32_t tqd = fdiv(tq, TR.nbuf_magic);
+        const int b = static_cast<int>(tq - tqd * TR.nbuf);
+        if (!dead) dead = !warp_wait(&sh.tfull[b], tqd & 1, ctx, 17);
         if (i == 0 && et == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
         tc_fence_after();
@@ -1082,10 +1127,11 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   const int npair = a.pair ? 2 : 1;
   const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M);
   const GemmShared sh = gemm_shared(a, smem, a.stages);
-  const long long U = static_cast<long long>(a.NT) * a.KB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.NT * a.KB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const int nunits = static_cast<int>(u1 - u0);
   const int S = a.stages;
+  const uint32_t smag = fdiv_magic(static_cast<uint32_t>(S));   // S >= 2
   const int kel = a.fp8 ? 128 : 64;  // elements per k-block
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1122,7 +1168,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     auto load_w = [&](int j, int s) {
       uint8_t* st = sh.stage0 + s * L.stage_bytes;
       for (int i = j * ups; i < nunits && i < (j + 1) * ups; ++i) {
-        const long long u = u0 + i;
+        const int u = u0 + i;
         const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
         const int sub = i - j * ups;
         tma_load_2d(st + sub * 16384, a.tmap_w, &sh.full[s], kb * kel, t * 128, pw);
@@ -1152,14 +1198,19 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
     int issued = pre;
     if (ok) {
       for (int j = pre; j < nslots; ++j) {
-        const int s = j % S;
-        if (!mbar_wait(&sh.empty[s], ((j / S) - 1) & 1, ctx, 11)) break;
+        const uint32_t jd = fdiv(static_cast<uint32_t>(j), smag);
+        const int s = j - static_cast<int>(jd) * S;
+        if (!mbar_wait(&sh.empty[s], (jd - 1) & 1, ctx, 11)) break;
         mbar_arrive_expect_tx(&sh.full[s], ub * units_in(j));
         load_w(j, s);
         load_x(j, s);
         issued = j + 1;
       }
     }
+    // every load of this share is out: warm L2 with the next projection's
+    // first tiles for the share with this CTA index
+    if (ok)
+      for (int c2 = c; c2 < a.pf.G; c2 += static_cast<int>(gridDim.x)) prefetch_next_share(a.pf, c2);
     // no copy may be in flight when the CTA leaves
     for (int s = 0; s < S && s < issued; ++s) {
       const int last = s + ((issued - 1 - s) / S) * S;  // last slot issued to stage s
@@ -1172,14 +1223,15 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   P.full = sh.full;
   P.empty = sh.empty;
   P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
-  P.ns = static_cast<uint32_t>(S);
+  pipe_set_ns(P, static_cast<uint32_t>(S));
   P.seq0 = 0;
   P.ups = ups;
   P.x_bytes = L.x_bytes;
   P.empty_cnt = kMMA ? 1 : 8;
   TmemRing TR;
   TR.base = tmem_base;
-  TR.nbuf = kMMA ? a.tmem_bufs : 1;
+  TR.nbuf = kMMA ? a.tmem_bufs : 2;   // unused by the GEMV path
+  TR.nbuf_magic = fdiv_magic(static_cast<uint32_t>(TR.nbuf));
   TR.stride = npair * (kMMA ? kMp : 0);
   TR.seq0 = 0;
   TR.rseq0 = 0;
@@ -1201,8 +1253,10 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int QRp, int stages) {
   L.stage_bytes = 4 * kAttnKeys * 128;
   L.q_off = stages * L.stage_bytes;                 // bf16 [QRp][128], swizzled
   L.o_off = L.q_off + QRp * 256;                    // fp32 [QRp][kOP]
-  L.xs_off = L.o_off + QRp * kOP * 4;               // partial-score exchange [2][8][nmt*8][32]
-  L.stat_off = L.xs_off + 2 * 8 * nmt * 8 * 32 * 4; // m, l per key group, lse, w, pos
+  // partial-score exchange [2][blocks per iteration][8][nmt*8][32]: two
+  // 64-key blocks per iteration below 64 query rows, one at 64
+  L.xs_off = L.o_off + QRp * kOP * 4;
+  L.stat_off = L.xs_off + 2 * 8 * (nmt < 2 ? 2 : nmt) * 8 * 32 * 4;  // m, l per key group, lse, w, pos
   L.bar_off = L.stat_off + (4 * QRp * 2 + QRp * 3) * 4 + 64;
   L.bar_off = (L.bar_off + 15) & ~15;
   // after the barriers: flags, producer page batch [32 units x 4 pages],
@@ -1310,8 +1364,8 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   int* row_pos = reinterpret_cast<int*>(row_w + QRp);
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
   int* ctb = flag + 16 + 32 * 4 + 64;     // [kMaxContrib] combine contributors
-  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.R * a.Hkv * a.NB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
   const int ct = tid - 32, wc = warp - 1;  // wc: 0..7
   // Warp wc works on key group kg = wc % 4 (16 keys of every 64-key block).
@@ -1322,6 +1376,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   constexpr bool kMS = (kNMT == 2);
   constexpr int kMT = kMS ? 1 : kNMT;      // m-tiles per warp
   constexpr int kND = kMS ? 16 : 8;        // 8-column d tiles per warp
+  constexpr int kU = kNMT == 4 ? 1 : 2;    // 64-key blocks per iteration
   const int kg = wc & 3, dh = wc >> 2;     // key group; d-half or m-tile
   const int mtb = kMS ? dh : 0;            // first m-tile of this warp
   const int dlo = kMS ? 0 : dh;            // first d-half of this warp
@@ -1339,12 +1394,12 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   bool dead = false;
   int i = 0;                               // valid-unit counter (matches producer)
   int pend[2], npend = 0;                  // pairs this CTA shares (first / last)
-  long long u = u0;
+  int u = u0;
   while (u < u1) {
     const int p = static_cast<int>(u / a.NB);
     const int blk_a = static_cast<int>(u % a.NB);
-    const long long run_end = min(u1, static_cast<long long>(p + 1) * a.NB);
-    const int blk_b = static_cast<int>(run_end - static_cast<long long>(p) * a.NB);
+    const int run_end = min(u1, (p + 1) * a.NB);
+    const int blk_b = run_end - p * a.NB;
     const int r = p / a.Hkv, h = p % a.Hkv;
     const int ctxr = pos[r * a.T + a.T - 1] + 1;
     // this pair's query rows (swizzled 16-byte chunks) and causal limits
@@ -1381,95 +1436,128 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       lrow[mt][0] = lrow[mt][1] = 0.f;
     }
     const int nvb = (ctxr + kAttnKeys - 1) / kAttnKeys;   // valid blocks
-    for (int blk = blk_a; blk < min(blk_b, nvb); ++blk, ++i) {
+    const int blk_end = min(blk_b, nvb);
+    // kU blocks per iteration: their scores share one online-softmax update
+    // (half the max / sum shuffles and rescales per key) and the two blocks'
+    // MMA chains are independent, so each warp has twice the work in flight.
+    int it = 0;
+    for (int blk = blk_a; blk < blk_end; ++it) {
+      const int nu = (kU == 2 && blk + 1 < blk_end) ? 2 : 1;
       if (!dead) dead = !pipe_warp_wait(P, i, ctx, 35);
+      if (nu == 2 && !dead) dead = !pipe_warp_wait(P, i + 1, ctx, 35);
       if (i == 0 && ct == 0) trace_stamp(ctx, c, TR_FIRST);
-      uint8_t* kst = attn_k(P, i);
-      uint8_t* vst = attn_v(P, i);
-      const uint32_t kb_u32 = smem_u32(kst), vb_u32 = smem_u32(vst);
-      const int k0 = blk * kAttnKeys;
-      const int nk = min(kAttnKeys, ctxr - k0);
-      float* xbuf = xs + (i & 1) * (8 * kXS * 32);
-      float sc[kMT][2][4];
+      uint32_t kb_u32[kU], vb_u32[kU];
+      int k0[kU], nk[kU];
+      bool part = false;
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
+      for (int uu = 0; uu < kU; ++uu) {
+        const int iu = uu < nu ? i + uu : i;
+        kb_u32[uu] = smem_u32(attn_k(P, iu));
+        vb_u32[uu] = smem_u32(attn_v(P, iu));
+        k0[uu] = (blk + uu) * kAttnKeys;
+        nk[uu] = uu < nu ? min(kAttnKeys, ctxr - k0[uu]) : 0;
+        if (uu < nu && nk[uu] < kAttnKeys) part = true;
+      }
+      float sc[kU][kMT][2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+      for (int uu = 0; uu < kU; ++uu)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+        for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[uu][mt][nt][e] = 0.f;
       if (!dead) {
-        if (nk < kAttnKeys) {
-          // keys past the context were not loaded (or hold stale data): zero
-          // this key group's V rows (the pair splits them by d-half) so that
-          // 0-probability keys contribute exactly 0
-          uint8_t* vh = vst + dh * kAttnKeys * 128;
-          for (int e = lane; e < 16 * 8; e += 32) {
-            const int key = kg * 16 + (e >> 3);
-            if (key >= nk) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int uu = 0; uu < kU; ++uu) {
+          if (uu < nu && nk[uu] < kAttnKeys) {
+            // keys past the context were not loaded (or hold stale data):
+            // zero this key group's V rows (the pair splits them by d-half)
+            // so that 0-probability keys contribute exactly 0
+            uint8_t* vh = attn_v(P, i + uu) + dh * kAttnKeys * 128;
+            for (int e = lane; e < 16 * 8; e += 32) {
+              const int key = kg * 16 + (e >> 3);
+              if (key >= nk[uu]) *reinterpret_cast<uint4*>(vh + key * 128 + (e & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
           }
-          __syncwarp();
         }
+        if (part) __syncwarp();
         // S over this warp's d range (both halves with kMS)
 #pragma unroll
         for (int dd = 0; dd < (kMS ? 2 : 1); ++dd) {
           const int dhh = dlo + dd;
 #pragma unroll
           for (int ks4 = 0; ks4 < 4; ++ks4) {
-            const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
-            const int ch = ks4 * 2 + ((lane >> 3) & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kb_u32 + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+            uint32_t qa[kMT][4];
 #pragma unroll
             for (int mt = 0; mt < kMT; ++mt) {
               const int qrow = (mtb + mt) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
               const int qch = (dhh * 4 + ks4) * 2 + (lane >> 4);
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), a0, a1, a2, a3);
-              mma_bf16_16816(sc[mt][0], a0, a1, a2, a3, b0, b1);
-              mma_bf16_16816(sc[mt][1], a0, a1, a2, a3, b2, b3);
+              ldsm_x4(qs_u32 + qrow * 256 + ((qch ^ (qrow & 7)) << 4), qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3]);
+            }
+#pragma unroll
+            for (int uu = 0; uu < kU; ++uu) {
+              if (uu >= nu) break;
+              const int key = kg * 16 + (lane & 7) + ((lane >> 4) << 3);
+              const int ch = ks4 * 2 + ((lane >> 3) & 1);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(kb_u32[uu] + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+              for (int mt = 0; mt < kMT; ++mt) {
+                mma_bf16_16816(sc[uu][mt][0], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], b0, b1);
+                mma_bf16_16816(sc[uu][mt][1], qa[mt][0], qa[mt][1], qa[mt][2], qa[mt][3], b2, b3);
+              }
             }
           }
         }
         if constexpr (!kMS) {
-          float* mine = xbuf + wc * (kXS * 32);
 #pragma unroll
-          for (int mt = 0; mt < kMT; ++mt)
+          for (int uu = 0; uu < kU; ++uu) {
+            float* mine = xs + ((it & 1) * kU + uu) * (8 * kXS * 32) + wc * (kXS * 32);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) mine[((mt * 2 + nt) * 4 + e) * 32 + lane] = sc[mt][nt][e];
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mine[((mt * 2 + nt) * 4 + e) * 32 + lane] = sc[uu][mt][nt][e];
+          }
         }
       }
       // the two d-half warps of this key group exchange partial scores
       // (with kMS: the pair only waits for each other's V zeroing)
-      if (!kMS || nk < kAttnKeys) named_bar(2 + kg, 64);
+      if (!kMS || part) named_bar(2 + kg, 64);
       if (!dead) {
         if constexpr (!kMS) {
-          const float* other = xbuf + partner * (kXS * 32);
 #pragma unroll
-          for (int mt = 0; mt < kMT; ++mt)
+          for (int uu = 0; uu < kU; ++uu) {
+            const float* other = xs + ((it & 1) * kU + uu) * (8 * kXS * 32) + partner * (kXS * 32);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) sc[mt][nt][e] += other[((mt * 2 + nt) * 4 + e) * 32 + lane];
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[uu][mt][nt][e] += other[((mt * 2 + nt) * 4 + e) * 32 + lane];
+          }
         }
-        // scale, mask, online softmax on this key group's 16 keys
+        // scale, mask, online softmax on this key group's 16 keys of each block
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             float mx = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int uu = 0; uu < kU; ++uu)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int col = kg * 16 + nt * 8 + qc * 2 + e;
-                const int key = k0 + col;
-                const bool valid = col < nk && key <= lim[mt][hr];
-                const float v = valid ? sc[mt][nt][hr * 2 + e] * a.scale_log2 : -INFINITY;
-                sc[mt][nt][hr * 2 + e] = v;
-                mx = fmaxf(mx, v);
-              }
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int col = kg * 16 + nt * 8 + qc * 2 + e;
+                  const int key = k0[uu] + col;
+                  const bool valid = col < nk[uu] && key <= lim[mt][hr];
+                  const float v = valid ? sc[uu][mt][nt][hr * 2 + e] * a.scale_log2 : -INFINITY;
+                  sc[uu][mt][nt][hr * 2 + e] = v;
+                  mx = fmaxf(mx, v);
+                }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float mold = mrow[mt][hr];
@@ -1477,13 +1565,15 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
             const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(mold - mnew);
             float sum = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int uu = 0; uu < kU; ++uu)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sc[mt][nt][hr * 2 + e] - mnew);
-                sc[mt][nt][hr * 2 + e] = pv;
-                sum += pv;
-              }
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float pv = (mnew == -INFINITY) ? 0.f : exp2f(sc[uu][mt][nt][hr * 2 + e] - mnew);
+                  sc[uu][mt][nt][hr * 2 + e] = pv;
+                  sum += pv;
+                }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             mrow[mt][hr] = mnew;
@@ -1503,29 +1593,42 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
         // O += P V over this warp's d range (columns [64 dh, 64 dh + 64), or
         // all 128 with kMS)
 #pragma unroll
-        for (int dd = 0; dd < (kMS ? 2 : 1); ++dd) {
-          const int dhh = dlo + dd;
+        for (int uu = 0; uu < kU; ++uu) {
+          if (uu >= nu) break;
+          uint32_t pa[kMT][4];
 #pragma unroll
-          for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
-            const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int ch = cp * 2 + (lane >> 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vb_u32 + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          for (int mt = 0; mt < kMT; ++mt) {
+            pa[mt][0] = pack_bf16(sc[uu][mt][0][0], sc[uu][mt][0][1]);
+            pa[mt][1] = pack_bf16(sc[uu][mt][0][2], sc[uu][mt][0][3]);
+            pa[mt][2] = pack_bf16(sc[uu][mt][1][0], sc[uu][mt][1][1]);
+            pa[mt][3] = pack_bf16(sc[uu][mt][1][2], sc[uu][mt][1][3]);
+          }
 #pragma unroll
-            for (int mt = 0; mt < kMT; ++mt) {
-              const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-              const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-              const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-              const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
-              mma_bf16_16816(o[mt][dd * 8 + cp * 2], a0, a1, a2, a3, b0, b1);
-              mma_bf16_16816(o[mt][dd * 8 + cp * 2 + 1], a0, a1, a2, a3, b2, b3);
+          for (int dd = 0; dd < (kMS ? 2 : 1); ++dd) {
+            const int dhh = dlo + dd;
+#pragma unroll
+            for (int cp = 0; cp < 4; ++cp) {        // pairs of 8-column n-tiles
+              const int key = kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+              const int ch = cp * 2 + (lane >> 4);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(vb_u32[uu] + dhh * kAttnKeys * 128 + key * 128 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+              for (int mt = 0; mt < kMT; ++mt) {
+                mma_bf16_16816(o[mt][dd * 8 + cp * 2], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
+                mma_bf16_16816(o[mt][dd * 8 + cp * 2 + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
+              }
             }
           }
         }
-        if (nk < kAttnKeys) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
+        if (part) fence_proxy_async_shared();  // zeroed rows vs the next TMA fill
         __syncwarp();
-        if (lane == 0) mbar_arrive(pipe_empty(P, pipe_q(P, i)));
+        if (lane == 0) {
+          mbar_arrive(pipe_empty(P, pipe_q(P, i)));
+          if (nu == 2) mbar_arrive(pipe_empty(P, pipe_q(P, i + 1)));
+        }
       }
+      blk += nu;
+      i += nu;
     }
     // ---- merge the four key groups (fixed order) into Ob, then lse
     if (named_bar_or(1, 256, dead)) return -1;
@@ -1601,7 +1704,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       // publish this pair's partial (slot 0: the pair where this CTA's range
       // begins; slot 1: a later pair, the range's last one) and an arrival;
       // the pair is combined once this CTA's range is done (below)
-      const long long ps = static_cast<long long>(p) * a.NB;
+      const int ps = p * a.NB;
       const int slot = (u0 >= ps) ? 0 : 1;
       const size_t part = static_cast<size_t>(QRp) * 129;
       float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
@@ -1630,7 +1733,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   // publications, then the n finished slices; the last slice resets it.
   for (int k = 0; k < npend; ++k) {
     const int p = pend[k];
-    const long long ps = static_cast<long long>(p) * a.NB;
+    const int ps = p * a.NB;
     const int r = p / a.Hkv, h = p % a.Hkv;
     const size_t part = static_cast<size_t>(QRp) * 129;
     if (ct == 0) {
@@ -1706,8 +1809,9 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   int* pgbuf = flag + 16;                 // [32][4] pages of the producer's batch
   int* ppos = pgbuf + 32 * 4;             // [64] token positions (producer)
   const int S = a.stages;
-  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const uint32_t smag = fdiv_magic(static_cast<uint32_t>(S));   // S >= 2
+  const int U = a.R * a.Hkv * a.NB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
   const CUtensorMap* kvm = &bd->kv_map;
   if (tid == 0) {
@@ -1746,12 +1850,12 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     const int npg = kAttnKeys / box;                      // boxes per 64-key unit
     const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
     int i = 0;
-    for (long long ub = u0; ok && ub < u1; ub += 32) {
-      const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
+    for (int ub = u0; ok && ub < u1; ub += 32) {
+      const int nb = min(32, u1 - ub);
       // the batch's page numbers, loaded by the whole warp
       for (int e = lane; e < nb * npg; e += 32) {
         const int j = e / npg, q = e % npg;
-        const long long u = ub + j;
+        const int u = ub + j;
         const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
         const int r = p / a.Hkv;
         const int ctxr = ppos[r * a.T + a.T - 1] + 1;
@@ -1763,14 +1867,15 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       __syncwarp();
       if (lane == 0) {
         for (int j = 0; j < nb && ok; ++j) {
-          const long long u = ub + j;
+          const int u = ub + j;
           const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
           const int r = p / a.Hkv, h = p % a.Hkv;
           const int ctxr = ppos[r * a.T + a.T - 1] + 1;
           const int k0 = blk * kAttnKeys;
           if (k0 >= ctxr) continue;
-          const int s = i % S;
-          if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1, ctx, 31)) {
+          const uint32_t id = fdiv(static_cast<uint32_t>(i), smag);
+          const int s = i - static_cast<int>(id) * S;
+          if (i >= S && !mbar_wait(&empty[s], (id - 1) & 1, ctx, 31)) {
             ok = false;
             break;
           }
@@ -1800,6 +1905,10 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       i = __shfl_sync(0xffffffffu, i, 0);
       __syncwarp();
     }
+    // every K/V load of this share is out: warm L2 with the O projection's
+    // first weight tiles (its shares c, c + CTAs, ...)
+    if (lane == 0 && ok)
+      for (int c2 = c; c2 < a.pf.G; c2 += static_cast<int>(gridDim.x)) prefetch_next_share(a.pf, c2);
     if (lane == 0) {
       const int issued = i;
       for (int s = 0; s < S && s < issued; ++s) {
@@ -1816,7 +1925,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   P.full = full;
   P.empty = empty;
   P.slot_bytes = static_cast<uint32_t>(L.stage_bytes);
-  P.ns = static_cast<uint32_t>(S);
+  pipe_set_ns(P, static_cast<uint32_t>(S));
   P.seq0 = 0;
   P.ups = 1;
   P.x_bytes = 0;
@@ -1860,8 +1969,8 @@ __device__ __noinline__ bool mk_produce_gemm(const GemmArgs& a_, int c, const De
   const Pipe R = R_;
   const int npair = a.pair ? 2 : 1;
   const int ups = npair == 1 ? 2 : 1;
-  const long long U = static_cast<long long>(a.NT) * a.KB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.NT * a.KB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const int n = static_cast<int>(u1 - u0);
   const int nslots = (n + ups - 1) / ups;
   const int kel = a.fp8 ? 128 : 64;
@@ -1883,7 +1992,7 @@ __device__ __noinline__ bool mk_produce_gemm(const GemmArgs& a_, int c, const De
     const uint32_t q = seq + static_cast<uint32_t>(j);
     if (q >= R.ns) {
       uint64_t* e = pipe_empty(R, q);
-      const uint32_t par = ((q / R.ns) - 1) & 1u;
+      const uint32_t par = (fdiv(q, R.ns_magic) - 1) & 1u;
       if (!deps_ok && pend < armed && !mbar_try_wait(e, par)) {
         deps_ok = poll_deps(dep, ctx, 60);
         trace_stamp(ctx, c, TR_PDEPS);
@@ -1902,7 +2011,7 @@ __device__ __noinline__ bool mk_produce_gemm(const GemmArgs& a_, int c, const De
     mbar_arrive_expect_tx(pipe_full(R, q), ub * static_cast<uint32_t>(i1 - i0));
     *hi = q + 1;
     for (int i = i0; i < i1; ++i) {
-      const long long u = u0 + i;
+      const int u = u0 + i;
       const int t = a.t_base + static_cast<int>(u / a.KB), kb = static_cast<int>(u % a.KB);
       tma_load_2d(pipe_slot(R, q) + (i - i0) * 16384, a.tmap_w, pipe_full(R, q), kb * kel,
                   t * 128, pw);
@@ -1936,8 +2045,8 @@ __device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const De
   const KernelCtx ctx = ctx_;
   const Pipe R = R_;
   const int lane = threadIdx.x & 31;
-  const long long U = static_cast<long long>(a.R) * a.Hkv * a.NB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.R * a.Hkv * a.NB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   const Binding* bd = ctx.binding;
   const CUtensorMap* kvm = &bd->kv_map;
   if (lane == 0) {
@@ -1955,11 +2064,11 @@ __device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const De
   const uint32_t half = kAttnKeys * 128;                // one d-half of K or V
   bool ok = true, deps_ok = dep.n == 0;
   int i = 0;
-  for (long long ub = u0; ok && ub < u1; ub += 32) {
-    const int nb = static_cast<int>(min(static_cast<long long>(32), u1 - ub));
+  for (int ub = u0; ok && ub < u1; ub += 32) {
+    const int nb = min(32, u1 - ub);
     for (int e = lane; e < nb * npg; e += 32) {
       const int j = e / npg, qq = e % npg;
-      const long long u = ub + j;
+      const int u = ub + j;
       const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
       const int r = p / a.Hkv;
       const int ctxr = ppos[r * a.T + a.T - 1] + 1;
@@ -1971,7 +2080,7 @@ __device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const De
     __syncwarp();
     if (lane == 0) {
       for (int j = 0; j < nb && ok; ++j) {
-        const long long u = ub + j;
+        const int u = ub + j;
         const int p = static_cast<int>(u / a.NB), blk = static_cast<int>(u % a.NB);
         const int r = p / a.Hkv, h = p % a.Hkv;
         const int ctxr = ppos[r * a.T + a.T - 1] + 1;
@@ -1988,7 +2097,7 @@ __device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const De
         }
         const int nbox = (nk + box - 1) / box;
         const uint32_t q = seq + static_cast<uint32_t>(i);
-        if (q >= R.ns && !mbar_wait(pipe_empty(R, q), ((q / R.ns) - 1) & 1u, ctx, 64)) {
+        if (q >= R.ns && !mbar_wait(pipe_empty(R, q), (fdiv(q, R.ns_magic) - 1) & 1u, ctx, 64)) {
           ok = false;
           break;
         }
@@ -2098,15 +2207,15 @@ __device__ int mk_attn(const AttnArgs& a, int c, const Dep& dep, const KernelCtx
 
 // Units of GEMM share c (its Stream-K range).
 __device__ __forceinline__ int gemm_share_units(const GemmArgs& a, int c) {
-  const long long U = static_cast<long long>(a.NT) * a.KB;
+  const int U = a.NT * a.KB;
   return static_cast<int>(sk_begin(U, a.G, c + 1) - sk_begin(U, a.G, c));
 }
 
 // Tiles GEMM share c hands to its fix-up warps: every tile its range
 // touches but the last (which the epilogue warps finish themselves).
 __device__ __forceinline__ int gemm_share_handoffs(const GemmArgs& a, int c) {
-  const long long U = static_cast<long long>(a.NT) * a.KB;
-  const long long u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const int U = a.NT * a.KB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
   return u1 > u0 ? static_cast<int>((u1 - 1) / a.KB - u0 / a.KB) : 0;
 }
 
