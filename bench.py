@@ -329,7 +329,8 @@ def main():
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         evs = []
         for _ in range(args.steps):
-            flush.zero_()
+            if args.l2 == "flush":
+                flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             plan.step_host(xh, rh, kv, bth, posh, outh, emode, stream)

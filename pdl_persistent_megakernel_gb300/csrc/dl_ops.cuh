@@ -666,14 +666,19 @@ __device__ __forceinline__ void unpack_e4m3x16(const uint4& v, float* f) {
 
 // The activation scales [M][KB] of the whole projection input, staged once
 // per CTA (float4 loads, several in flight per thread).
+// Activation scales [M][KB] -> shared [KB][Mp] (zero for padding tokens):
+// an epilogue reads the Mp scales of one k-block as contiguous vectors.
 __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShared& sh,
                                                int nthr, int ct, int bar) {
-  const int n4 = (a.M * a.KB) / 4;   // KB is a multiple of 4 for every projection
-  const float4* src = reinterpret_cast<const float4*>(a.x_scale);
-  float4* dst = reinterpret_cast<float4*>(sh.sx);
-#pragma unroll 4
-  for (int e = ct; e < n4; e += nthr) dst[e] = __ldcg(src + e);
-  for (int e = n4 * 4 + ct; e < a.M * a.KB; e += nthr) sh.sx[e] = __ldcg(a.x_scale + e);
+  const int M = a.M, KB = a.KB, Mp = a.Mp;
+  for (int e = ct; e < M * KB; e += nthr) {
+    const int m = e / KB, kb = e - m * KB;
+    sh.sx[kb * Mp + m] = __ldcg(a.x_scale + e);
+  }
+  for (int e = ct; e < (Mp - M) * KB; e += nthr) {
+    const int m = M + e / KB, kb = e % KB;
+    sh.sx[kb * Mp + m] = 0.f;
+  }
   named_bar(bar, nthr);
 }
 
@@ -871,7 +876,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
                 float d = 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) d = fmaf(wf[e], xf[m][e], d);
-                const float sa = m < a.M ? sh.sx[m * a.KB + kb0 + k] : 0.f;
+                const float sa = m < a.M ? sh.sx[(kb0 + k) * a.Mp + m] : 0.f;
                 acc[p][j][m] = fmaf(d, sw * sa, acc[p][j][m]);
               }
             }
@@ -1003,6 +1008,11 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
     if (et == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
+    // loop invariants in registers (the arguments may sit in memory that
+    // every asm memory clobber below would make the compiler read again)
+    const bool fp8 = a.fp8 != 0;
+    const uint32_t tl_base = TR.base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t tstride = static_cast<uint32_t>(TR.stride);
     bool dead = false;
     int i = 0;
     uint32_t rq = TR.rseq0;
@@ -1032,25 +1042,39 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         if (i == 0 && et == 0) trace_stamp(ctx, c, TR_FIRST);
         if (dead) continue;
         tc_fence_after();
+        const uint32_t tb = tl_base + static_cast<uint32_t>(b) * tstride;
+        const float sw0 = fp8 ? sh.sw[k] : 1.f;
+        const float sw1 = (fp8 && npair == 2) ? sh.sw[run + k] : 1.f;
+        const float4* sxk = reinterpret_cast<const float4*>(sh.sx + (kb0 + k) * kMp);
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          if (p >= npair) break;
-          const float sw = a.fp8 ? sh.sw[p * run + k] : 1.f;
+        for (int c16 = 0; c16 < kMp / 16; ++c16) {
+          // both tiles' accumulators of these 16 tokens, one wait
+          float v[2][16];
+          tmem_ld16(tb + c16 * 16, v[0]);
+          if (npair == 2) tmem_ld16(tb + kMp + c16 * 16, v[1]);
+          tmem_wait_ld();
+          if (fp8) {
+            float sa[16];
 #pragma unroll
-          for (int c16 = 0; c16 < kMp / 16; ++c16) {
-            float v[16];
-            tmem_ld16(TR.base + (static_cast<uint32_t>(q * 32) << 16) + b * TR.stride + p * kMp + c16 * 16, v);
-            tmem_wait_ld();
-            if (a.fp8) {
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const float4 t4 = sxk[c16 * 4 + e4];
+              sa[e4 * 4] = t4.x;
+              sa[e4 * 4 + 1] = t4.y;
+              sa[e4 * 4 + 2] = t4.z;
+              sa[e4 * 4 + 3] = t4.w;
+            }
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int m = c16 * 16 + e;
-                const float sa = m < a.M ? sh.sx[m * a.KB + kb0 + k] : 0.f;
-                acc[p][m] = fmaf(v[e], sw * sa, acc[p][m]);
-              }
-            } else {
+            for (int e = 0; e < 16; ++e) acc[0][c16 * 16 + e] = fmaf(v[0][e], sw0 * sa[e], acc[0][c16 * 16 + e]);
+            if (npair == 2) {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) acc[p][c16 * 16 + e] += v[e];
+              for (int e = 0; e < 16; ++e) acc[1][c16 * 16 + e] = fmaf(v[1][e], sw1 * sa[e], acc[1][c16 * 16 + e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[0][c16 * 16 + e] += v[0][e];
+            if (npair == 2) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) acc[1][c16 * 16 + e] += v[1][e];
             }
           }
         }
@@ -1344,8 +1368,10 @@ __device__ __forceinline__ void attn_write_row(const AttnArgs& a, int r, int h, 
 // Consumer side of an attention share (warps 1-8): `priv` is the share's
 // private shared memory (layout attn_smem_layout(QRp, 0)).  Returns the
 // number of key blocks it consumed (the blocks below each pair's context),
-// or -1 after a failed wait.
-template <int kNMT>
+// or -1 after a failed wait.  kU2: two 64-key blocks per iteration below
+// 64 query rows (the standalone kernel; the megakernel's register budget,
+// shared with its argument copies, keeps one).
+template <int kNMT, bool kU2>
 __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
                               const KernelCtx& ctx, uint8_t* priv, const Pipe& P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1376,7 +1402,7 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
   constexpr bool kMS = (kNMT == 2);
   constexpr int kMT = kMS ? 1 : kNMT;      // m-tiles per warp
   constexpr int kND = kMS ? 16 : 8;        // 8-column d tiles per warp
-  constexpr int kU = kNMT == 4 ? 1 : 2;    // 64-key blocks per iteration
+  constexpr int kU = (kU2 && kNMT < 4) ? 2 : 1;   // 64-key blocks per iteration
   const int kg = wc & 3, dh = wc >> 2;     // key group; d-half or m-tile
   const int mtb = kMS ? dh : 0;            // first m-tile of this warp
   const int dlo = kMS ? 0 : dh;            // first d-half of this warp
@@ -1930,7 +1956,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   P.ups = 1;
   P.x_bytes = 0;
   P.empty_cnt = 8;
-  attn_consume_t<kNMT>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
+  attn_consume_t<kNMT, true>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
 }
 
 __device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
@@ -2161,7 +2187,7 @@ __device__ __noinline__ int mk_attn_v(const AttnArgs& a_, int c, const Dep& dep_
   const Dep dep = dep_;
   const KernelCtx ctx = ctx_;
   const Pipe P = P_;
-  return attn_consume_t<kNMT>(a, c, dep, ctx, priv, P);
+  return attn_consume_t<kNMT, false>(a, c, dep, ctx, priv, P);
 }
 
 __device__ __noinline__ void mk_norm(const NormArgs& a_, int c, const Dep& dep_,
