@@ -1365,6 +1365,115 @@ __device__ __forceinline__ void attn_write_row(const AttnArgs& a, int r, int h, 
   }
 }
 
+// A finished pair run of this CTA: Ob holds its normalised rows, row_lse
+// their log-sum-exp (base 2).  The whole pair: write the attention output;
+// otherwise publish the partial (slot 0: the pair where this CTA's range
+// begins; slot 1: a later pair, the range's last one) and an arrival; the
+// pair is combined once the CTA's range is done (attn_combine).
+__device__ void attn_pair_out(const AttnArgs& a, int c, int u0, int p, int blk_a, int blk_b,
+                              const float* Ob, const float* row_lse, int* pend, int* npend) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int ct = tid - 32, wc = (tid >> 5) - 1;
+  const int QRp = a.QRp, G = a.Hq / a.Hkv;
+  const int r = p / a.Hkv, h = p % a.Hkv;
+  const bool whole = (blk_a == 0 && blk_b == a.NB);
+  if (!whole) {
+    const int ps = p * a.NB;
+    const int slot = (u0 >= ps) ? 0 : 1;
+    const size_t part = static_cast<size_t>(QRp) * 129;
+    float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
+    for (int e4 = ct; e4 < QRp * 32; e4 += 256)
+      reinterpret_cast<float4*>(mine)[e4] =
+          *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
+    for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
+    __threadfence();
+    named_bar(1, 256);
+    if (ct == 0) atomicAdd(a.pair_cnt + p, 1u);
+    pend[(*npend)++] = p;
+  } else {
+    // the whole pair is this CTA's: write the attention output, one warp
+    // per query row
+    for (int rr = wc; rr < a.QR; rr += 8)
+      attn_write_row(a, r, h, G, rr, *reinterpret_cast<const float4*>(Ob + rr * kOP + lane * 4), lane);
+  }
+}
+
+// Split-KV combine of the pairs this CTA published partials for (warps
+// 1-8, named barrier 1).  False after a failed wait.
+__device__ bool attn_combine(const AttnArgs& a, int c, const KernelCtx& ctx, const int* pend,
+                             int npend, int* flag, int* ctb) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int ct = tid - 32, wc = (tid >> 5) - 1;
+  const int QRp = a.QRp, G = a.Hq / a.Hkv;
+  const int U = a.R * a.Hkv * a.NB;
+  // ---- split-KV combine, shared by all CTAs of a pair: once every partial
+  // of the pair is published, contributor j (CTA order) combines query rows
+  // [j * per, (j + 1) * per) by their log-sum-exp weights, in CTA order, and
+  // writes them (one warp per row).  The pair's counter counts the n
+  // publications, then the n finished slices; the last slice resets it.
+  for (int k = 0; k < npend; ++k) {
+    const int p = pend[k];
+    const int ps = p * a.NB;
+    const int r = p / a.Hkv, h = p % a.Hkv;
+    const size_t part = static_cast<size_t>(QRp) * 129;
+    if (ct == 0) {
+      const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
+      int j = 0;
+      while (j < n && (ctb[j] >> 1) != c) ++j;
+      flag[1] = n;
+      flag[3] = j;
+      flag[0] = wait_counter(a.pair_cnt + p, static_cast<unsigned>(n), ctx, 36) ? 1 : -1;
+    }
+    named_bar(1, 256);
+    if (flag[0] < 0) return false;
+    __threadfence();
+    const int n = flag[1], jme = flag[3];
+    const int per = (a.QR + n - 1) / n;
+    const int r1 = min(a.QR, (jme + 1) * per);
+    for (int rr = jme * per + wc; rr < r1; rr += 8) {
+      // lane j holds contributor j's weight (j < 32, then j + 32)
+      float l0 = -INFINITY, l1 = -INFINITY;
+      if (lane < n) l0 = __ldcg(a.ws + static_cast<size_t>(ctb[lane]) * part + QRp * 128 + rr);
+      if (lane + 32 < n) l1 = __ldcg(a.ws + static_cast<size_t>(ctb[lane + 32]) * part + QRp * 128 + rr);
+      const float mx = warp_max(fmaxf(l0, l1));
+      const float w0 = (mx == -INFINITY || lane >= n) ? 0.f : exp2f(l0 - mx);
+      const float w1 = (mx == -INFINITY || lane + 32 >= n) ? 0.f : exp2f(l1 - mx);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj < n ? j0 + jj : 0;
+          v[jj] = __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<size_t>(ctb[j]) * part +
+                                                          static_cast<size_t>(rr) * 128) + lane);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const float wsrc = __shfl_sync(0xffffffffu, j < 32 ? w0 : w1, j & 31);
+          if (j < n) {
+            den += wsrc;
+            acc.x = fmaf(wsrc, v[jj].x, acc.x);
+            acc.y = fmaf(wsrc, v[jj].y, acc.y);
+            acc.z = fmaf(wsrc, v[jj].z, acc.z);
+            acc.w = fmaf(wsrc, v[jj].w, acc.w);
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      attn_write_row(a, r, h, G, rr, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv), lane);
+    }
+    named_bar(1, 256);
+    if (ct == 0) {
+      const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
+      if (old + 1 == 2u * static_cast<unsigned>(n)) a.pair_cnt[p] = 0u;
+      trace_stamp(ctx, c, TR_REDUCE);
+    }
+  }
+  return true;
+}
+
 // Consumer side of an attention share (warps 1-8): `priv` is the share's
 // private shared memory (layout attn_smem_layout(QRp, 0)).  Returns the
 // number of key blocks it consumed (the blocks below each pair's context),
@@ -1725,98 +1834,12 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
       }
       named_bar(1, 256);
     }
-    const bool whole = (blk_a == 0 && blk_b == a.NB);
-    if (!whole) {
-      // publish this pair's partial (slot 0: the pair where this CTA's range
-      // begins; slot 1: a later pair, the range's last one) and an arrival;
-      // the pair is combined once this CTA's range is done (below)
-      const int ps = p * a.NB;
-      const int slot = (u0 >= ps) ? 0 : 1;
-      const size_t part = static_cast<size_t>(QRp) * 129;
-      float* mine = a.ws + static_cast<size_t>(c * 2 + slot) * part;
-      for (int e4 = ct; e4 < QRp * 32; e4 += 256)
-        reinterpret_cast<float4*>(mine)[e4] =
-            *reinterpret_cast<const float4*>(Ob + (e4 >> 5) * kOP + (e4 & 31) * 4);
-      for (int rr = ct; rr < QRp; rr += 256) mine[QRp * 128 + rr] = row_lse[rr];
-      __threadfence();
-      named_bar(1, 256);
-      if (ct == 0) atomicAdd(a.pair_cnt + p, 1u);
-      pend[npend++] = p;
-    } else {
-      // the whole pair is this CTA's: write the attention output, one warp
-      // per query row
-      for (int rr = wc; rr < a.QR; rr += 8)
-        attn_write_row(a, r, h, G, rr, *reinterpret_cast<const float4*>(Ob + rr * kOP + lane * 4), lane);
-    }
+    attn_pair_out(a, c, u0, p, blk_a, blk_b, Ob, row_lse, pend, &npend);
     named_bar(1, 256);
     u = run_end;
   }
   if (ct == 0) trace_stamp(ctx, c, TR_LOOP_END);
-  // ---- split-KV combine, shared by all CTAs of a pair: once every partial
-  // of the pair is published, contributor j (CTA order) combines query rows
-  // [j * per, (j + 1) * per) by their log-sum-exp weights, in CTA order, and
-  // writes them (one warp per row).  The pair's counter counts the n
-  // publications, then the n finished slices; the last slice resets it.
-  for (int k = 0; k < npend; ++k) {
-    const int p = pend[k];
-    const int ps = p * a.NB;
-    const int r = p / a.Hkv, h = p % a.Hkv;
-    const size_t part = static_cast<size_t>(QRp) * 129;
-    if (ct == 0) {
-      const int n = sk_contributors(U, a.G, ps, a.NB, ctb);
-      int j = 0;
-      while (j < n && (ctb[j] >> 1) != c) ++j;
-      flag[1] = n;
-      flag[3] = j;
-      flag[0] = wait_counter(a.pair_cnt + p, static_cast<unsigned>(n), ctx, 36) ? 1 : -1;
-    }
-    named_bar(1, 256);
-    if (flag[0] < 0) return -1;
-    __threadfence();
-    const int n = flag[1], jme = flag[3];
-    const int per = (a.QR + n - 1) / n;
-    const int r1 = min(a.QR, (jme + 1) * per);
-    for (int rr = jme * per + wc; rr < r1; rr += 8) {
-      // lane j holds contributor j's weight (j < 32, then j + 32)
-      float l0 = -INFINITY, l1 = -INFINITY;
-      if (lane < n) l0 = __ldcg(a.ws + static_cast<size_t>(ctb[lane]) * part + QRp * 128 + rr);
-      if (lane + 32 < n) l1 = __ldcg(a.ws + static_cast<size_t>(ctb[lane + 32]) * part + QRp * 128 + rr);
-      const float mx = warp_max(fmaxf(l0, l1));
-      const float w0 = (mx == -INFINITY || lane >= n) ? 0.f : exp2f(l0 - mx);
-      const float w1 = (mx == -INFINITY || lane + 32 >= n) ? 0.f : exp2f(l1 - mx);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float den = 0.f;
-      for (int j0 = 0; j0 < n; j0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj < n ? j0 + jj : 0;
-          v[jj] = __ldcg(reinterpret_cast<const float4*>(a.ws + static_cast<size_t>(ctb[j]) * part +
-                                                          static_cast<size_t>(rr) * 128) + lane);
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj;
-          const float wsrc = __shfl_sync(0xffffffffu, j < 32 ? w0 : w1, j & 31);
-          if (j < n) {
-            den += wsrc;
-            acc.x = fmaf(wsrc, v[jj].x, acc.x);
-            acc.y = fmaf(wsrc, v[jj].y, acc.y);
-            acc.z = fmaf(wsrc, v[jj].z, acc.z);
-            acc.w = fmaf(wsrc, v[jj].w, acc.w);
-          }
-        }
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      attn_write_row(a, r, h, G, rr, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv), lane);
-    }
-    named_bar(1, 256);
-    if (ct == 0) {
-      const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
-      if (old + 1 == 2u * static_cast<unsigned>(n)) a.pair_cnt[p] = 0u;
-      trace_stamp(ctx, c, TR_REDUCE);
-    }
-  }
+  if (!attn_combine(a, c, ctx, pend, npend, flag, ctb)) return -1;
   if (ct == 0) trace_stamp(ctx, c, TR_END);
   return i;
 }
@@ -1853,15 +1876,11 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
 
   if (warp == 0) {
     // ------------------------------------------ producer (warp 0, lane 0 issues)
-    bool ok = true;
-    if (dep.mode == 0) {
-      gdc_wait();
-      gdc_launch_dependents();
-      ok = !aborted(ctx.status);
-    } else {
-      if (lane == 0) ok = poll_deps(dep, ctx, 30);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    }
+    // Blocks that hold none of this step's new keys (the only K/V rows the
+    // previous kernel writes) go out before the dependency wait; positions
+    // and block table are step inputs.  Lane 0 waits at the first block that
+    // holds a new key.
+    bool ok = true, deps_ok = false;
     if (lane == 0) {
       fence_tmap_acquire(kvm);
       prefetch_tmap(kvm);
@@ -1907,6 +1926,16 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
           }
           uint8_t* st = stage0 + s * L.stage_bytes;
           const int nk = min(kAttnKeys, ctxr - k0);
+          if (!deps_ok && k0 + nk > ppos[r * a.T]) {
+            deps_ok = true;
+            if (dep.mode == 0) {
+              gdc_wait();
+              ok = !aborted(ctx.status);
+            } else {
+              ok = poll_deps(dep, ctx, 30);
+            }
+            if (!ok) break;
+          }
           const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
           mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
           for (int q = 0; q < nbox; ++q) {
@@ -1930,6 +1959,12 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       i = __shfl_sync(0xffffffffu, i, 0);
       __syncwarp();
+    }
+    // every thread passes the dependency once (the CTA's completion then
+    // implies its dependencies' completion)
+    if (dep.mode == 0) {
+      gdc_wait();
+      gdc_launch_dependents();
     }
     // every K/V load of this share is out: warm L2 with the O projection's
     // first weight tiles (its shares c, c + CTAs, ...)
