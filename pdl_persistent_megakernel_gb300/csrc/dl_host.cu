@@ -112,6 +112,7 @@ struct dl_plan {
   int L = 0, V = 0, R = 0, T = 0, P = 0;
   bool fp8 = false, full = false, mma = false;
   int pf_units = 4;    // L2 prefetch units per share (DL_L2_PREFETCH_UNITS; 0: off)
+  bool attn_tc = true; // standalone attention on tcgen05 (DL_ATTN=mma_sync: mma.sync)
   unsigned long long budget_ns = 1000000000ull;
 
   std::vector<void*> allocs;
@@ -204,6 +205,7 @@ static KernelCtx make_ctx(const dl_plan* p, int op_id) {
 
 // ------------------------------------------------------------ op builders
 constexpr int kGemmSmemTarget = 210 * 1024;
+constexpr int kAttnTcSmemTarget = 224 * 1024;
 static int choose_stages(int stage_bytes, int fixed_bytes, int target) {
   int s = (target - fixed_bytes) / stage_bytes;
   return std::max(2, std::min(kMaxStages, s));
@@ -326,15 +328,19 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.QRp = a.QR <= 16 ? 16 : (a.QR <= 32 ? 32 : 64);
   a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
   a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms);
-  // 4 stages of 32 KiB keep the KV stream at full rate (more adds nothing)
-  a.stages = std::max(2, std::min(4, (kGemmSmemTarget - attn_smem_bytes(a.QRp, 0)) /
-                                         (4 * kAttnKeys * 128)));
+  // stages of 32 KiB: 4 keep the mma.sync engine fed (more add nothing);
+  // the tcgen05 engine holds a block from its arrival to its PV commit
+  // (about 2.3 us), so it takes as many as fit (up to 6)
+  const int fixed = p->attn_tc ? attn_tc_smem_bytes(a.QRp, 0) : attn_smem_bytes(a.QRp, 0);
+  a.stages = p->attn_tc
+      ? std::max(2, std::min(6, (kAttnTcSmemTarget - fixed) / (4 * kAttnKeys * 128)))
+      : std::max(2, std::min(4, (kGemmSmemTarget - fixed) / (4 * kAttnKeys * 128)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d)));
   a.ws = p->ws_attn;
   a.pair_cnt = cnt;
-  op.kernel = attn_kernel(a.QRp);
+  op.kernel = p->attn_tc ? attn_tc_kernel() : attn_kernel(a.QRp);
   op.grid = a.G;
-  op.smem = attn_smem_bytes(a.QRp, a.stages);
+  op.smem = p->attn_tc ? attn_tc_smem_bytes(a.QRp, a.stages) : attn_smem_bytes(a.QRp, a.stages);
   op.name = "attention";
   return op;
 }
@@ -705,6 +711,7 @@ static dl_status build_plan(dl_plan* p) {
   };
 
   const size_t MH2 = static_cast<size_t>(M) * H * 2;
+  if (const char* e = std::getenv("DL_ATTN")) p->attn_tc = std::strcmp(e, "mma_sync") != 0;
   for (int l = 0; l < p->L; ++l) {
     const dl_layer_weights& lw = p->layers[l];
     const bool last = (l == p->L - 1);

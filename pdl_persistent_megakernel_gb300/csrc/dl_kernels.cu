@@ -61,7 +61,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(AttnArgs a, KernelCtx ctx)
   extern __shared__ uint8_t smem_raw[];
   Dep dep{};
   dep.mode = 0;
-  attn_op_t<kNMT>(a, blockIdx.x, dep, ctx, align1024(smem_raw));
+  attn_op_t<kNMT, false>(a, blockIdx.x, dep, ctx, align1024(smem_raw), 0u);
+}
+
+// tcgen05 attention: 512 TMEM columns (two O, two S buffers) for the CTA.
+__global__ void __launch_bounds__(kThreads, 1) k_attn_tc(AttnArgs a, KernelCtx ctx) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  if ((threadIdx.x >> 5) == 1) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  Dep dep{};
+  dep.mode = 0;
+  attn_op_t<1, true>(a, blockIdx.x, dep, ctx, align1024(smem_raw), tmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 1) tmem_dealloc(tmem, 512);
 }
 
 __global__ void k_bind(Binding* dst, Binding v) { *dst = v; }
@@ -317,6 +338,12 @@ const void* gemm_kernel(int mma, int m_or_mp) {
 }
 
 const void* norm_kernel() { return reinterpret_cast<const void*>(&k_norm); }
+const void* attn_tc_kernel() { return reinterpret_cast<const void*>(&k_attn_tc); }
+
+int attn_tc_smem_bytes(int QRp, int stages) {
+  return attn_tc_smem_layout(QRp, stages).total + 1024;
+}
+
 const void* attn_kernel(int QRp) {
   if (QRp <= 16) return reinterpret_cast<const void*>(&k_attn<1>);
   if (QRp <= 32) return reinterpret_cast<const void*>(&k_attn<2>);

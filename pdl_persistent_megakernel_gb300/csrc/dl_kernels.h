@@ -10,6 +10,8 @@ namespace dl {
 const void* gemm_kernel(int mma, int m_or_mp);
 const void* norm_kernel();
 const void* attn_kernel(int QRp);
+const void* attn_tc_kernel();
+int attn_tc_smem_bytes(int QRp, int stages);
 const void* mega_kernel();
 cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s);
 int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M);

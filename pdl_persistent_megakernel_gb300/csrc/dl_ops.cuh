@@ -1264,7 +1264,8 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
 
 // ============================================================== ATTENTION
 struct AttnSmem {
-  int stage_bytes, q_off, o_off, xs_off, stat_off, bar_off, misc_off, total;
+  int stage_bytes, stage_off, q_off, p_off, o_off, xs_off, stat_off, bar_off, tbar_off, misc_off,
+      total;
 };
 
 constexpr int kOP = 136;   // fp32 row pitch of the merged O tile (bank spread)
@@ -1275,6 +1276,8 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int QRp, int stages) {
   AttnSmem L;
   const int nmt = QRp / 16;
   L.stage_bytes = 4 * kAttnKeys * 128;
+  L.stage_off = 0;
+  L.p_off = L.tbar_off = 0;                         // (tcgen05 layout only)
   L.q_off = stages * L.stage_bytes;                 // bf16 [QRp][128], swizzled
   L.o_off = L.q_off + QRp * 256;                    // fp32 [QRp][kOP]
   // partial-score exchange [2][blocks per iteration][8][nmt*8][32]: two
@@ -1286,6 +1289,30 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int QRp, int stages) {
   // after the barriers: flags, producer page batch [32 units x 4 pages],
   // token positions [64], contributor list, combine weights [kMaxContrib]
   L.misc_off = L.bar_off + 2 * kMaxStages * 8;
+  L.total = L.misc_off + 64 + 32 * 4 * 4 + 64 * 4 + kMaxContrib * 4 + kMaxContrib * 4;
+  return L;
+}
+
+// Layout of the tcgen05 attention share.  Q and the two P buffers come
+// first: an M = 128 operand reads 128 rows of 128 bytes from each start,
+// and only the first QRp rows are the operand's (the rest alias what follows
+// and feed accumulator rows that are never read).
+//   Q  [2 d-halves][QRp][128 B]   P  [2][QRp][128 B]   (128-byte swizzle)
+//   stages  [S][K lo | K hi | V lo | V hi]   O  fp32 [QRp][kOP]
+//   row lse / positions / max / sum [QRp] each; stage, S/P/PV barriers;
+//   control area.
+__host__ __device__ inline AttnSmem attn_tc_smem_layout(int QRp, int stages) {
+  AttnSmem L;
+  L.stage_bytes = 4 * kAttnKeys * 128;
+  L.q_off = 0;
+  L.p_off = 2 * QRp * 128;
+  L.stage_off = (4 * QRp * 128 + 1023) & ~1023;
+  L.o_off = L.stage_off + stages * L.stage_bytes;
+  L.xs_off = L.o_off;                               // (no score exchange)
+  L.stat_off = L.o_off + QRp * kOP * 4;             // lse, positions, max, sum [QRp]
+  L.bar_off = (L.stat_off + 4 * QRp * 4 + 15) & ~15;
+  L.tbar_off = L.bar_off + 2 * kMaxStages * 8;      // s_full[2] s_free[2] p_full[2] pv_done[2]
+  L.misc_off = L.tbar_off + 8 * 8;
   L.total = L.misc_off + 64 + 32 * 4 * 4 + 64 * 4 + kMaxContrib * 4 + kMaxContrib * 4;
   return L;
 }
@@ -1472,6 +1499,321 @@ __device__ bool attn_combine(const AttnArgs& a, int c, const KernelCtx& ctx, con
     }
   }
   return true;
+}
+
+// Consumer side of a tcgen05 attention share (warps 1-8; layout
+// attn_tc_smem_layout; 512 TMEM columns: O0 [0, 128), O1 [128, 256),
+// S0 [256, 320), S1 [320, 384)).  For valid 64-key block g of the share:
+//   warp 2 (lane 0) issues S_g = Q K_g^T into S[g & 1] (M = 128 query rows,
+//     of which the first QRp are real, N = 64 keys, K = d in 8 steps);
+//   warp 3 (lane 0), once P_g is in shared memory, issues O[g & 1] +=
+//     P_g V_g (N = d, K = 64 keys in 4 steps, V read MN-major); its commits
+//     release K/V's stage and P's buffer;
+//   softmax: blocks alternate between two warps per TMEM lane quarter
+//     (rows 0-31: warps 4 and 8; rows 32-63: warps 1 and 5), each with its
+//     own running maximum and sum per row and its own O.  A warp reads its
+//     rows of S_g, masks them, writes P_g (bf16) and, for a partial block,
+//     zeroes the V rows past the context (0-probability keys must add
+//     exactly 0).  While a block's maximum is within 2^8 of the running one
+//     the running maximum stays (P <= 256; exact in the final
+//     normalisation, since the warp's O and sum share it); otherwise it
+//     moves and the warp rescales its O in TMEM after its previous block's
+//     PV.
+// At the end of a pair run the first warp of each pair merges the two
+// (maximum, sum, O) into Ob with the rows' log-sum-exp (base 2).
+__device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
+                               uint8_t* smem, const AttnSmem& L, const Pipe& P, uint32_t tmem) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int QRp = a.QRp, G = a.Hq / a.Hkv;
+  uint8_t* qs = smem + L.q_off;
+  uint8_t* ps = smem + L.p_off;
+  float* Ob = reinterpret_cast<float*>(smem + L.o_off);
+  float* row_lse = reinterpret_cast<float*>(smem + L.stat_off);
+  int* row_pos = reinterpret_cast<int*>(row_lse + QRp);
+  float* row_m1 = reinterpret_cast<float*>(row_pos + QRp);    // second warp's max / sum
+  float* row_l1 = row_m1 + QRp;
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + L.tbar_off);
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_full + 4;
+  uint64_t* pv_done = s_full + 6;
+  int* flag = reinterpret_cast<int*>(smem + L.misc_off);
+  int* ctb = flag + 16 + 32 * 4 + 64;
+  const int U = a.R * a.Hkv * a.NB;
+  const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
+  const Binding* bd = ctx.binding;
+  const int ct = tid - 32;
+  const int nq = QRp > 32 ? 2 : 1;                   // TMEM lane quarters in use
+  const int quarter = warp & 3;
+  // softmax role: quarter 0 -> warps 4 (k = 0), 8 (k = 1); quarter 1 -> warps 1, 5
+  const bool is_sm = (quarter < nq) && (warp == 4 || warp == 8 || warp == 1 || warp == 5);
+  const int kk_sm = (warp >= 5) ? 1 : 0;             // which of the pair
+  const int row = quarter * 32 + lane;
+  if (ct == 0) {
+    trace_stamp(ctx, c, TR_START);
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(u1 - u0));
+  }
+  if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return -1;
+  if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
+  const int* pos = resolve<const int>(a.pos, bd);
+  const uint16_t* qg = static_cast<const uint16_t*>(a.q);
+  const uint32_t qs_u32 = smem_u32(qs), ps_u32 = smem_u32(ps);
+  const uint32_t idesc_s = umma_idesc(kAttnKeys, true);
+  const uint32_t idesc_o = umma_idesc(128, true) | (1u << 16);   // B (V) MN-major
+  const uint32_t t_o = tmem, t_s = tmem + 256;
+  const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+  bool dead = false;
+  int i = 0;                                // valid blocks before this run (the producer's slots)
+  int pend[2], npend = 0;
+  int u = u0;
+  while (u < u1) {
+    const int p = u / a.NB, blk_a = u % a.NB;
+    const int run_end = min(u1, (p + 1) * a.NB);
+    const int blk_b = run_end - p * a.NB;
+    const int r = p / a.Hkv, h = p % a.Hkv;
+    const int ctxr = pos[r * a.T + a.T - 1] + 1;
+    const int nvb = (ctxr + kAttnKeys - 1) / kAttnKeys;
+    const int n = max(0, min(blk_b, nvb) - blk_a);    // valid blocks of this run
+    // this pair's query rows: [d-half][row][128 B], 16-byte chunk c8 of a
+    // row at (c8 ^ (row & 7)) (128-byte swizzle); rows QR..QRp-1 zero
+#pragma unroll 4
+    for (int e = ct; e < QRp * 16; e += 256) {
+      const int rr = e >> 4, ch = e & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (rr < a.QR) {
+        const int t = rr / G, g = rr % G;
+        const size_t src = (static_cast<size_t>(r * a.T + t) * a.Hq + h * G + g) * 128 + ch * 8;
+        v = __ldcg(reinterpret_cast<const uint4*>(qg + src));
+      }
+      const int hf = ch >> 3, c8 = ch & 7;
+      *reinterpret_cast<uint4*>(qs + hf * QRp * 128 + rr * 128 + ((c8 ^ (rr & 7)) << 4)) = v;
+    }
+    for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
+    fence_proxy_async_shared();    // Q, written by threads, is read by the tensor core
+    named_bar(1, 256);
+    if (warp == 2) {
+      // --------------------------------------------------- QK^T issuer
+      if (lane == 0 && !dead && n > 0) {
+        int last = -1;
+        for (int j = 0; j < n; ++j) {
+          const int g = i + j;
+          const uint32_t q = pipe_q(P, g);
+          if (!mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 80) ||
+              (g >= 2 && !mbar_wait(&s_free[g & 1], ((g >> 1) - 1) & 1, ctx, 81))) {
+            dead = true;
+            break;
+          }
+          if (g == 0) trace_stamp(ctx, c, TR_FIRST);
+          tc_fence_after();
+          const uint32_t kb = smem_u32(attn_k(P, g));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = umma_desc_sw128(qs_u32 + (kk >> 2) * QRp * 128 + (kk & 3) * 32);
+            const uint64_t bdd = umma_desc_sw128(kb + (kk >> 2) * kAttnKeys * 128 + (kk & 3) * 32);
+            umma_bf16(t_s + (g & 1) * kAttnKeys, ad, bdd, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[g & 1]);
+          last = g;
+        }
+        // nothing the tensor core still runs may outlive the share
+        if (dead && last >= 0) mbar_drain(&s_full[last & 1], (last >> 1) & 1, ctx.budget_ns);
+      }
+      dead = __shfl_sync(0xffffffffu, dead ? 1 : 0, 0) != 0;
+    } else if (warp == 3) {
+      // ------------------------------------------------------- PV issuer
+      if (lane == 0 && !dead && n > 0) {
+        int last = -1;
+        for (int j = 0; j < n; ++j) {
+          const int g = i + j;
+          if (!mbar_wait(&p_full[g & 1], (g >> 1) & 1, ctx, 82)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = smem_u32(attn_v(P, g));
+          const uint32_t pb = ps_u32 + (g & 1) * QRp * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = umma_desc_sw128(pb + kk * 32);
+            // keys kk*16 .. +15: two 8-key groups (1024 B apart); the d
+            // halves (64 elements each) are 8 KiB apart
+            const uint64_t bdd = umma_desc_sw128_mn(vb + kk * 2048, kAttnKeys * 128, 1024);
+            // O[g & 1] starts at the run's first block of its parity
+            umma_bf16(t_o + (g & 1) * 128, ad, bdd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(pipe_empty(P, pipe_q(P, g)));
+          umma_commit(&pv_done[g & 1]);
+          last = g;
+        }
+        if (dead && last >= 0) mbar_drain(&pv_done[last & 1], (last >> 1) & 1, ctx.budget_ns);
+      }
+      dead = __shfl_sync(0xffffffffu, dead ? 1 : 0, 0) != 0;
+    } else if (is_sm) {
+      // --------------------------------------------------- softmax warps
+      const int lim = row < QRp ? row_pos[row] : -1;    // rows past QRp: all masked
+      const int lim0 = row_pos[0];                       // the pair's first query position
+      const float scl = a.scale_log2;
+      const uint32_t t_my = t_o + static_cast<uint32_t>(((i + kk_sm) & 1) * 128) + t_lane;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = kk_sm; j < n && !dead; j += 2) {
+        const int g = i + j;
+        const int k0 = (blk_a + j) * kAttnKeys;
+        const int nk = min(kAttnKeys, ctxr - k0);
+        if (!warp_wait(&s_full[g & 1], (g >> 1) & 1, ctx, 83)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        float sv[kAttnKeys];
+#pragma unroll
+        for (int c4 = 0; c4 < kAttnKeys / 16; ++c4)
+          tmem_ld16(t_s + t_lane + (g & 1) * kAttnKeys + c4 * 16, sv + c4 * 16);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[g & 1]);
+        // the block's row maximum of the scores (the scale is positive, so it
+        // is applied after the max and folded into the exponent below); a
+        // whole block before the pair's first new token needs no mask
+        float mx = -INFINITY;
+        if (nk == kAttnKeys && k0 + kAttnKeys - 1 <= lim0) {
+#pragma unroll
+          for (int e = 0; e < kAttnKeys; ++e) mx = fmaxf(mx, sv[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kAttnKeys; ++e) {
+            sv[e] = (e < nk && k0 + e <= lim) ? sv[e] : -INFINITY;
+            mx = fmaxf(mx, sv[e]);
+          }
+        }
+        mx = row < QRp ? mx * scl : -INFINITY;
+        const bool grow = mx > m_run + 8.f;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mx);
+          m_run = mx;
+        }
+        l_run *= alpha;
+        // P buffer g & 1 and this warp's O were last used by PV_{g-2}
+        if (g >= 2 && !warp_wait(&pv_done[g & 1], ((g >> 1) - 1) & 1, ctx, 85)) {
+          dead = true;
+          break;
+        }
+        // this warp's O holds its earlier blocks of the run: rescale it
+        const float oa = (grow && j >= 2) ? alpha : 1.f;
+        if (__any_sync(0xffffffffu, oa != 1.f)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 8; ++c16) {
+            float ov[16];
+            tmem_ld16(t_my + c16 * 16, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] *= oa;
+            tmem_st16(t_my + c16 * 16, ov);
+          }
+          tmem_wait_st();
+        }
+        const float nmb = m_run == -INFINITY ? 0.f : -m_run;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[kAttnKeys / 2];
+#pragma unroll
+        for (int e = 0; e < kAttnKeys; e += 2) {
+          const float p0 = ex2_approx(fmaf(sv[e], scl, nmb));
+          const float p1 = ex2_approx(fmaf(sv[e + 1], scl, nmb));
+          s4[(e >> 1) & 3] += p0 + p1;
+          pk[e >> 1] = pack_bf16(p0, p1);
+        }
+        l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (nk < kAttnKeys && quarter == 0) {
+          // V rows past the context were not loaded (or are stale)
+          uint8_t* vst = attn_v(P, g);
+          for (int e = lane; e < (kAttnKeys - nk) * 16; e += 32) {
+            const int key = nk + (e >> 4), hf = (e >> 3) & 1, c8 = e & 7;
+            *reinterpret_cast<uint4*>(vst + hf * kAttnKeys * 128 + key * 128 + c8 * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (row < QRp) {
+          uint8_t* prow = ps + (g & 1) * QRp * 128 + row * 128;
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        }
+        fence_proxy_async_shared();   // P and the zeroed V rows feed the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+      }
+      // merge the two warps' (max, sum, O) per row: the second hands its max
+      // and sum over, the first reads both O and writes Ob and the lse
+      if (kk_sm == 1 && row < QRp) {
+        row_m1[row] = m_run;
+        row_l1[row] = l_run;
+      }
+      named_bar(3 + quarter, 64);
+      if (kk_sm == 0) {
+        const float m1 = row < QRp ? row_m1[row] : -INFINITY;
+        const float l1 = row < QRp ? row_l1[row] : 0.f;
+        const float mm = fmaxf(m_run, m1);
+        const float f0 = l_run > 0.f ? exp2f(m_run - mm) : 0.f;
+        const float f1 = l1 > 0.f ? exp2f(m1 - mm) : 0.f;
+        const float l = l_run * f0 + l1 * f1;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool use0 = __any_sync(0xffffffffu, l_run > 0.f);
+        const bool use1 = __any_sync(0xffffffffu, l1 > 0.f);
+        bool ok = n > 0 && !dead;
+        if (ok) {
+          // the last PV into each O
+          const int g0 = i + ((n - 1) & ~1);
+          const int g1 = i + ((n & 1) ? n - 2 : n - 1);
+          ok = warp_wait(&pv_done[g0 & 1], (g0 >> 1) & 1, ctx, 86) &&
+               (n < 2 || warp_wait(&pv_done[g1 & 1], (g1 >> 1) & 1, ctx, 87));
+          if (!ok) dead = true;
+        }
+        if (ok) {
+          tc_fence_after();
+          const uint32_t ta = t_o + static_cast<uint32_t>((i & 1) * 128) + t_lane;
+          const uint32_t tb = t_o + static_cast<uint32_t>(((i + 1) & 1) * 128) + t_lane;
+#pragma unroll 1
+          for (int c16 = 0; c16 < 8; ++c16) {
+            float o0[16], o1[16];
+            if (use0) tmem_ld16(ta + c16 * 16, o0);
+            if (use1) tmem_ld16(tb + c16 * 16, o1);
+            tmem_wait_ld();
+            if (row < QRp) {
+#pragma unroll
+              for (int e4 = 0; e4 < 4; ++e4) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int x = e4 * 4 + e;
+                  v[e] = ((use0 && l_run > 0.f) ? o0[x] * f0 : 0.f) +
+                         ((use1 && l1 > 0.f) ? o1[x] * f1 : 0.f);
+                }
+                *reinterpret_cast<float4*>(Ob + row * kOP + c16 * 16 + e4 * 4) =
+                    make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+              }
+            }
+          }
+          tc_fence_before();
+        } else if (row < QRp) {
+          for (int e4 = 0; e4 < 32; ++e4)
+            *reinterpret_cast<float4*>(Ob + row * kOP + e4 * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (row < QRp) row_lse[row] = l > 0.f ? mm + log2f(l) : -INFINITY;
+      }
+    }
+    if (named_bar_or(1, 256, dead)) return -1;
+    attn_pair_out(a, c, u0, p, blk_a, blk_b, Ob, row_lse, pend, &npend);
+    named_bar(1, 256);
+    i += n;
+    u = run_end;
+  }
+  if (ct == 0) trace_stamp(ctx, c, TR_LOOP_END);
+  if (!attn_combine(a, c, ctx, pend, npend, flag, ctb)) return -1;
+  if (ct == 0) trace_stamp(ctx, c, TR_END);
+  return i;
 }
 
 // Consumer side of an attention share (warps 1-8): `priv` is the share's
@@ -1845,13 +2187,15 @@ __device__ int attn_consume_t(const AttnArgs& a, int c, const Dep& dep,
 }
 
 
-template <int kNMT>
+// Standalone attention share: the K/V producer (warp 0) and the mma.sync
+// consumer, or (kTC) the tcgen05 consumer over `tmem` (512 columns).
+template <int kNMT, bool kTC>
 __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
-                          const KernelCtx& ctx, uint8_t* smem) {
+                          const KernelCtx& ctx, uint8_t* smem, uint32_t tmem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QRp = a.QRp;
-  const AttnSmem L = attn_smem_layout(QRp, a.stages);
-  uint8_t* stage0 = smem;
+  const AttnSmem L = kTC ? attn_tc_smem_layout(QRp, a.stages) : attn_smem_layout(QRp, a.stages);
+  uint8_t* stage0 = smem + L.stage_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kMaxStages;
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
@@ -1866,7 +2210,19 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
+      mbar_init(&empty[s], kTC ? 1 : 8);   // one MMA commit, or 8 consumer warps
+    }
+    if (kTC) {
+      uint64_t* tb = reinterpret_cast<uint64_t*>(smem + L.tbar_off);
+      const uint32_t nsm = QRp > 32 ? 2u : 1u;
+      mbar_init(&tb[0], 1);      // s_full: QK^T commit
+      mbar_init(&tb[1], 1);
+      mbar_init(&tb[2], nsm);    // s_free: softmax warps read S
+      mbar_init(&tb[3], nsm);
+      mbar_init(&tb[4], nsm);    // p_full: softmax warps wrote P
+      mbar_init(&tb[5], nsm);
+      mbar_init(&tb[6], 1);      // pv_done: PV commit
+      mbar_init(&tb[7], 1);
     }
     flag[0] = flag[1] = 0;
     flag[2] = 1;
@@ -1990,18 +2346,11 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
   P.seq0 = 0;
   P.ups = 1;
   P.x_bytes = 0;
-  P.empty_cnt = 8;
-  attn_consume_t<kNMT, true>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
-}
-
-__device__ void attn_op(const AttnArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
-                        uint8_t* smem) {
-  if (a.QRp <= 16)
-    attn_op_t<1>(a, c, dep, ctx, smem);
-  else if (a.QRp <= 32)
-    attn_op_t<2>(a, c, dep, ctx, smem);
+  P.empty_cnt = kTC ? 1 : 8;
+  if constexpr (kTC)
+    attn_consume_tc(a, c, dep, ctx, smem, L, P, tmem);
   else
-    attn_op_t<4>(a, c, dep, ctx, smem);
+    attn_consume_t<kNMT, true>(a, c, dep, ctx, smem + S * L.stage_bytes, P);
 }
 
 // ========================================================= MEGAKERNEL

@@ -139,9 +139,12 @@ def _check_intermediates(c, plan, out):
 
 @pytest.mark.parametrize("name", ["bf16_m1", "fp8_m16", "step_m1"])
 def test_schedules_bitwise_identical(name):
-    """Serial, graph (linear, +PDL) and megakernel run the same tile engines
-    over the same work split, so their results are bit-identical; replaying
-    a step with the same inputs reproduces it exactly."""
+    """Serial and graph (linear, +PDL) launch the same kernels over the same
+    work split, so their results are bit-identical; replaying a step with the
+    same inputs reproduces it exactly.  The megakernel runs the same
+    projection engines and the mma.sync attention engine (the standalone
+    kernels run attention on tcgen05): its cache and outputs agree to
+    rounding (bf16 tolerance)."""
     c = case(name)
     plan = c.plan()
     outs = {}
@@ -150,9 +153,16 @@ def test_schedules_bitwise_identical(name):
         out, kv = c.run(plan, mode, steps=3)
         outs[mode] = (out.cpu(), kv.cpu())
     base = outs[dl.MODE_SERIAL]
+    u16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
     for mode, (o, k) in outs.items():
-        assert torch.equal(o, base[0]), dl.MODE_NAMES[mode]
-        assert torch.equal(k, base[1]), dl.MODE_NAMES[mode]
+        if mode == dl.MODE_MEGAKERNEL:
+            # (greedy ids of the full step are checked against the oracle)
+            bf16_close(u16(k), u16(base[1]), "megakernel vs serial cache")
+            if o.dtype == torch.bfloat16:
+                bf16_close(u16(o), u16(base[0]), "megakernel vs serial")
+        else:
+            assert torch.equal(k, base[1]), dl.MODE_NAMES[mode]
+            assert torch.equal(o, base[0]), dl.MODE_NAMES[mode]
     plan.close()
 
 
