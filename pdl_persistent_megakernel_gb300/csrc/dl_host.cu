@@ -272,11 +272,12 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   a.up_row = s.up_row;
   const long long U = static_cast<long long>(a.NT) * a.KB;
   a.G = static_cast<int>(std::min<long long>(p->sms, U));
+  a.share_max = static_cast<int>((U + a.G - 1) / a.G);
   const int npair = s.pair ? 2 : 1;
   // a stage: 32 KiB of tiles (gate + up, or two consecutive units) and one
   // activation slice per unit
   const int stage_bytes = 32768 + (npair == 1 ? 2 : 1) * (((a.Mp * 128 + 1023) / 1024) * 1024);
-  const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0, a.KB, a.fp8, s.epi, a.M);
+  const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0, a.KB, a.fp8, s.epi, a.M, a.share_max);
   // one CTA per SM; 3-4 stages of 32 KiB in flight per SM already reach the
   // HBM copy rate, a few more absorb jitter
   a.stages = std::min(5, choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget));
@@ -287,7 +288,7 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   a.done_cnt = cnt + a.NT;
   op.kernel = gemm_kernel(a.mma, a.mma ? a.Mp : a.M);
   op.grid = a.G;
-  op.smem = gemm_smem_bytes(npair, a.Mp, a.stages, a.KB, a.fp8, s.epi, a.M);
+  op.smem = gemm_smem_bytes(npair, a.Mp, a.stages, a.KB, a.fp8, s.epi, a.M, a.share_max);
   op.name = s.name;
   return op;
 }
@@ -903,7 +904,8 @@ static dl_status build_plan(dl_plan* p) {
       if (op.args.kind == OP_GEMM) {
         const GemmArgs& a = op.args.gemm;
         slot = std::max(slot, 32768 + (a.pair ? 1 : 2) * (((a.Mp * 128 + 1023) / 1024) * 1024));
-        priv = std::max(priv, gemm_smem_bytes(a.pair ? 2 : 1, a.Mp, 0, a.KB, a.fp8, a.epi, a.M));
+        priv = std::max(priv, gemm_smem_bytes(a.pair ? 2 : 1, a.Mp, 0, a.KB, a.fp8, a.epi, a.M,
+                                              a.share_max));
       } else if (op.args.kind == OP_ATTN) {
         priv = std::max(priv, attn_smem_bytes(op.args.attn.QRp, 0));
       }

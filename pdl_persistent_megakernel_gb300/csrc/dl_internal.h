@@ -119,6 +119,7 @@ struct GemmArgs {
   int M, Mp;                  // tokens, rows of the activation tile
   int K;                      // elements
   int KB;                     // 128-byte k-blocks per tile
+  int share_max;              // units of the largest CTA share (ceil(NT KB / G))
   int NT;                     // output tiles (pairs for gate/up)
   int t_base;                 // first tile (a branch may cover a sub-range)
   int pair;                   // 1: tile t = gate rows t*128.. + up rows up_row+t*128..

@@ -356,8 +356,8 @@ cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M) {
-  return gemm_smem_layout(npair, Mp, stages, KB, fp8, epi, M).total + 1024;
+int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M, int share) {
+  return gemm_smem_layout(npair, Mp, stages, KB, fp8, epi, M, share).total + 1024;
 }
 
 int attn_smem_bytes(int QRp, int stages) {

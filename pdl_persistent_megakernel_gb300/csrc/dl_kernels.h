@@ -14,7 +14,7 @@ const void* attn_tc_kernel();
 int attn_tc_smem_bytes(int QRp, int stages);
 const void* mega_kernel();
 cudaError_t launch_bind(Binding* dst, const Binding& v, cudaStream_t s);
-int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M);
+int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int M, int share);
 int attn_smem_bytes(int QRp, int stages);
 // CTAs of a split-KV attention over `pairs` (request, kv head) streams of
 // `nb` 64-key blocks on `sms` SMs (dl_host.cu).

@@ -268,7 +268,8 @@ __host__ __device__ inline int gemm_ntout(int npair, int Mp) {
 // epilogue's per-token positions / cache rows / RoPE rows, barriers and a
 // small control area (flags, contributor list of a Stream-K fix-up).
 __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stages,
-                                                     int KB, int fp8, int epi, int M) {
+                                                     int KB, int fp8, int epi, int M,
+                                                     int share) {
   GemmSmem L;
   L.w_bytes = 16384;
   L.x_bytes = ((Mp * 128 + 1023) / 1024) * 1024;
@@ -278,7 +279,7 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   L.tile_off = stages * L.stage_bytes;
   L.sx_off = L.tile_off + gemm_ntout(npair, Mp) * npair * Mp * 128 * 4;
   L.sw_off = L.sx_off + (fp8 ? KB * Mp * 4 : 0);
-  L.epi_off = ((L.sw_off + (fp8 ? 2 * KB * 4 : 0)) + 15) & ~15;
+  L.epi_off = ((L.sw_off + (fp8 ? 2 * share * 4 : 0)) + 15) & ~15;   // sw [2][share]
   L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) : 0);
   L.bar_off = (L.bar_off + 15) & ~15;
   L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 4) * 8;
@@ -682,6 +683,21 @@ __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShar
   named_bar(bar, nthr);
 }
 
+// Weight scales of every unit of the share [npair][n] (weights are not an
+// operation's output: staged before the dependency wait; read after the
+// epilogue group's next barrier).
+__device__ __forceinline__ void stage_w_scales(const GemmArgs& a, const GemmShared& sh, int u0,
+                                               int n, int nthr, int ct) {
+  const int npair = a.pair ? 2 : 1;
+  for (int e = ct; e < npair * n; e += nthr) {
+    const int p = e / n, i = e - p * n;
+    const int u = u0 + i;
+    const int tg = a.t_base + u / a.KB, kb = u % a.KB;
+    const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
+    sh.sw[p * n + i] = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb);
+  }
+}
+
 // ------------------------------------------------------------ pipelines
 // Where the operands of a pipeline's units live and how they are handed
 // over.  Every slot holds 32 KiB of weight tiles or K/V, then activation
@@ -806,6 +822,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     // the QKV epilogue's operands (positions, cache rows, RoPE rows) are
     // step inputs: load them before the dependency wait
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 256, ct, 1, ctx, sh);
+    if (a.fp8) stage_w_scales(a, sh, u0, nunits, 256, ct);
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
     if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 256, ct, 1);
@@ -816,16 +833,6 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       const int u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
-      const int tg = a.t_base + tl;
-      if (a.fp8) {
-        // this run's weight scales sw[p][k]
-        for (int e = ct; e < npair * run; e += 256) {
-          const int p = e / run, k = e % run;
-          const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
-          sh.sw[p * run + k] = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb0 + k);
-        }
-        named_bar(1, 256);
-      }
       float acc[2][4][kMG];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
@@ -864,7 +871,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           for (int p = 0; p < 2; ++p) {
             if (p >= npair) break;
             const uint8_t* wt = gemm_w(P, i, p);
-            const float sw = sh.sw[p * run + k];
+            const float sw = sh.sw[p * nunits + i];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int r = r0 + 32 * j;
@@ -1005,6 +1012,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     const int q = warp & 3;
     const int row = q * 32 + lane;
     if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
+    if (a.fp8) stage_w_scales(a, sh, u0, nunits, 128, et);
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
     if (et == 0) trace_stamp(ctx, c, TR_DEPS);
     if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
@@ -1020,15 +1028,6 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       const int u = u0 + i;
       const int tl = static_cast<int>(u / a.KB), kb0 = static_cast<int>(u % a.KB);
       const int run = min(nunits - i, a.KB - kb0);
-      const int tg = a.t_base + tl;
-      if (a.fp8) {
-        for (int e = et; e < npair * run; e += 128) {
-          const int p = e / run, k = e % run;
-          const int rt = p == 0 ? tg : (a.up_row >> 7) + tg;
-          sh.sw[p * run + k] = __ldg(a.w_scale + static_cast<size_t>(rt) * a.KB + kb0 + k);
-        }
-        named_bar(2, 128);
-      }
       float acc[2][kMp];
 #pragma unroll
       for (int p = 0; p < 2; ++p)
@@ -1043,8 +1042,8 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         if (dead) continue;
         tc_fence_after();
         const uint32_t tb = tl_base + static_cast<uint32_t>(b) * tstride;
-        const float sw0 = fp8 ? sh.sw[k] : 1.f;
-        const float sw1 = (fp8 && npair == 2) ? sh.sw[run + k] : 1.f;
+        const float sw0 = fp8 ? sh.sw[i] : 1.f;
+        const float sw1 = (fp8 && npair == 2) ? sh.sw[nunits + i] : 1.f;
         const float4* sxk = reinterpret_cast<const float4*>(sh.sx + (kb0 + k) * kMp);
 #pragma unroll
         for (int c16 = 0; c16 < kMp / 16; ++c16) {
@@ -1119,7 +1118,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
 // `stages` of them) and the private area after them.
 __device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* smem, int stages) {
   const int npair = a.pair ? 2 : 1;
-  const GemmSmem L = gemm_smem_layout(npair, a.Mp, stages, a.KB, a.fp8, a.epi, a.M);
+  const GemmSmem L = gemm_smem_layout(npair, a.Mp, stages, a.KB, a.fp8, a.epi, a.M, a.share_max);
   GemmShared sh;
   sh.stage0 = smem;
   sh.tout = reinterpret_cast<float*>(smem + L.tile_off);
@@ -1149,7 +1148,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   constexpr bool kMMA = kMp > 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npair = a.pair ? 2 : 1;
-  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M);
+  const GemmSmem L = gemm_smem_layout(npair, a.Mp, a.stages, a.KB, a.fp8, a.epi, a.M, a.share_max);
   const GemmShared sh = gemm_shared(a, smem, a.stages);
   const int U = a.NT * a.KB;
   const int u0 = sk_begin(U, a.G, c), u1 = sk_begin(U, a.G, c + 1);
@@ -1180,10 +1179,12 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
   const int nslots = (nunits + ups - 1) / ups;
   if (warp == 0) {
     // ------------------------------------------------------- producer
-    if (lane != 0) {
-      idle_wait(dep);
-      return;
-    }
+    // Lanes 1-31 leave at once: a warp whose other lanes sit in
+    // griddepcontrol.wait does not run lane 0 either (measured: the weight
+    // loads then start only when the previous kernel has finished).  The
+    // CTA's other threads pass the dependency, so its completion still
+    // implies its dependencies' completion.
+    if (lane != 0) return;
     prefetch_tmap(a.tmap_w);
     prefetch_tmap(a.tmap_x);
     const uint32_t ub = npair * 16384 + a.Mp * 128;   // bytes of one unit
