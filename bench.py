@@ -183,6 +183,73 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Crossover sweep of the Qwen3-8B-shaped layer: batch {1, 4, 16, 64}
+    requests of one token x context {1024, 8192, 32768}, bf16 and FP8
+    weights; per cell the serial, graph + PDL and megakernel step times
+    (L2 flushed before every step), the best schedule's achieved HBM GB/s
+    and the PDL-vs-megakernel gap.  One line per cell on stderr, one JSON
+    summary line on stdout."""
+    import torch
+
+    import pdl_persistent_megakernel_gb300 as dl
+    from pdl_persistent_megakernel_gb300 import bytes_model, synth
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    modes = [dl.MODE_SERIAL, dl.MODE_GRAPH_LINEAR_PDL, dl.MODE_MEGAKERNEL]
+    cells = []
+    for fp8 in (False, True):
+        wd = None
+        for batch in (1, 4, 16, 64):
+            for ctx in (1024, 8192, 32768):
+                cfg = synth.sweep_config(batch, ctx, fp8)
+                if wd is None:   # one weight set per dtype (same shapes)
+                    wd = synth.make_weights(cfg, device=device)
+                inp = synth.make_inputs(cfg, device=device)
+                plan = dl.Plan(cfg, wd, modes_mask=sum(1 << m for m in modes))
+                out = torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device)
+                algo = bytes_model.algorithmic_bytes(cfg)["total"]
+                res = {}
+                with torch.cuda.stream(stream):
+                    for m in modes:
+                        for _ in range(args.warmup):
+                            plan.step(inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"],
+                                      inp["positions"], out, m, stream)
+                        evs = []
+                        for _ in range(args.steps):
+                            flush.zero_()
+                            a, b = (torch.cuda.Event(enable_timing=True),
+                                    torch.cuda.Event(enable_timing=True))
+                            a.record(stream)
+                            plan.step(inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"],
+                                      inp["positions"], out, m, stream)
+                            b.record(stream)
+                            evs.append((a, b))
+                        torch.cuda.synchronize(device)
+                        res[dl.MODE_NAMES[m]] = statistics.median(
+                            [a.elapsed_time(b) * 1e3 for a, b in evs])
+                plan.status()
+                plan.close()
+                best = min(res, key=res.get)
+                cell = {"batch": batch, "context": ctx, "dtype": "fp8_e4m3" if fp8 else "bf16",
+                        "us": {k: round(v, 2) for k, v in res.items()}, "best": best,
+                        "best_GBs": round(algo / (res[best] * 1e-6) / 1e9, 1),
+                        "frac_of_8TBs": round(algo / (res[best] * 1e-6) / 1e9 / HBM_NOMINAL_GBS, 3),
+                        "mega_over_pdl": round(res["megakernel"] / res["graph_linear_pdl"], 3),
+                        "algorithmic_bytes": algo}
+                cells.append(cell)
+                print(json.dumps(cell), file=sys.stderr, flush=True)
+                del inp, out
+                torch.cuda.empty_cache()
+    print(json.dumps({"metric": "crossover sweep: decode-layer us per schedule and best GB/s",
+                      "cells": cells, "steps": args.steps, "warmup": args.warmup,
+                      "l2": "256 MiB write between timed steps", "data": "synthetic"}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -194,6 +261,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--per-kernel", action="store_true", default=True)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the crossover sweep (batch x context x dtype) instead")
     ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
                     help="flush: a 256 MiB write before every step; stream: steps back to "
                          "back (each step reads more bytes than the 129 MB L2 holds)")
@@ -201,6 +270,9 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
 
     import torch
@@ -215,7 +287,8 @@ def main():
         dist.init_process_group("gloo")
 
     need_cpu = (rank == 0 and ws == 1 and not args.no_cpu)
-    cfg, w, inp = build_workload(args.config, device, cpu_weights=True)
+    # the weights are drawn on the host only when the oracle leg needs them
+    cfg, w, inp = build_workload(args.config, device, cpu_weights=need_cpu)
     wd = to_dev(w, device)
     modes = [m for m in args.modes.split(",") if m]
     name_to_mode = {v: k for k, v in dl.MODE_NAMES.items()}

@@ -824,14 +824,20 @@ static dl_status build_plan(dl_plan* p) {
       if (U * G >= (1LL << 32)) return fail(DL_ERR_PLAN_INVALID, "too many work units for one op");
     }
   if (const char* e = std::getenv("DL_L2_PREFETCH_UNITS")) p->pf_units = std::atoi(e);
-  // L2 prefetch: a norm, an attention or a projection directly followed (on
-  // the same stream) by a projection warms L2 with the weight tiles that
+  // L2 prefetch: an attention or a projection directly followed (on the
+  // same stream) by a projection warms L2 with the weight tiles that
   // projection's first stages load, once its own loads are out
   for (auto* list : {&p->lin, &p->dag})
     for (size_t i = 0; i + 1 < list->size(); ++i) {
       LaunchOp& cur = (*list)[i];
       const LaunchOp& nx = (*list)[i + 1];
       if (nx.args.kind != OP_GEMM || nx.branch != 0 || cur.branch != 0) continue;
+      // not from a norm: its M CTAs (one at batch 1) would issue the whole
+      // projection's prefetches through their own TMA units (measured: 38
+      // and 78 us before the QKV and gate/up projections at batch 1), and
+      // under programmatic dependent launch the projection's CTAs load their
+      // first stages during the norm themselves
+      if (cur.args.kind == OP_NORM) continue;
       const GemmArgs& g = nx.args.gemm;
       PrefetchSpec pf;
       pf.tmap = g.tmap_w;
@@ -847,8 +853,7 @@ static dl_status build_plan(dl_plan* p) {
       // the boundary's own latency-bound reads
       pf.units = std::max(0, p->pf_units);
       if (pf.units == 0) pf.tmap = nullptr;
-      if (cur.args.kind == OP_NORM) cur.args.norm.pf = pf;
-      else if (cur.args.kind == OP_ATTN) cur.args.attn.pf = pf;
+      if (cur.args.kind == OP_ATTN) cur.args.attn.pf = pf;
       else if (cur.args.kind == OP_GEMM) cur.args.gemm.pf = pf;
     }
 

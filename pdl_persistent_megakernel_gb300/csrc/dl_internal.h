@@ -106,7 +106,6 @@ struct NormArgs {
   float* h_scale;     // FP8: [M, H/128]
   int fp8, M, H, rows_per_cta;
   float eps;
-  PrefetchSpec pf;
 };
 
 struct GemmArgs {

@@ -128,13 +128,6 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
                         const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x;
   if (tid < 32) {
-    // the next projection's first weight tiles (independent of everything)
-    // stream into L2 while this short op runs: share c' is prefetched by
-    // lane (c' / norm CTAs) % 32 of norm CTA c' mod (norm CTAs)
-    if (a.pf.tmap && dep.mode == 0) {
-      const int nc = static_cast<int>(gridDim.x);
-      for (int c2 = c + tid * nc; c2 < a.pf.G; c2 += 32 * nc) prefetch_next_share(a.pf, c2);
-    }
     idle_wait(dep);
     return;
   }
