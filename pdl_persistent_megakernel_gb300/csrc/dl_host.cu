@@ -601,7 +601,11 @@ static dl_status build_plan(dl_plan* p) {
   p->M = p->R * p->T;
   p->fp8 = c.weight_dtype == DL_WEIGHT_FP8_E4M3_B128;
   p->full = c.vocab > 0;
-  p->mma = p->M > 4;   // CUDA-core GEMV up to 4 tokens, tcgen05 beyond
+  // One token: the CUDA-core GEMV (a warp per 16 rows).  From two tokens on,
+  // tcgen05 with the tokens padded to N = 16: at 4 tokens the GEMV is bound
+  // by its FP8 unpacking and dot products (measured 1.05 us per unit of the
+  // Qwen3-8B QKV projection, against 0.41 us for tcgen05 at 16 tokens).
+  p->mma = p->M > 1;
   p->Mp = p->mma ? (p->M <= 16 ? 16 : (p->M <= 32 ? 32 : 64)) : p->M;
   p->Mrows = p->Mp;
   if (!load_encode()) return fail(DL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
