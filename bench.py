@@ -64,6 +64,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int) -> float:
+    """The slowest rank's figure (the process group is up when ws > 1)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class Clocks:
     """nvidia-smi sampling (200 ms) during the timed region."""
 
@@ -336,11 +347,7 @@ def main():
         for m in modes:
             mode = name_to_mode[m]
             ms = timed_steps(mode, args.steps, args.warmup)
-            mean_ms = sum(ms) / len(ms)
-            if ws > 1:
-                t = torch.tensor([mean_ms], dtype=torch.float64)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                mean_ms = float(t.item())
+            mean_ms = max_over_ranks(sum(ms) / len(ms), ws)
             results[m] = {"us": mean_ms * 1e3, "us_median": statistics.median(ms) * 1e3,
                           "us_p10": sorted(ms)[max(0, len(ms) // 10)] * 1e3,
                           "GBs": ws * algo / (mean_ms * 1e-3) / 1e9}
@@ -411,11 +418,7 @@ def main():
             evs.append((a, b))
         barrier()
     plan.status()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / len(evs), ws)
     h2d = xh.numel() * 2 + rh.numel() * 2 + bth.numel() * 4 + posh.numel() * 4
     d2h = outh.numel() * outh.element_size()
     e2e = {"value": ws * algo / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",

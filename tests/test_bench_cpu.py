@@ -1,0 +1,93 @@
+"""Host-side checks of bench.py: the reference arm's JSON line (the oracle
+timed on this host's cores), its behaviour under a two-rank torchrun (rank
+0 alone prints), and the slowest-rank aggregation over a two-rank gloo
+process group.  No GPU is used."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+SMALL = ["--config", "q06_layer_b1_ctx1024", "--steps", "1", "--warmup", "0"]
+
+
+def _json_lines(out: str):
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"] + SMALL,
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1, r.stdout
+    d = lines[0]
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["steps"] == 1
+    assert d["config"]["workload"] == "q06_layer_b1_ctx1024"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert abs(d["ms_per_step"] * 1e-3 * d["value"] * 1e9 - _algo_bytes("q06_layer_b1_ctx1024")) \
+        < 1e-6 * _algo_bytes("q06_layer_b1_ctx1024")
+
+
+def _algo_bytes(name):
+    from pdl_persistent_megakernel_gb300 import bytes_model, synth
+    return bytes_model.algorithmic_bytes(synth.CONFIGS[name])["total"]
+
+
+def test_reference_arm_two_ranks_rank0_prints():
+    """Under torchrun with two ranks the reference arm runs on rank 0 only:
+    one JSON line, both ranks exit 0."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", "29631",
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2"] + SMALL
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def _max_rank(rank, ws, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    import bench
+    q.put((rank, bench.max_over_ranks(10.0 + 5.0 * rank, ws)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    """The per-schedule and end-to-end times are the slowest rank's."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ps = [ctx.Process(target=_max_rank, args=(r, 2, 29632, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_max_over_ranks_single():
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_sources_hash_gates_traffic():
+    """The DRAM traffic figure in profiles/traffic.json is used only while the
+    device sources hash to the value recorded with it."""
+    import bench
+    h = bench.kernel_sources_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        tj = json.load(f)
+    assert {"workload", "kernel", "bytes_per_launch", "sources_sha256_16"} <= set(tj)
