@@ -261,6 +261,94 @@ def run_sweep(args):
           flush=True)
 
 
+def run_ablation(args):
+    """Per-edge ablation of programmatic dependent launch on the add + RMSNorm
+    (+quant) -> QKV projection edge (the layer's ops 0 and 1), after page
+    "Kernel-Mega-PDL" (the section on where the gain of PDL comes from): the
+    projection waits on the norm at kernel entry ("entry"), after its
+    prologue ("deepgemm") or after issuing its first weight stages
+    ("prefetch", the schedules' own placement), each without and with
+    programmatic launch.  The figure is the span from the norm's start to the
+    projection's end: a CUDA graph of the two launches, timed with events,
+    L2 flushed before every replay.  For the headline layer it also gives the
+    incremental-subgraph table: the layer's graph grown op by op, what each op
+    adds to the span against its time alone.  One line per cell on stderr,
+    one JSON summary line on stdout."""
+    import torch
+
+    import pdl_persistent_megakernel_gb300 as dl
+    from pdl_persistent_megakernel_gb300 import synth
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    reps = max(10, args.steps)
+
+    def graph_of(plan, first, count, pdl, mode):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            plan.launch_ops(first, count, pdl, mode, stream)
+        return g
+
+    def span_us(g):
+        ts = []
+        with torch.cuda.stream(stream):
+            for it in range(reps + args.warmup):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                torch.cuda.synchronize(device)
+                if it >= args.warmup:
+                    ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    cells = [synth.CONFIGS["q8_layer_m16_ctx8192_fp8"], synth.sweep_config(32, 8192, True),
+             synth.sweep_config(64, 8192, True)]
+    names = {2: "entry", 1: "deepgemm", 0: "prefetch"}
+    out_cells, incremental = [], []
+    for cfg in cells:
+        w = synth.make_weights(cfg, device=device)
+        inp = synth.make_inputs(cfg, device=device)
+        plan = dl.Plan(cfg, w, modes_mask=1 << dl.MODE_SERIAL)
+        out = torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            plan.step(inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"],
+                      inp["positions"], out, dl.MODE_SERIAL, stream)
+        torch.cuda.synchronize(device)
+        spans = {}
+        for mode in (2, 1, 0):
+            for pdl in (False, True):
+                spans[f"{names[mode]}_{'on' if pdl else 'off'}"] = round(
+                    span_us(graph_of(plan, 0, 2, pdl, mode)), 2)
+        cell = {"config": cfg.name, "M": cfg.M, "span_us": spans,
+                "pdl_gain_us": {n: round(spans[f"{n}_off"] - spans[f"{n}_on"], 2)
+                                for n in names.values()},
+                "prologue_before_wait_us": round(spans["entry_on"] - spans["deepgemm_on"], 2),
+                "weights_before_wait_us": round(spans["deepgemm_on"] - spans["prefetch_on"], 2)}
+        out_cells.append(cell)
+        print(json.dumps(cell), file=sys.stderr, flush=True)
+        if cfg.name == "q8_layer_m16_ctx8192_fp8":
+            prev = 0.0
+            for k in range(1, len(plan.ops()) + 1):
+                tk = span_us(graph_of(plan, 0, k, True, 0))
+                alone = span_us(graph_of(plan, k - 1, 1, False, 0))
+                incremental.append({"op": plan.ops()[k - 1][0], "prefix_us": round(tk, 2),
+                                    "added_us": round(tk - prev, 2), "alone_us": round(alone, 2)})
+                prev = tk
+            print(json.dumps({"incremental": incremental}), file=sys.stderr, flush=True)
+        plan.status()
+        plan.close()
+        del w, inp, out
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "programmatic-launch ablation: norm -> QKV edge span (us)",
+                      "cells": out_cells, "incremental": incremental, "steps": reps,
+                      "warmup": args.warmup, "l2": "256 MiB write before every replay",
+                      "data": "synthetic"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -272,6 +360,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--per-kernel", action="store_true", default=True)
+    ap.add_argument("--ablation", action="store_true",
+                    help="per-edge programmatic-launch ablation and incremental-subgraph table")
     ap.add_argument("--sweep", action="store_true",
                     help="time the crossover sweep (batch x context x dtype) instead")
     ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
@@ -284,6 +374,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.ablation:
+        run_ablation(args)
         return
 
     import torch

@@ -195,6 +195,21 @@ dl_status dl_plan_op_info(dl_plan* plan, int i, char* name, size_t name_len,
                           int* grid, int* smem_bytes);
 dl_status dl_plan_launch_op(dl_plan* plan, int i, void* stream);
 
+/* The serial schedule's operations [first, first + count) launched in order
+ * on `stream`, with programmatic stream serialization on every launch when
+ * `pdl` != 0, and every projection waiting on its producer where `gdc_mode`
+ * says: 0 after issuing its first weight stages (the schedules' own
+ * placement), 1 after its prologue (barriers, TMEM, descriptors) but before
+ * any load, 2 at kernel entry.  A measurement hook for the per-edge ablation
+ * of programmatic dependent launch (page "Kernel-Mega-PDL", the section on
+ * where the gain of PDL comes from: its entry / deepgemm / prefetch
+ * consumers); captured in a
+ * CUDA graph it gives the producer-start to consumer-end span of an edge.
+ * Operands are those bound by the last dl_decode_step on this plan.
+ * DL_ERR_INVALID_ARG for a bad range or mode, or before any step. */
+dl_status dl_plan_launch_ops(dl_plan* plan, int first, int count, int pdl, int gdc_mode,
+                             void* stream);
+
 /* Megakernel queue statistics: workers, queue length, events. */
 dl_status dl_plan_mega_info(dl_plan* plan, int* workers, int* qlen,
                             int* events);

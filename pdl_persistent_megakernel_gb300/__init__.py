@@ -118,7 +118,7 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
            "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
-           "dl_plan_launch_op", "dl_attention_noalloc", "dl_plan_trace")
+           "dl_plan_launch_op", "dl_plan_launch_ops", "dl_attention_noalloc", "dl_plan_trace")
 
 
 def lib(path: Optional[str] = None):
@@ -157,6 +157,8 @@ def lib(path: Optional[str] = None):
         L.dl_plan_op_info.restype = i32
         L.dl_plan_launch_op.argtypes = [vp, i32, vp]
         L.dl_plan_launch_op.restype = i32
+        L.dl_plan_launch_ops.argtypes = [vp, i32, i32, i32, i32, vp]
+        L.dl_plan_launch_ops.restype = i32
         L.dl_plan_trace.argtypes = [vp, vp, C.c_size_t, C.POINTER(i32), C.POINTER(i32)]
         L.dl_plan_trace.restype = i32
         L.dl_attention_noalloc.argtypes = [C.POINTER(Config), i32] + [vp] * 6 + [i32, vp]
@@ -306,6 +308,14 @@ class Plan:
 
     def launch_op(self, i: int, stream=None):
         _check(lib().dl_plan_launch_op(self._h, i, _stream_handle(stream)))
+
+    def launch_ops(self, first: int, count: int, pdl: bool, gdc_mode: int = 0, stream=None):
+        """Ops [first, first + count) of the serial list, with or without
+        programmatic dependent launch, projections waiting on their producer
+        per gdc_mode (0 after their first weight stages, 1 after their
+        prologue, 2 at entry): the per-edge ablation hook."""
+        _check(lib().dl_plan_launch_ops(self._h, first, count, int(bool(pdl)), gdc_mode,
+                                        _stream_handle(stream)))
 
     def perturb_wait(self, delta: int, budget_ns: int, validate: bool):
         return lib().dl_plan_debug_perturb_wait(self._h, delta, budget_ns, int(validate))

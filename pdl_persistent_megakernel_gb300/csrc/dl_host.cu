@@ -1155,6 +1155,20 @@ extern "C" dl_status dl_plan_launch_op(dl_plan* p, int i, void* stream) {
   return DL_OK;
 }
 
+extern "C" dl_status dl_plan_launch_ops(dl_plan* p, int first, int count, int pdl,
+                                        int gdc_mode, void* stream) {
+  if (!p || first < 0 || count < 1 || first + count > static_cast<int>(p->lin.size()))
+    return fail(DL_ERR_INVALID_ARG, "op range out of range");
+  if (gdc_mode < 0 || gdc_mode > 2) return fail(DL_ERR_INVALID_ARG, "gdc_mode must be 0, 1 or 2");
+  if (!p->have_last) return fail(DL_ERR_INVALID_ARG, "no operands bound yet");
+  for (int i = first; i < first + count; ++i) {
+    LaunchOp op = p->lin[i];
+    if (op.args.kind == OP_GEMM) op.args.gemm.gdc_mode = gdc_mode;
+    CK(launch_op(p, op, static_cast<cudaStream_t>(stream), pdl != 0, i));
+  }
+  return DL_OK;
+}
+
 extern "C" dl_status dl_plan_mega_info(dl_plan* p, int* workers, int* qlen, int* events) {
   if (!p || !p->d_queues) return fail(DL_ERR_INVALID_ARG, "no megakernel plan");
   if (workers) *workers = p->workers;

@@ -151,6 +151,11 @@ struct GemmArgs {
   int* best_idx;              // [NT][M]
   DPtr ids;                   // int32 [M]
   PrefetchSpec pf;
+  // Where a standalone projection waits on its producer (the per-edge
+  // programmatic-launch ablation): 0 after issuing its first weight stages
+  // (the default), 1 after its prologue but before any load, 2 at kernel
+  // entry, before its prologue.
+  int gdc_mode;
 };
 
 struct AttnArgs {

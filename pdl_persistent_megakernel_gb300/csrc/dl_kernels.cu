@@ -31,6 +31,7 @@ template <int kMG, int kMp>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm(GemmArgs a, KernelCtx ctx) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_slot;
+  if (a.gdc_mode == 2) gdc_wait();   // ablation: wait at entry, before the prologue
   uint8_t* smem = align1024(smem_raw);
   uint32_t tmem = 0;
   int cols = 0;

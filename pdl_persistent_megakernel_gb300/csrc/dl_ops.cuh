@@ -1203,13 +1203,16 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       }
     };
     auto units_in = [&](int j) { return min(ups, nunits - j * ups); };
-    const int pre = min(S, nslots);
-    // weights of the first stages do not depend on the previous op
+    // weights of the first stages do not depend on the previous op: they go
+    // out before the dependency wait (the ablation variants wait first)
+    bool ok = true;
+    if (a.gdc_mode != 0) ok = single_wait(dep, ctx, 10);
+    const int pre = ok ? min(S, nslots) : 0;
     for (int j = 0; j < pre; ++j) {
       mbar_arrive_expect_tx(&sh.full[j], ub * units_in(j));
       load_w(j, j);
     }
-    bool ok = single_wait(dep, ctx, 10);
+    if (a.gdc_mode == 0) ok = single_wait(dep, ctx, 10);
     // activations of the prefetched stages (issued even after a failed wait
     // so that every armed stage completes and can be drained)
     for (int j = 0; j < pre; ++j) load_x(j, j);
