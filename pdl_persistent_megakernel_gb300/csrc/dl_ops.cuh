@@ -273,7 +273,7 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   L.sx_off = L.tile_off + gemm_ntout(npair, Mp) * npair * Mp * 128 * 4;
   L.sw_off = L.sx_off + (fp8 ? KB * Mp * 4 : 0);
   L.epi_off = ((L.sw_off + (fp8 ? 2 * share * 4 : 0)) + 15) & ~15;   // sw [2][share]
-  L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) : 0);
+  L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) + 256 * 4 + 16 : 0);
   L.bar_off = (L.bar_off + 15) & ~15;
   L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 4) * 8;
   // two control areas (flags + contributor list): the fix-up warps' and the
@@ -290,6 +290,8 @@ struct GemmShared {
   int* tok_pos;   // [M] positions (QKV epilogue)
   int* tok_row;   // [M] cache row of (layer, page, K, head 0, slot) (QKV epilogue)
   float2* rope;   // [M][64] (cos, sin) at each token's position (QKV epilogue)
+  float* qkw;     // [2][128] q and k head-norm weights (QKV epilogue)
+  uint16_t** kvp; // the paged cache, resolved from the binding (QKV epilogue)
   uint64_t* full;
   uint64_t* empty;
   uint64_t* tfull;
@@ -384,9 +386,12 @@ __device__ void epi_store_bf16(const GemmArgs& a, int tg, const float* tout,
   }
 }
 
-// Per-token operands of the QKV epilogue, loaded once per CTA: positions,
-// the cache row of each token's slot, and the (cos, sin) rows at each
-// position.  Out-of-range positions or pages are reported and skipped.
+// Operands of the QKV epilogue, loaded once per CTA before the dependency
+// wait (none is an earlier operation's output): positions, the cache row of
+// each token's slot, the (cos, sin) rows at each position, the q / k
+// head-norm weights and the cache pointer.  Under load one dependent global
+// read costs about a microsecond, so the epilogue itself reads shared memory
+// only.  Out-of-range positions or pages are reported and skipped.
 __device__ void qkv_epi_prepare(const GemmArgs& a, int nthr, int ct, int bar,
                                 const KernelCtx& ctx, const GemmShared& sh) {
   const Binding* bd = ctx.binding;
@@ -409,6 +414,11 @@ __device__ void qkv_epi_prepare(const GemmArgs& a, int nthr, int ct, int bar,
     sh.tok_pos[m] = p;
     sh.tok_row[m] = row;
   }
+  for (int e = ct; e < 256; e += nthr) {
+    const uint16_t* w = static_cast<const uint16_t*>(e < 128 ? a.q_norm_w : a.k_norm_w);
+    sh.qkw[e] = __uint_as_float(static_cast<uint32_t>(w[e & 127]) << 16);
+  }
+  if (ct == 0) *sh.kvp = resolve<uint16_t>(a.kv, bd);
   named_bar(bar, nthr);
   const float2* cs = reinterpret_cast<const float2*>(a.rope_cs);
   for (int e = ct; e < a.M * 64; e += nthr)
@@ -422,15 +432,14 @@ __device__ void epi_qkv_rope(const GemmArgs& a, int tg, const float* tout,
                              int nthr, int ct, const KernelCtx& ctx,
                              const GemmShared& sh) {
   const int lane = ct & 31, wi = ct >> 5, nw = nthr >> 5;
-  uint16_t* kv = resolve<uint16_t>(a.kv, ctx.binding);
+  uint16_t* kv = *sh.kvp;
   const int hh = tg;
   const bool is_q = hh < a.Hq;
   const bool is_k = !is_q && hh < a.Hq + a.Hkv;
   float wn[4] = {1.f, 1.f, 1.f, 1.f};
   if (is_q || is_k) {
-    const uint16_t* nw_ = static_cast<const uint16_t*>(is_q ? a.q_norm_w : a.k_norm_w);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) wn[k] = __uint_as_float(static_cast<uint32_t>(nw_[lane + 32 * k]) << 16);
+    for (int k = 0; k < 4; ++k) wn[k] = sh.qkw[(is_q ? 0 : 128) + lane + 32 * k];
   }
   for (int m = wi; m < a.M; m += nw) {
     float v[4];
@@ -1120,6 +1129,8 @@ __device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* sm
   sh.tok_pos = reinterpret_cast<int*>(smem + L.epi_off);
   sh.tok_row = sh.tok_pos + a.M;
   sh.rope = reinterpret_cast<float2*>(smem + L.epi_off + a.M * 8);
+  sh.qkw = reinterpret_cast<float*>(smem + L.epi_off + a.M * (8 + 512));
+  sh.kvp = reinterpret_cast<uint16_t**>(smem + L.epi_off + a.M * (8 + 512) + 256 * 4);
   sh.full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   sh.empty = sh.full + kMaxStages;
   sh.tfull = sh.empty + kMaxStages;
