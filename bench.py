@@ -149,18 +149,34 @@ def to_dev(w, device):
             "lm_head_w": None if w.get("lm_head_w") is None else w["lm_head_w"].to(device)}
 
 
-def time_cpu_oracle(cfg, w, inp, min_seconds: float, max_reps: int):
-    """The oracle as it stands on the host cores; returns (s/step, reps, threads)."""
+def time_cpu_oracle(cfg, w, inp, min_seconds: float, max_reps: int, threads: int = 0):
+    """The oracle as it stands on the host cores (all of them, or `threads`);
+    returns (s/step, reps, threads used)."""
     import oracle
-    n = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.decode_step(cfg, w, inp)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= min_seconds or n >= max_reps:
-            break
-    return el / n, n, oracle.num_threads()
+    full = oracle.num_threads()
+    if threads > 0:
+        oracle.set_num_threads(threads)
+    try:
+        used = oracle.num_threads()
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle.decode_step(cfg, w, inp)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or n >= max_reps:
+                break
+    finally:
+        if threads > 0:
+            oracle.set_num_threads(full)
+    return el / n, n, used
+
+
+def single_thread_baseline(cfg, w, inp, byts: float) -> dict:
+    """The same oracle on one host thread, one step (a bounded sample)."""
+    sec, reps, used = time_cpu_oracle(cfg, w, inp, 0.0, 1, threads=1)
+    return {"value": byts / sec / 1e9, "unit": "GB/s", "cores": used,
+            "sample": f"{reps} full {cfg.name} step, {sec * 1e3:.0f} ms"}
 
 
 def run_reference(args, ws, rank):
@@ -187,7 +203,8 @@ def run_reference(args, ws, rank):
         "config": {"workload": cfg.name, "layers": cfg.n_layers, "M": cfg.M,
                    "context": cfg.context, "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16"},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"one full {cfg.name} step per timed step"},
+                         "sample": f"one full {cfg.name} step per timed step",
+                         "single_thread": single_thread_baseline(cfg, w, inp, byts)},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -523,7 +540,8 @@ def main():
         sec, reps, threads = time_cpu_oracle(cfg, w, inp, args.cpu_seconds, 50)
         cpu = {"value": algo / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{reps} full {cfg.name} step(s) of the fp64 C oracle, "
-                         f"{sec * 1e3:.0f} ms each"}
+                         f"{sec * 1e3:.0f} ms each",
+               "single_thread": single_thread_baseline(cfg, w, inp, algo)}
 
     if rank == 0:
         r = results[best]

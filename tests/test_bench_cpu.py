@@ -31,6 +31,9 @@ def test_reference_arm_line():
     assert d["config"]["workload"] == "q06_layer_b1_ctx1024"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    # the same oracle on one thread, reported beside the all-cores figure
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["unit"] == "GB/s" and st["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert abs(d["ms_per_step"] * 1e-3 * d["value"] * 1e9 - _algo_bytes("q06_layer_b1_ctx1024")) \
         < 1e-6 * _algo_bytes("q06_layer_b1_ctx1024")
