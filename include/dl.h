@@ -289,6 +289,22 @@ dl_status dl_test_kv_gather(const void* kv_pages, const int32_t* block_table,
                             int n_kv_heads, int head_dim, int page_size,
                             int num_pages, int max_pages, void* stream);
 
+/* Megakernel queue validator (page "Kernel-Mega-PDL", section 4: a wait
+ * may name only an event of an earlier instruction in the global order, so
+ * the persistent grid cannot deadlock), on a host description:
+ *   queues: host array [workers][qlen] of 128-byte instructions, each 32
+ *     uint32: op_row (0xffffffff = NoOp), cta, n_wait (<= 4), n_signal
+ *     (<= 2), wait_event[4], wait_value[4], signal_event[2],
+ *     signal_inc[2], 16 unused words.
+ * DL_OK when every queue lists its ops in increasing op_row, ends with at
+ * least one NoOp and has nothing after it, and every wait names an event
+ * e < its own op_row whose total signal increments over all queues reach
+ * the awaited value; otherwise DL_ERR_PLAN_INVALID with a message
+ * (dl_last_error).  DL_ERR_INVALID_ARG for a NULL or empty description.
+ * Pure host code: no device is touched. */
+dl_status dl_test_validate_mega_queues(const void* queues, int workers, int qlen,
+                                       int n_events);
+
 #ifdef __cplusplus
 }
 #endif

@@ -118,7 +118,8 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_plan_debug_buffer", "dl_plan_kernel_count", "dl_plan_mega_info",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
            "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
-           "dl_plan_launch_op", "dl_plan_launch_ops", "dl_attention_noalloc", "dl_plan_trace")
+           "dl_plan_launch_op", "dl_plan_launch_ops", "dl_attention_noalloc", "dl_plan_trace",
+           "dl_test_validate_mega_queues")
 
 
 def lib(path: Optional[str] = None):
@@ -167,6 +168,8 @@ def lib(path: Optional[str] = None):
         L.dl_test_kv_write.restype = i32
         L.dl_test_kv_gather.argtypes = [vp] * 3 + [i32] * 8 + [vp]
         L.dl_test_kv_gather.restype = i32
+        L.dl_test_validate_mega_queues.argtypes = [vp, i32, i32, i32]
+        L.dl_test_validate_mega_queues.restype = i32
         if path is None:
             _lib = L
         return L

@@ -508,23 +508,27 @@ static dl_status build_mega(dl_plan* p) {
 }
 
 // Host validator: every wait names an event of an earlier op whose total
-// signals reach the threshold, queues are in global op order, and the grid
-// fits co-resident.  Returns DL_ERR_PLAN_INVALID with a message otherwise.
-static dl_status validate_mega(const dl_plan* p) {
-  std::vector<unsigned long long> total(p->n_events, 0);
-  for (const Instr& in : p->queues) {
+// signals reach the threshold, and every queue is in global op order with
+// its NoOp terminator last.  Returns DL_ERR_PLAN_INVALID with a message
+// otherwise.
+static dl_status validate_queues(const Instr* queues, int workers, int qlen, int n_events) {
+  std::vector<unsigned long long> total(static_cast<size_t>(n_events), 0);
+  const size_t n = static_cast<size_t>(workers) * qlen;
+  for (size_t i = 0; i < n; ++i) {
+    const Instr& in = queues[i];
     if (in.op_row == 0xffffffffu) continue;
+    if (in.n_signal > 2) return fail(DL_ERR_PLAN_INVALID, "too many waits/signals");
     for (uint32_t s = 0; s < in.n_signal; ++s) {
-      if (in.signal_event[s] >= static_cast<uint32_t>(p->n_events))
+      if (in.signal_event[s] >= static_cast<uint32_t>(n_events))
         return fail(DL_ERR_PLAN_INVALID, "signal of an unknown event");
       total[in.signal_event[s]] += in.signal_inc[s];
     }
   }
-  for (int w = 0; w < p->workers; ++w) {
+  for (int w = 0; w < workers; ++w) {
     long long prev = -1;
     bool ended = false;
-    for (int i = 0; i < p->qlen; ++i) {
-      const Instr& in = p->queues[static_cast<size_t>(w) * p->qlen + i];
+    for (int i = 0; i < qlen; ++i) {
+      const Instr& in = queues[static_cast<size_t>(w) * qlen + i];
       if (in.op_row == 0xffffffffu) {
         ended = true;
         continue;
@@ -538,12 +542,17 @@ static dl_status validate_mega(const dl_plan* p) {
         const uint32_t e = in.wait_event[k];
         if (e >= in.op_row)
           return fail(DL_ERR_PLAN_INVALID, "wait on an event of a later op (deadlock)");
-        if (in.wait_value[k] > total[e])
+        if (e >= static_cast<uint32_t>(n_events) || in.wait_value[k] > total[e])
           return fail(DL_ERR_PLAN_INVALID, "wait threshold above the event's total signals");
       }
     }
+    if (!ended) return fail(DL_ERR_PLAN_INVALID, "queue without its NoOp terminator");
   }
   return DL_OK;
+}
+
+static dl_status validate_mega(const dl_plan* p) {
+  return validate_queues(p->queues.data(), p->workers, p->qlen, p->n_events);
 }
 
 static dl_status upload_mega(dl_plan* p) {
@@ -1175,6 +1184,15 @@ extern "C" dl_status dl_plan_mega_info(dl_plan* p, int* workers, int* qlen, int*
   if (qlen) *qlen = p->qlen;
   if (events) *events = p->n_events;
   return DL_OK;
+}
+
+// Test-only: the megakernel queue validator on a host array of
+// instructions (the layout of include/dl.h's dl_test_validate_mega_queues).
+extern "C" dl_status dl_test_validate_mega_queues(const void* queues, int workers, int qlen,
+                                                  int n_events) {
+  if (!queues || workers <= 0 || qlen <= 0 || n_events <= 0)
+    return fail(DL_ERR_INVALID_ARG, "empty queue description");
+  return validate_queues(static_cast<const Instr*>(queues), workers, qlen, n_events);
 }
 
 extern "C" dl_status dl_plan_debug_perturb_wait(dl_plan* p, unsigned delta,
