@@ -278,6 +278,86 @@ def run_sweep(args):
           flush=True)
 
 
+def trace_timeline(tr, ops):
+    """Per-op timeline of one traced step.  tr: the trace table [ops][ctas][8]
+    of a DL_TRACE=1 plan (per CTA share, %globaltimer ns at its start,
+    dependency release, first and last consumed unit, exit, then its work
+    units and the end of its last fix-up or combine); ops: the plan's (name,
+    grid, smem) list.  Times in us from the earliest share start; a slot that
+    no share stamped (a norm has no unit loop) is None."""
+    import numpy as np
+    tr = np.asarray(tr).astype(np.int64)
+    starts = [tr[k, :g, 0] for k, (_, g, _) in enumerate(ops)]
+    t0 = min(int(x[x > 0].min()) for x in starts if (x > 0).any())
+    rows = []
+    for k, (name, grid, _) in enumerate(ops):
+        t = tr[k, :grid]
+
+        def stat(slot, fn):
+            v = t[:, slot]
+            v = v[v > 0]
+            return None if v.size == 0 else round((float(fn(v)) - t0) / 1e3, 2)
+
+        units = t[:, 5]
+        busy = (units > 0) & (t[:, 2] > 0) & (t[:, 3] > 0)
+        per_unit = None
+        if busy.any():
+            per = (t[busy, 3] - t[busy, 2]) / np.maximum(units[busy] - 1, 1)
+            per_unit = round(float(np.median(per)) / 1e3, 3)
+        rows.append({"op": name, "grid": int(grid),
+                     "start_min": stat(0, np.min), "start_max": stat(0, np.max),
+                     "deps_med": stat(1, np.median), "first_med": stat(2, np.median),
+                     "loop_end_med": stat(3, np.median), "loop_end_max": stat(3, np.max),
+                     "reduce_max": stat(6, np.max),
+                     "end_med": stat(4, np.median), "end_max": stat(4, np.max),
+                     "units": int(units.sum()), "us_per_unit_med": per_unit})
+    return {"span_us": max(r["end_max"] for r in rows if r["end_max"] is not None),
+            "ops": rows}
+
+
+def run_trace(args):
+    """One traced step per schedule of --modes (a DL_TRACE=1 plan; L2 flushed
+    before it, after warm-up steps): the per-op timeline of trace_timeline as
+    one JSON line per schedule.  The stamps cost a few global stores per
+    share, so the span is close to, not equal to, the untraced step."""
+    import os
+    os.environ["DL_TRACE"] = "1"
+    import torch
+
+    import pdl_persistent_megakernel_gb300 as dl
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    cfg, w, inp = build_workload(args.config, device, False)
+    inp = {k: v.to(device) for k, v in inp.items()}
+    name_to_mode = {v: k for k, v in dl.MODE_NAMES.items()}
+    modes = [name_to_mode[m] for m in args.modes.split(",")]
+    mask = 0
+    for m in modes:
+        mask |= 1 << m
+    plan = dl.Plan(cfg, w, modes_mask=mask)
+    if cfg.vocab:
+        out = torch.zeros((cfg.M,), dtype=torch.int32, device=device)
+    else:
+        out = torch.zeros((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    args_ = (inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"], inp["positions"], out)
+    for mode in modes:
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            plan.step(*args_, mode=mode)
+        torch.cuda.synchronize(device)
+        plan.trace()                      # reading clears the table
+        flush.zero_()
+        torch.cuda.synchronize(device)
+        plan.step(*args_, mode=mode)
+        torch.cuda.synchronize(device)
+        plan.status()
+        line = {"trace": dl.MODE_NAMES[mode], "workload": cfg.name}
+        line.update(trace_timeline(plan.trace(), plan.ops()))
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def run_ablation(args):
     """Per-edge ablation of programmatic dependent launch on the add + RMSNorm
     (+quant) -> QKV projection edge (the layer's ops 0 and 1), after page
@@ -381,6 +461,8 @@ def main():
                     help="per-edge programmatic-launch ablation and incremental-subgraph table")
     ap.add_argument("--sweep", action="store_true",
                     help="time the crossover sweep (batch x context x dtype) instead")
+    ap.add_argument("--trace", action="store_true",
+                    help="one traced step per schedule of --modes: the per-op timeline")
     ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
                     help="flush: a 256 MiB write before every step; stream: steps back to "
                          "back (each step reads more bytes than the 129 MB L2 holds)")
@@ -394,6 +476,9 @@ def main():
         return
     if args.ablation:
         run_ablation(args)
+        return
+    if args.trace:
+        run_trace(args)
         return
 
     import torch

@@ -94,3 +94,29 @@ def test_sources_hash_gates_traffic():
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         tj = json.load(f)
     assert {"workload", "kernel", "bytes_per_launch", "sources_sha256_16"} <= set(tj)
+
+
+def test_trace_timeline_from_a_synthetic_table():
+    """bench.py --trace summarises a trace table: times from the earliest
+    share start, medians and maxima per slot, per-unit time of the loop, and
+    None for slots a share never stamps (a norm has no unit loop)."""
+    import numpy as np
+    import bench
+    ops = [("add_rmsnorm1", 2, 0), ("o_proj", 3, 0)]
+    tr = np.zeros((2, 4, 8), dtype=np.uint64)
+    base = 10_000_000
+    # norm shares: start, dependency release, exit, one unit each
+    tr[0, 0, [0, 1, 4, 5]] = [base, base + 500, base + 3000, 1]
+    tr[0, 1, [0, 1, 4, 5]] = [base + 100, base + 600, base + 3500, 1]
+    # projection shares: 5 units, first and last unit 4 us apart (1 us each)
+    for c in range(3):
+        s = base + 4000 + 100 * c
+        tr[1, c] = [s, s + 200, s + 1000, s + 5000, s + 7000, 5, s + 6000, 0]
+    tl = bench.trace_timeline(tr, ops)
+    norm, proj = tl["ops"]
+    assert norm["start_min"] == 0.0 and norm["end_max"] == 3.5
+    assert norm["first_med"] is None and norm["loop_end_max"] is None
+    assert norm["units"] == 2 and norm["us_per_unit_med"] is None
+    assert proj["start_min"] == 4.0 and proj["start_max"] == 4.2 and proj["deps_med"] == 4.3
+    assert proj["us_per_unit_med"] == 1.0 and proj["units"] == 15
+    assert proj["reduce_max"] == 10.2 and proj["end_max"] == 11.2 and tl["span_us"] == 11.2
