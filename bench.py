@@ -172,8 +172,13 @@ def time_cpu_oracle(cfg, w, inp, min_seconds: float, max_reps: int, threads: int
     return el / n, n, used
 
 
-def single_thread_baseline(cfg, w, inp, byts: float) -> dict:
-    """The same oracle on one host thread, one step (a bounded sample)."""
+def single_thread_baseline(cfg, w, inp, byts: float, sec_all: float = 0.0,
+                           threads_all: int = 1, limit_s: float = 30.0) -> dict:
+    """The same oracle on one host thread, one step: a bounded sample, skipped
+    when the all-cores time x threads says it would take over limit_s."""
+    if sec_all * threads_all > limit_s:
+        return {"value": None, "unit": "GB/s", "cores": 1,
+                "sample": f"skipped: one step estimated at {sec_all * threads_all:.0f} s"}
     sec, reps, used = time_cpu_oracle(cfg, w, inp, 0.0, 1, threads=1)
     return {"value": byts / sec / 1e9, "unit": "GB/s", "cores": used,
             "sample": f"{reps} full {cfg.name} step, {sec * 1e3:.0f} ms"}
@@ -204,7 +209,8 @@ def run_reference(args, ws, rank):
                    "context": cfg.context, "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16"},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"one full {cfg.name} step per timed step",
-                         "single_thread": single_thread_baseline(cfg, w, inp, byts)},
+                         "single_thread": single_thread_baseline(cfg, w, inp, byts, sec,
+                                                                 threads)},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -626,7 +632,7 @@ def main():
         cpu = {"value": algo / sec / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{reps} full {cfg.name} step(s) of the fp64 C oracle, "
                          f"{sec * 1e3:.0f} ms each",
-               "single_thread": single_thread_baseline(cfg, w, inp, algo)}
+               "single_thread": single_thread_baseline(cfg, w, inp, algo, sec, threads)}
 
     if rank == 0:
         r = results[best]

@@ -120,3 +120,11 @@ def test_trace_timeline_from_a_synthetic_table():
     assert proj["start_min"] == 4.0 and proj["start_max"] == 4.2 and proj["deps_med"] == 4.3
     assert proj["us_per_unit_med"] == 1.0 and proj["units"] == 15
     assert proj["reduce_max"] == 10.2 and proj["end_max"] == 11.2 and tl["span_us"] == 11.2
+
+
+def test_single_thread_sample_is_bounded():
+    """The one-thread oracle sample is skipped, with the estimate stated,
+    when the all-cores time x threads is over the limit."""
+    import bench
+    st = bench.single_thread_baseline(None, None, None, 1e9, sec_all=4.0, threads_all=16)
+    assert st["value"] is None and st["cores"] == 1 and "skipped" in st["sample"]
