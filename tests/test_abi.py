@@ -49,3 +49,32 @@ def test_plan_create_rejects_bad_config_without_gpu():
     with pytest.raises(dl.DLError) as e:
         dl.Plan(cfg, w)
     assert "head_dim" in str(e.value)
+
+
+def _cfg(**kw):
+    from pdl_persistent_megakernel_gb300 import synth
+    base = dict(hidden=256, inter=384, n_q_heads=4, n_kv_heads=2, head_dim=128, n_layers=1,
+                vocab=0, fp8=False, num_requests=1, tokens_per_request=1, context=100,
+                page_size=16)
+    base.update(kw)
+    return synth.DecodeConfig("bad", **base)
+
+
+@pytest.mark.parametrize("kw,plan_kw,msg", [
+    (dict(n_q_heads=6, n_kv_heads=4), {}, "n_q_heads % n_kv_heads"),
+    (dict(hidden=200), {}, "multiples of 128"),
+    (dict(hidden=16384), {}, "hidden > 8192"),
+    (dict(vocab=1000), {}, "vocab must be a multiple of 128"),
+    (dict(num_requests=65), {}, "more than 64 tokens"),
+    (dict(tokens_per_request=16, n_q_heads=32, n_kv_heads=2), {}, "group size > 64"),
+    (dict(page_size=48), {}, "page_size must divide 64"),
+    (dict(), dict(max_context=400), "max_context"),
+    (dict(fp8=True, vocab=128), {}, "layer plans"),
+], ids=["gqa", "hidden128", "hidden_max", "vocab128", "tokens", "qrows", "page", "pages",
+        "fp8_full"])
+def test_plan_create_rejects_each_config_rule_without_gpu(kw, plan_kw, msg):
+    """Every rule of the plan's config check, violated alone, is refused with
+    its own message before any CUDA call."""
+    with pytest.raises(dl.DLError) as e:
+        dl.Plan(_cfg(**kw), {"layers": [{}]}, **plan_kw)
+    assert msg in str(e.value)
