@@ -78,3 +78,42 @@ def test_plan_create_rejects_each_config_rule_without_gpu(kw, plan_kw, msg):
     with pytest.raises(dl.DLError) as e:
         dl.Plan(_cfg(**kw), {"layers": [{}]}, **plan_kw)
     assert msg in str(e.value)
+
+
+class _Addr:
+    """A stand-in tensor: only its address is read (the checks under test
+    run before any CUDA call, so nothing dereferences it)."""
+
+    def __init__(self, a):
+        self.a = a
+
+    def data_ptr(self):
+        return self.a
+
+
+@pytest.mark.parametrize("kw,call_kw,msg", [
+    (dict(head_dim=64), {}, "head_dim must be 128"),
+    (dict(n_q_heads=6, n_kv_heads=4), {}, "n_q_heads % n_kv_heads"),
+    (dict(), dict(layer=1), "layer out of range"),
+    (dict(num_requests=65), {}, "more than 64 tokens"),
+    (dict(tokens_per_request=16, n_q_heads=32, n_kv_heads=2), {}, "group size > 64"),
+    (dict(page_size=48), {}, "page_size must divide 64"),
+    (dict(), dict(max_context=400), "max_pages_per_request * page_size < max_context"),
+    (dict(num_requests=64, n_q_heads=65, n_kv_heads=65), {}, "4096"),
+    (dict(), dict(q=None), "NULL tensor pointer"),
+    (dict(fp8=True), {}, "NULL tensor pointer"),          # FP8 needs out_scale
+    (dict(), dict(q=_Addr(0x1008)), "misaligned"),
+], ids=["head_dim", "gqa", "layer", "tokens", "qrows", "page", "pages", "pairs", "null",
+        "fp8_scale", "align"])
+def test_attention_noalloc_rejects_each_rule_without_gpu(kw, call_kw, msg):
+    """Every host check of the allocation-free attention entry point,
+    violated alone, is refused with its own message before any CUDA call."""
+    args = dict(layer=0, q=_Addr(0x10000), kv_pages=_Addr(0x20000),
+                block_table=_Addr(0x30000), positions=_Addr(0x40000), out=_Addr(0x50000))
+    args.update(call_kw)
+    max_context = args.pop("max_context", None)
+    with pytest.raises(dl.DLError) as e:
+        dl.attention_noalloc(_cfg(**kw), args["layer"], args["q"], args["kv_pages"],
+                             args["block_table"], args["positions"], args["out"],
+                             max_context=max_context, check=False, stream=0)
+    assert msg in str(e.value)
