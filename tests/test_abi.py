@@ -117,3 +117,29 @@ def test_attention_noalloc_rejects_each_rule_without_gpu(kw, call_kw, msg):
                              args["block_table"], args["positions"], args["out"],
                              max_context=max_context, check=False, stream=0)
     assert msg in str(e.value)
+
+
+def test_null_plan_is_an_argument_error_everywhere():
+    """Every entry point that takes a plan refuses NULL without touching a
+    device: a dl_status of DL_ERR_INVALID_ARG, -1 for the counts, NULL for
+    the logits pointer, nothing for destroy."""
+    import ctypes as C
+    L = dl.lib()
+    INVALID = 1
+    z = None
+    assert L.dl_decode_step(z, z, z, z, z, z, z, 0, z) == INVALID
+    assert L.dl_decode_step_host(z, z, z, z, z, z, z, 0, z) == INVALID
+    assert L.dl_plan_status(z) == INVALID
+    p, n = C.c_void_p(), C.c_size_t()
+    assert L.dl_plan_debug_buffer(z, 0, C.byref(p), C.byref(n)) == INVALID
+    i = C.c_int()
+    assert L.dl_plan_mega_info(z, C.byref(i), C.byref(i), C.byref(i)) == INVALID
+    assert L.dl_plan_debug_perturb_wait(z, 0, 0, 1) == INVALID
+    buf = C.create_string_buffer(32)
+    assert L.dl_plan_op_info(z, 0, buf, 32, C.byref(i), C.byref(i)) == INVALID
+    assert L.dl_plan_launch_op(z, 0, z) == INVALID
+    assert L.dl_plan_launch_ops(z, 0, 1, 0, 0, z) == INVALID
+    assert L.dl_plan_trace(z, z, 0, C.byref(i), C.byref(i)) == INVALID
+    assert L.dl_plan_kernel_count(z, 0) == -1 and L.dl_plan_op_count(z) == -1
+    assert not L.dl_plan_logits(z)
+    L.dl_plan_destroy(z)
