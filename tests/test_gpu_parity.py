@@ -187,3 +187,24 @@ def test_full_size_intermediates(name):
     out, _ = c.run(plan, dl.MODE_SERIAL)
     _check_intermediates(c, plan, out)
     plan.close()
+
+
+def test_host_buffer_entry_matches_device_entry():
+    """dl_decode_step_host (pinned host buffers in, the result read back to a
+    pinned host buffer) gives the bytes of dl_decode_step on the same inputs
+    and the same starting cache."""
+    from gpu_harness import DEV
+    c = case("fp8_m16")
+    mode = dl.MODE_GRAPH_LINEAR_PDL
+    plan = c.plan(modes=1 << mode)
+    out_dev, kv_dev = c.run(plan, mode)
+    kv = c.inp["kv_pages"].to(DEV)
+    xh, rh = c.inp["x"].pin_memory(), c.inp["residual"].pin_memory()
+    bth, posh = c.inp["block_table"].pin_memory(), c.inp["positions"].pin_memory()
+    outh = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    plan.step_host(xh, rh, kv, bth, posh, outh, mode=mode)
+    torch.cuda.synchronize()
+    plan.status()
+    assert torch.equal(outh, out_dev.cpu())
+    assert torch.equal(kv.cpu(), kv_dev.cpu())
+    plan.close()
