@@ -1057,6 +1057,29 @@ extern "C" dl_status dl_decode_step_host(dl_plan* p, const void* x_host, const v
     return fail(DL_ERR_INVALID_ARG, "NULL host pointer");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t MH2 = static_cast<size_t>(p->M) * p->H * 2;
+  // Host buffers the device can address (page-locked and mapped: every
+  // page-locked allocation under unified addressing) are used in place: the
+  // first kernels read the inputs across the host link and the last ones
+  // write the result there, with no copy of its own on the stream (each
+  // copy costs a few microseconds of latency however small it is).  Any
+  // other buffer goes through the plan's staging copies.
+  auto device_view = [](const void* h) -> void* {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+      cudaGetLastError();   // not a CUDA-known pointer: clear the error
+      return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+    return (reinterpret_cast<uintptr_t>(at.devicePointer) & 15) == 0 ? at.devicePointer : nullptr;
+  };
+  void* dx = device_view(x_host);
+  void* dres = device_view(residual_host);
+  void* dbt = device_view(block_table_host);
+  void* dpos = device_view(positions_host);
+  void* dout = device_view(out_host);
+  if (dx && dres && dbt && dpos && dout)
+    return dl_decode_step(p, dx, dres, kv_pages, static_cast<const int32_t*>(dbt),
+                          static_cast<const int32_t*>(dpos), dout, mode, stream);
   CK(cudaMemcpyAsync(p->st_x, x_host, MH2, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(p->st_res, residual_host, MH2, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(p->st_bt, block_table_host,
