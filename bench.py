@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -85,7 +86,7 @@ class Clocks:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dl_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -317,8 +318,34 @@ def trace_timeline(tr, ops):
                      "reduce_max": stat(6, np.max),
                      "end_med": stat(4, np.median), "end_max": stat(4, np.max),
                      "units": int(units.sum()), "us_per_unit_med": per_unit})
-    return {"span_us": max(r["end_max"] for r in rows if r["end_max"] is not None),
-            "ops": rows}
+    span = max(r["end_max"] for r in rows if r["end_max"] is not None)
+    # time-weighted average of the CTA shares in flight (a share from its
+    # first stamp to its exit), and the bubbles: the time in which no share
+    # of any op is inside its unit loop (first to last unit consumed)
+    ev = []
+    for k, (name, grid, _) in enumerate(ops):
+        t = tr[k, :grid]
+        for c in range(grid):
+            a, b = int(t[c, 0]), int(t[c, 4])
+            if a > 0 and b >= a:
+                ev.append((a, 1))
+                ev.append((b, -1))
+    ev.sort()
+    area, cur, last = 0, 0, t0
+    for x, dv in ev:
+        area += cur * (x - last)
+        cur += dv
+        last = x
+    loops = sorted((r["first_med"], r["loop_end_max"]) for r in rows
+                   if r["first_med"] is not None and r["loop_end_max"] is not None)
+    covered, reach = 0.0, 0.0
+    for a, b in loops:
+        a = max(a, reach)
+        if b > a:
+            covered += b - a
+            reach = b
+    return {"span_us": span, "active_ctas_avg": round(area / 1e3 / span, 1) if span else None,
+            "bubble_us": round(span - covered, 2), "ops": rows}
 
 
 def run_trace(args):
@@ -362,6 +389,73 @@ def run_trace(args):
         line.update(trace_timeline(plan.trace(), plan.ops()))
         print(json.dumps(line), flush=True)
     plan.close()
+
+
+def run_micro(args):
+    """Microbenchmarks (one JSON line): ns per tcgen05.mma at the decode
+    step's shapes (M = 128, N 16..256, e4m3 and bf16, one or four TMEM
+    accumulators, one or two issuing threads); the release-add /
+    acquire-poll round trip between two CTAs; the empty megakernel (every
+    worker's queue one NoOp) on --config's plan; and the trace build's cost:
+    the graph_linear_pdl and megakernel steps with and without DL_TRACE=1."""
+    import os
+    import torch
+
+    import pdl_persistent_megakernel_gb300 as dl
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    mma = []
+    for fp8 in (True, False):
+        for n in (16, 64, 128, 256):
+            for lean in (False, True):
+                for iss in (1, 2):
+                    nacc = 2 if n <= 256 else 1
+                    ns = dl.bench_mma(fp8, n, 4096, nacc, iss, lean)
+                    mma.append({"dtype": "e4m3" if fp8 else "bf16", "n": n, "lean": lean,
+                                "accumulators": nacc, "issuers": iss, "ns_per_mma": round(ns, 1)})
+    poll_ns = dl.bench_poll_latency(20000)
+    cfg, w, inp = build_workload(args.config, device, False)
+    inp = {k: v.to(device) for k, v in inp.items()}
+    out = torch.zeros((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device) \
+        if not cfg.vocab else torch.zeros((cfg.M,), dtype=torch.int32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    args_ = (inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"], inp["positions"], out)
+    modes = (dl.MODE_GRAPH_LINEAR_PDL, dl.MODE_MEGAKERNEL)
+    mask = sum(1 << m for m in modes)
+
+    def time_modes(plan):
+        res = {}
+        for mode in modes:
+            for _ in range(max(3, args.warmup)):
+                plan.step(*args_, mode=mode)
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                plan.step(*args_, mode=mode)
+                b.record()
+                ts.append((a, b))
+            torch.cuda.synchronize(device)
+            plan.status()
+            if os.environ.get("DL_TRACE") == "1":
+                plan.trace()
+            res[dl.MODE_NAMES[mode]] = round(sum(a.elapsed_time(b) for a, b in ts) / len(ts) * 1e3, 2)
+        return res
+
+    os.environ.pop("DL_TRACE", None)
+    plan = dl.Plan(cfg, w, modes_mask=mask)
+    empty_us = plan.bench_empty_megakernel(100)
+    off = time_modes(plan)
+    plan.close()
+    os.environ["DL_TRACE"] = "1"
+    plan = dl.Plan(cfg, w, modes_mask=mask)
+    on = time_modes(plan)
+    plan.close()
+    os.environ.pop("DL_TRACE", None)
+    print(json.dumps({"micro": cfg.name, "mma": mma, "poll_round_trip_ns": round(poll_ns, 1),
+                      "empty_megakernel_us": round(empty_us, 3),
+                      "trace_off_us": off, "trace_on_us": on}), flush=True)
 
 
 def run_ablation(args):
@@ -469,6 +563,9 @@ def main():
                     help="time the crossover sweep (batch x context x dtype) instead")
     ap.add_argument("--trace", action="store_true",
                     help="one traced step per schedule of --modes: the per-op timeline")
+    ap.add_argument("--micro", action="store_true",
+                    help="microbenchmarks: tcgen05.mma cost, acquire-poll round trip, empty "
+                         "megakernel, trace build overhead")
     ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
                     help="flush: a 256 MiB write before every step; stream: steps back to "
                          "back (each step reads more bytes than the 129 MB L2 holds)")
@@ -485,6 +582,9 @@ def main():
         return
     if args.trace:
         run_trace(args)
+        return
+    if args.micro:
+        run_micro(args)
         return
 
     import torch
@@ -624,7 +724,9 @@ def main():
     d2h = outh.numel() * outh.element_size()
     e2e = {"value": ws * algo / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "us": e2e_ms * 1e3,
-           "schedule": best}
+           "schedule": best,
+           "host_buffers": "page-locked; the kernels read the inputs and write the ids or "
+                           "layer output across the host link in place"}
 
     cpu = None
     if need_cpu:
@@ -634,6 +736,8 @@ def main():
                          f"{sec * 1e3:.0f} ms each",
                "single_thread": single_thread_baseline(cfg, w, inp, algo, sec, threads)}
 
+    pdl_modes = [m for m in ("pdl_graph", "graph_linear_pdl") if m in results]
+    best_pdl = min(pdl_modes, key=lambda m: results[m]["us"]) if pdl_modes else None
     if rank == 0:
         r = results[best]
         sched = {m: {k: (round(v, 3) if isinstance(v, float) else v) for k, v in d.items()}
@@ -655,8 +759,12 @@ def main():
             "frac_of_8TBs": r["frac_of_8TBs"],
             "frac_of_measured_hbm": r["GBs"] / ws / peak,
             "schedules": sched,
-            "serial_pdl_mega_us": [round(results[m]["us"], 2) if m in results else None
-                                   for m in ("serial", "pdl_graph", "megakernel")],
+            # serial / the faster programmatic-launch graph / megakernel
+            "serial_pdl_mega_us": [round(results[m]["us"], 2) if m else None
+                                   for m in ("serial" if "serial" in results else None,
+                                             best_pdl, "megakernel" if "megakernel" in results
+                                             else None)],
+            "serial_pdl_mega_schedules": ["serial", best_pdl, "megakernel"],
             "roofline": roofline,
             "per_kernel_us": {k: round(v["us"], 2) for k, v in per_kernel.items()},
             "cpu_baseline": cpu,

@@ -139,9 +139,13 @@ dl_status dl_decode_step(dl_plan* plan, const void* x, const void* residual,
                          void* stream);
 
 /* End-to-end variant: x, residual, block_table, positions and out are HOST
- * buffers (pinned memory makes the copies asynchronous); the step copies
- * them to and from plan-owned device buffers on `stream`.  kv_pages is a
- * device pointer.  The result is in out_host once the stream is done. */
+ * buffers; kv_pages is a device pointer.  When all five host buffers are
+ * device-addressable page-locked memory (cudaHostAlloc / cudaHostRegister,
+ * mapped under unified addressing, 16-byte aligned) the kernels read the
+ * inputs and write the result across the host link in place, with no copy
+ * of their own; otherwise the step copies them to and from plan-owned
+ * device buffers on `stream` (asynchronous for page-locked buffers).  The
+ * result is in out_host once the stream is done. */
 dl_status dl_decode_step_host(dl_plan* plan, const void* x_host,
                               const void* residual_host, void* kv_pages,
                               const int32_t* block_table_host,
@@ -178,7 +182,8 @@ const float* dl_plan_logits(dl_plan* plan);
  *   3 q (bf16 [M,Hq,d])   4 attn (bf16/e4m3 [Mp, Hq d])       5 attn scales
  *   6 o2 (bf16 [M,H])     7 r2 (bf16 [M,H])                   8 h2
  *   9 h2 scales           10 act (bf16/e4m3 [Mp, I])          11 act scales
- *   12 y (bf16 [M,H])
+ *   12 y (bf16 [M,H])     16 final RMSNorm output, the lm_head input (bf16
+ *                          [M,H]; full-step plans only)
  * Returns DL_ERR_INVALID_ARG for an unknown index. */
 dl_status dl_plan_debug_buffer(dl_plan* plan, int which, void** ptr,
                                size_t* bytes);
@@ -227,15 +232,18 @@ void dl_plan_destroy(dl_plan* plan);
 
 /* ------------------------------------------- attention without allocation
  * The split-KV GQA attention of one layer (per (request, kv head) the keys
- * are split over CTAs, each partial keeps its row log-sum-exp, and the last
- * CTA to finish merges them), for callers that may not allocate device
- * memory where they call it: a framework that owns the device allocator and
- * forbids foreign allocations, or code running under a memory-pool budget
- * that is already spent.  The paper has no counterpart of this entry point;
- * it packages the plans' attention kernel.  It allocates nothing, neither
- * through CUDA nor through a library: its binding table, status word,
- * arrival counters and fp32 partials live in one statically reserved 8 MiB
- * device array, which every GPU that loads the library holds until exit.
+ * are split over CTAs, each partial keeps its rows' log-sum-exp, and once
+ * every partial of a pair is published each CTA of the pair combines a
+ * slice of its query rows), for callers that may not allocate device memory
+ * where they call it: a framework that owns the device allocator and forbids
+ * foreign allocations, or code running under a memory-pool budget that is
+ * already spent.  The paper has no counterpart of this entry point.  It
+ * launches the split-KV attention kernel of the mma.sync engine (the
+ * megakernel's attention engine) with the plans' work split and pipeline
+ * depth.  It allocates nothing, neither through CUDA nor through a library:
+ * its binding table, status word, arrival counters and fp32 partials live in
+ * one statically reserved 8 MiB device array, which every GPU that loads the
+ * library holds until exit.
  *
  *   cfg          only the attention fields are read: n_q_heads, n_kv_heads,
  *                head_dim (128), n_layers, weight_dtype (FP8 selects e4m3
@@ -245,17 +253,23 @@ void dl_plan_destroy(dl_plan* plan);
  *   q            bf16 [M, n_q_heads, head_dim], after QK-norm and RoPE.
  *   kv_pages, block_table, positions  as in dl_decode_step; the cache must
  *                already hold this step's K/V (it is only read here).
+ *                Every position must lie in [0, max_context).
  *   out          bf16 [M, n_q_heads head_dim]; with FP8, e4m3 codes of the
  *                same shape plus out_scale fp32 [M, n_q_heads head_dim / 128]
  *                (one scale per token per 128 values; NULL for bf16).
  *   check        0: asynchronous on `stream`; nonzero: also synchronise the
- *                stream and report device-side failures (DL_ERR_TIMEOUT,
- *                DL_ERR_DEVICE_BOUNDS).
- * Limits: the partials take G x 2 x QRp x 516 bytes of the 8 MiB, where G
- * is min(num_sms, key blocks) CTAs and QRp is tokens_per_request x group
- * size rounded up to 16, 32 or 64, and num_requests x n_kv_heads <= 4096.
- * Larger requests are rejected with DL_ERR_UNSUPPORTED and a message naming
- * the bytes needed (on a 152-SM GPU, QRp = 64 needs num_sms <= 126).  All
+ *                stream and report device-side failures (DL_ERR_TIMEOUT;
+ *                DL_ERR_DEVICE_BOUNDS for a position outside [0,
+ *                max_context) or a block-table entry outside [0,
+ *                num_pages), after which the output is unspecified).
+ * Limits: the partials take G x 2 x QRp x 516 bytes of the 8 MiB.  QRp is
+ * tokens_per_request x group size rounded up to 16, 32 or 64.  G is the
+ * plans' CTA count: with pairs = num_requests x n_kv_heads, blocks =
+ * ceil(max_context / 64) and S = num_sms (0: every SM), G = min(pairs x
+ * min(62, S / pairs), pairs x blocks) when pairs <= S, else min(S, pairs x
+ * blocks); it is at most S.  num_requests x n_kv_heads <= 4096.  Larger
+ * requests are rejected with DL_ERR_UNSUPPORTED and a message naming the
+ * bytes needed (on a 152-SM GPU, QRp = 64 needs num_sms <= 126).  All
  * tensor pointers are caller-owned.
  * Set-up: the first call on a device (made with that device current) looks
  * up the scratch's device address and sets the kernels' shared-memory
@@ -269,6 +283,39 @@ dl_status dl_attention_noalloc(const dl_config* cfg, int layer, const void* q,
                                const void* kv_pages, const int32_t* block_table,
                                const int32_t* positions, void* out,
                                float* out_scale, int check, void* stream);
+
+/* ------------------------------------------------------- measurement
+ * Microbenchmarks of the mechanisms the schedules rest on, each one small
+ * synchronous run on the current device (they allocate a few bytes of
+ * device memory, and return DL_ERR_TIMEOUT if a bounded device wait gave
+ * up).
+ *   dl_bench_mma: one CTA issues n_mma tcgen05.mma instructions (M = 128,
+ *     N = n in 16..256, a multiple of 16; fp8 != 0: kind::f8f6f4 e4m3 with
+ *     K = 32, else kind::f16 bf16 with K = 16) over zero operands in shared
+ *     memory, into n_accumulators TMEM accumulators (n_accumulators x n <=
+ *     512) in turn, from n_issuers (1 or 2) threads; *ns_per_mma = the span
+ *     from the first issue to the completion of the last, over n_mma (a
+ *     multiple of 4, <= 65536).  lean = 0: each MMA's descriptors and
+ *     accumulator are computed in the loop, as a straightforward issuer
+ *     does; lean != 0: descriptors built once and advanced by constants,
+ *     four MMAs per pass into one accumulator per issuer.  The cost of the
+ *     projections' and attention's tensor-core work at the decode step's
+ *     small N.
+ *   dl_bench_poll_latency: two co-resident CTAs pass a token back and forth
+ *     through one global counter, red.release.gpu.add on one side,
+ *     ld.acquire.gpu polling on the other (the megakernel's event protocol,
+ *     page "Kernel-Mega-PDL", section 4); *ns_per_round_trip over iters
+ *     (<= 2^20) round trips.
+ *   dl_plan_bench_empty_megakernel: the plan's megakernel launched iters
+ *     times on `stream` with every worker's queue a single NoOp: the cost
+ *     of the framework itself (page "Kernel-Mega-PDL", the megakernel's
+ *     empty-framework run); *us_per_launch from CUDA events.  Needs a plan
+ *     built with the megakernel mode; synchronises the stream. */
+dl_status dl_bench_mma(int fp8, int n, int n_mma, int n_accumulators, int n_issuers,
+                       int lean, double* ns_per_mma);
+dl_status dl_bench_poll_latency(int iters, double* ns_per_round_trip);
+dl_status dl_plan_bench_empty_megakernel(dl_plan* plan, int iters, double* us_per_launch,
+                                         void* stream);
 
 /* ------------------------------------------------------ test-only exports
  * Bit-exact paged-KV indexing (the slot math of the QKV epilogue and the

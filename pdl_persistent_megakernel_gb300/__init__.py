@@ -20,7 +20,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libdl.so")
-_SOURCES = ["dl_kernels.cu", "dl_host.cu", "dl_noalloc.cu"]
+_SOURCES = ["dl_kernels.cu", "dl_host.cu", "dl_noalloc.cu", "dl_bench.cu"]
 _HEADERS = ["dl_internal.h", "dl_device.cuh", "dl_ops.cuh", "dl_kernels.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -32,7 +32,7 @@ ALL_MODES = (1 << 6) - 1
 
 DEBUG_BUFFERS = {"r1": 0, "h1": 1, "h1_scales": 2, "q_rot": 3, "attn": 4,
                  "attn_scales": 5, "o2": 6, "r2": 7, "h2": 8, "h2_scales": 9,
-                 "act": 10, "act_scales": 11, "y": 12}
+                 "act": 10, "act_scales": 11, "y": 12, "h_final": 16}
 
 
 def _nvcc() -> str:
@@ -119,7 +119,8 @@ EXPORTS = ("dl_plan_create", "dl_last_error", "dl_decode_step",
            "dl_plan_debug_perturb_wait", "dl_plan_destroy", "dl_test_kv_write",
            "dl_test_kv_gather", "dl_plan_op_count", "dl_plan_op_info",
            "dl_plan_launch_op", "dl_plan_launch_ops", "dl_attention_noalloc", "dl_plan_trace",
-           "dl_test_validate_mega_queues")
+           "dl_test_validate_mega_queues", "dl_bench_mma", "dl_bench_poll_latency",
+           "dl_plan_bench_empty_megakernel")
 
 
 def lib(path: Optional[str] = None):
@@ -170,6 +171,12 @@ def lib(path: Optional[str] = None):
         L.dl_test_kv_gather.restype = i32
         L.dl_test_validate_mega_queues.argtypes = [vp, i32, i32, i32]
         L.dl_test_validate_mega_queues.restype = i32
+        L.dl_bench_mma.argtypes = [i32, i32, i32, i32, i32, i32, C.POINTER(C.c_double)]
+        L.dl_bench_mma.restype = i32
+        L.dl_bench_poll_latency.argtypes = [i32, C.POINTER(C.c_double)]
+        L.dl_bench_poll_latency.restype = i32
+        L.dl_plan_bench_empty_megakernel.argtypes = [vp, i32, C.POINTER(C.c_double), vp]
+        L.dl_plan_bench_empty_megakernel.restype = i32
         if path is None:
             _lib = L
         return L
@@ -217,6 +224,25 @@ def attention_noalloc(cfg, layer: int, q, kv_pages, block_table, positions, out,
     _check(lib().dl_attention_noalloc(C.byref(c), layer, _ptr(q), _ptr(kv_pages),
                                       _ptr(block_table), _ptr(positions), _ptr(out),
                                       _ptr(out_scale), int(check), _stream_handle(stream)))
+
+
+def bench_mma(fp8: bool, n: int, n_mma: int, n_accumulators: int = 1,
+              n_issuers: int = 1, lean: bool = False) -> float:
+    """ns per tcgen05.mma (M = 128, N = n; bf16 K = 16 or e4m3 K = 32) over
+    n_mma instructions into n_accumulators TMEM accumulators from n_issuers
+    threads; lean: descriptors precomputed (dl_bench_mma)."""
+    v = C.c_double()
+    _check(lib().dl_bench_mma(int(bool(fp8)), n, n_mma, n_accumulators, n_issuers,
+                              int(bool(lean)), C.byref(v)))
+    return v.value
+
+
+def bench_poll_latency(iters: int = 10000) -> float:
+    """ns per release-add / acquire-poll round trip between two CTAs
+    (dl_bench_poll_latency)."""
+    v = C.c_double()
+    _check(lib().dl_bench_poll_latency(iters, C.byref(v)))
+    return v.value
 
 
 class Plan:
@@ -319,6 +345,13 @@ class Plan:
         prologue, 2 at entry): the per-edge ablation hook."""
         _check(lib().dl_plan_launch_ops(self._h, first, count, int(bool(pdl)), gdc_mode,
                                         _stream_handle(stream)))
+
+    def bench_empty_megakernel(self, iters: int = 50, stream=None) -> float:
+        """µs per launch of the megakernel with all-NoOp queues."""
+        v = C.c_double()
+        _check(lib().dl_plan_bench_empty_megakernel(self._h, iters, C.byref(v),
+                                                     _stream_handle(stream)))
+        return v.value
 
     def perturb_wait(self, delta: int, budget_ns: int, validate: bool):
         return lib().dl_plan_debug_perturb_wait(self._h, delta, budget_ns, int(validate))

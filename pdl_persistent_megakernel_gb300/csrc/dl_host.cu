@@ -113,6 +113,21 @@ struct dl_plan {
   bool fp8 = false, full = false, mma = false;
   int pf_units = 4;    // L2 prefetch units per share (DL_L2_PREFETCH_UNITS; 0: off)
   bool attn_tc = true; // standalone attention on tcgen05 (DL_ATTN=mma_sync: mma.sync)
+  // Most operand stages a projection / the tcgen05 attention keeps (in
+  // flight before its dependency, and in its ring): DL_GEMM_STAGES,
+  // DL_ATTN_STAGES.
+  int gemm_stages_max = 5, attn_stages_max = 6;
+  Instr* d_noop_queues = nullptr;   // [workers][1] NoOps (the empty megakernel)
+  // the DAG schedule's fork and join edges programmatic under PDL
+  // (DL_DAG_PROGRAMMATIC_EDGES=0: event edges, as in the non-PDL DAG)
+  bool dag_prog_edges = true;
+  // tcgen05 attention up to 32 query rows: one S-reading warp and four exp
+  // warps on the four SM sub-partitions (DL_ATTN_SPLIT_SOFTMAX=0: two
+  // alternating softmax warps of sub-partition 0)
+  bool split_sm = true;
+  // megakernel: attention shares wait on per-head QKV tile events
+  // (DL_MEGA_HEAD_EVENTS=0: on the whole projection)
+  bool head_events = true;
   unsigned long long budget_ns = 1000000000ull;
 
   std::vector<void*> allocs;
@@ -186,6 +201,7 @@ static void free_plan(dl_plan* p) {
     if (e) cudaGraphExecDestroy(e);
   if (p->cap) cudaStreamDestroy(p->cap);
   if (p->side) cudaStreamDestroy(p->side);
+  if (p->d_noop_queues) cudaFree(p->d_noop_queues);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->ev_join) cudaEventDestroy(p->ev_join);
   for (void* a : p->allocs) cudaFree(a);
@@ -280,7 +296,7 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   const int fixed_bytes = gemm_smem_bytes(npair, a.Mp, 0, a.KB, a.fp8, s.epi, a.M, a.share_max);
   // one CTA per SM; 3-4 stages of 32 KiB in flight per SM already reach the
   // HBM copy rate, a few more absorb jitter
-  a.stages = std::min(5, choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget));
+  a.stages = std::min(p->gemm_stages_max, choose_stages(stage_bytes, fixed_bytes, kGemmSmemTarget));
   a.tmem_bufs = a.mma ? std::min(4, 512 / (npair * a.Mp)) : 1;
   a.epi = s.epi;
   a.ws = p->ws_gemm[s.ws_slot];
@@ -302,6 +318,11 @@ int dl::attn_ctas(int pairs, int nb, int sms) {
   const long long U = static_cast<long long>(pairs) * nb;
   long long g = pairs <= sms ? static_cast<long long>(pairs) * std::min(62, sms / pairs) : sms;
   return static_cast<int>(std::max(1LL, std::min(g, U)));
+}
+
+// 4 stages of 32 KiB keep the mma.sync engine fed (more add nothing).
+int dl::attn_mma_stages(int QRp) {
+  return std::max(2, std::min(4, (kGemmSmemTarget - attn_smem_bytes(QRp, 0)) / (4 * kAttnKeys * 128)));
 }
 
 static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
@@ -328,14 +349,15 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.QR = p->T * (p->Hq / p->Hkv);
   a.QRp = a.QR <= 16 ? 16 : (a.QR <= 32 ? 32 : 64);
   a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
+  a.max_ctx = p->cfg.max_context;
+  a.split_sm = p->split_sm ? 1 : 0;
   a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms);
-  // stages of 32 KiB: 4 keep the mma.sync engine fed (more add nothing);
-  // the tcgen05 engine holds a block from its arrival to its PV commit
-  // (about 2.3 us), so it takes as many as fit (up to 6)
-  const int fixed = p->attn_tc ? attn_tc_smem_bytes(a.QRp, 0) : attn_smem_bytes(a.QRp, 0);
+  // stages of 32 KiB: the tcgen05 engine holds a block from its arrival to
+  // its PV commit, so it takes as many as fit (up to 6)
   a.stages = p->attn_tc
-      ? std::max(2, std::min(6, (kAttnTcSmemTarget - fixed) / (4 * kAttnKeys * 128)))
-      : std::max(2, std::min(4, (kGemmSmemTarget - fixed) / (4 * kAttnKeys * 128)));
+      ? std::max(2, std::min(p->attn_stages_max, (kAttnTcSmemTarget - attn_tc_smem_bytes(a.QRp, 0)) /
+                                    (4 * kAttnKeys * 128)))
+      : attn_mma_stages(a.QRp);
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->d)));
   a.ws = p->ws_attn;
   a.pair_cnt = cnt;
@@ -378,18 +400,29 @@ static dl_status check_config(const dl_config* c) {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // ------------------------------------------------- graph / launch helpers
+// prog_event: the launch also records a programmatic event, which fires
+// once every CTA of the kernel has passed griddepcontrol.launch_dependents
+// (not at block start): a launch on another stream that waits on it is the
+// kernel's programmatic dependent, as the next launch on the same stream is.
 static cudaError_t launch_op(const dl_plan* p, const LaunchOp& op, cudaStream_t s, bool pdl,
-                             int op_id) {
+                             int op_id, cudaEvent_t prog_event = nullptr) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(op.grid);
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = op.smem;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   lc.attrs = attr;
   lc.numAttrs = 1;
+  if (prog_event) {
+    attr[1].id = cudaLaunchAttributeProgrammaticEvent;
+    attr[1].val.programmaticEvent.event = prog_event;
+    attr[1].val.programmaticEvent.flags = 0;
+    attr[1].val.programmaticEvent.triggerAtBlockStart = 0;
+    lc.numAttrs = 2;
+  }
   KernelCtx ctx = make_ctx(p, op_id);
   switch (op.args.kind) {
     case OP_NORM: {
@@ -412,20 +445,36 @@ static cudaError_t launch_op(const dl_plan* p, const LaunchOp& op, cudaStream_t 
   }
 }
 
+// The DAG schedule's branch: op i with branch == 1 runs on the side stream,
+// forked after the main stream's previous op; the next op with branch == 2
+// joins it.  Under programmatic launch both edges are programmatic: the fork
+// op and the branch op record programmatic events (fired when all their
+// CTAs have passed launch_dependents), so the branch op's CTAs may start,
+// and the joining op's may run their prologue and weight / K/V prefetch,
+// before their producers finish; every kernel still waits for its
+// producers' completion (griddepcontrol.wait) before a dependent read.
+// Without it the edges are full event dependencies.
 static cudaError_t enqueue_list(dl_plan* p, const std::vector<LaunchOp>& ops, cudaStream_t s,
                                 bool pdl) {
+  const bool prog = pdl && p->dag_prog_edges;
   for (size_t i = 0; i < ops.size(); ++i) {
     const LaunchOp& op = ops[i];
+    const bool forks = i + 1 < ops.size() && ops[i + 1].branch == 1;
     if (op.branch == 1) {
       // side branch: forks from the main stream after the previous main op
-      cudaError_t e = cudaEventRecord(p->ev_fork, s);
-      if (e != cudaSuccess) return e;
+      cudaError_t e;
+      if (!prog) {
+        e = cudaEventRecord(p->ev_fork, s);
+        if (e != cudaSuccess) return e;
+      }
       e = cudaStreamWaitEvent(p->side, p->ev_fork, 0);
       if (e != cudaSuccess) return e;
-      e = launch_op(p, op, p->side, pdl, static_cast<int>(i));
+      e = launch_op(p, op, p->side, pdl, static_cast<int>(i), prog ? p->ev_join : nullptr);
       if (e != cudaSuccess) return e;
-      e = cudaEventRecord(p->ev_join, p->side);
-      if (e != cudaSuccess) return e;
+      if (!prog) {
+        e = cudaEventRecord(p->ev_join, p->side);
+        if (e != cudaSuccess) return e;
+      }
       continue;
     }
     if (op.branch == 2) {
@@ -433,7 +482,8 @@ static cudaError_t enqueue_list(dl_plan* p, const std::vector<LaunchOp>& ops, cu
       cudaError_t e = cudaStreamWaitEvent(s, p->ev_join, 0);
       if (e != cudaSuccess) return e;
     }
-    const cudaError_t e = launch_op(p, op, s, pdl, static_cast<int>(i));
+    const cudaError_t e =
+        launch_op(p, op, s, pdl, static_cast<int>(i), (prog && forks) ? p->ev_fork : nullptr);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -465,6 +515,18 @@ static dl_status capture_graph(dl_plan* p, int mode) {
 // topological order in which each depends on its predecessor, so the chain
 // of waits orders every true dependency (and every write-after-read reuse
 // of a buffer) of the list.
+// The device's Stream-K range arithmetic (32-bit, as in the kernels).
+static unsigned host_sk_begin(unsigned U, int G, int c) {
+  return (U * static_cast<unsigned>(c)) / static_cast<unsigned>(G);
+}
+static int host_sk_owner(unsigned U, int G, unsigned x) {
+  int c = static_cast<int>((x * static_cast<unsigned>(G)) / U);
+  if (c >= G) c = G - 1;
+  while (c > 0 && host_sk_begin(U, G, c) > x) --c;
+  while (c + 1 < G && host_sk_begin(U, G, c + 1) <= x) ++c;
+  return c;
+}
+
 static dl_status build_mega(dl_plan* p) {
   const std::vector<LaunchOp>& ops = p->lin;
   const int nops = static_cast<int>(ops.size());
@@ -489,6 +551,83 @@ static dl_status build_mega(dl_plan* p) {
       qs[c].push_back(in);
     }
   }
+  // Per-head events (the per-head events of page "Kernel-Mega-PDL",
+  // section 4, where a downstream task waits only on the heads it reads):
+  // an attention share waits for the QKV tiles of the kv heads of its
+  // (request, kv head) pairs -- the group's q heads, its k head and its v
+  // head -- instead of the whole projection.  A tile is finished (Stream-K
+  // fix-up and epilogue) by the share that owns its first unit, so that
+  // share's instruction adds 1 to the tile's head event when it ends.
+  int n_events = nops;
+  if (p->head_events) {
+    for (int k = 1; k < nops; ++k) {
+      const LaunchOp& at = ops[k];
+      const LaunchOp& qk = ops[k - 1];
+      if (at.args.kind != OP_ATTN || qk.args.kind != OP_GEMM ||
+          qk.args.gemm.epi != EPI_QKV_ROPE)
+        continue;
+      const GemmArgs& g = qk.args.gemm;
+      const AttnArgs& a = at.args.attn;
+      const int grp_size = a.Hq / a.Hkv;
+      if (g.t_base != 0 || g.NT != a.Hq + 2 * a.Hkv) continue;
+      const int ev0 = n_events;
+      n_events += a.Hkv;
+      const unsigned U = static_cast<unsigned>(g.NT) * static_cast<unsigned>(g.KB);
+      for (int t = 0; t < g.NT; ++t) {
+        const int h = t < a.Hq ? t / grp_size : (t < a.Hq + a.Hkv ? t - a.Hq : t - a.Hq - a.Hkv);
+        const int own = host_sk_owner(U, g.G, static_cast<unsigned>(t) * g.KB);
+        Instr* in = nullptr;
+        for (Instr& x : qs[own])
+          if (x.op_row == static_cast<uint32_t>(k - 1)) in = &x;
+        if (!in) return fail(DL_ERR_PLAN_INVALID, "tile owner without a QKV instruction");
+        bool merged = false;
+        for (uint32_t sgi = 0; sgi < in->n_signal; ++sgi)
+          if (instr_signal_event(*in, sgi) == static_cast<uint32_t>(ev0 + h)) {
+            (sgi < 2 ? in->signal_inc[sgi] : in->signal_inc_hi[sgi - 2]) += 1;
+            merged = true;
+          }
+        if (!merged) {
+          if (in->n_signal >= kMaxSignals)
+            return fail(DL_ERR_PLAN_INVALID, "a QKV share finishes tiles of too many heads");
+          const uint32_t sgi = in->n_signal++;
+          if (sgi < 2) {
+            in->signal_event[sgi] = static_cast<uint32_t>(ev0 + h);
+            in->signal_inc[sgi] = 1;
+          } else {
+            in->signal_event_hi[sgi - 2] = static_cast<uint32_t>(ev0 + h);
+            in->signal_inc_hi[sgi - 2] = 1;
+          }
+        }
+      }
+      // each attention share: the head events of its pairs (at most four
+      // distinct heads; otherwise it keeps the wait on the whole projection)
+      const unsigned Ua = static_cast<unsigned>(a.R * a.Hkv) * static_cast<unsigned>(a.NB);
+      for (int c = 0; c < at.grid; ++c) {
+        const unsigned u0 = host_sk_begin(Ua, a.G, c), u1 = host_sk_begin(Ua, a.G, c + 1);
+        if (u1 <= u0) continue;
+        int heads[4], nh = 0;
+        bool too_many = false;
+        for (unsigned pr = u0 / a.NB; pr <= (u1 - 1) / a.NB && !too_many; ++pr) {
+          const int h = static_cast<int>(pr % a.Hkv);
+          bool seen = false;
+          for (int i = 0; i < nh; ++i) seen |= heads[i] == h;
+          if (seen) continue;
+          if (nh == 4) too_many = true;
+          else heads[nh++] = h;
+        }
+        if (too_many) continue;
+        Instr* in = nullptr;
+        for (Instr& x : qs[c])
+          if (x.op_row == static_cast<uint32_t>(k)) in = &x;
+        if (!in) return fail(DL_ERR_PLAN_INVALID, "attention share without an instruction");
+        in->n_wait = static_cast<uint32_t>(nh);
+        for (int i = 0; i < nh; ++i) {
+          in->wait_event[i] = static_cast<uint32_t>(ev0 + heads[i]);
+          in->wait_value[i] = static_cast<uint32_t>(grp_size + 2);
+        }
+      }
+    }
+  }
   p->qlen = 0;
   for (auto& q : qs) p->qlen = std::max<int>(p->qlen, static_cast<int>(q.size()));
   p->qlen += 1;  // at least one NoOp terminator per queue
@@ -503,7 +642,7 @@ static dl_status build_mega(dl_plan* p) {
         dst.op_row = 0xffffffffu;
       }
     }
-  p->n_events = nops;
+  p->n_events = n_events;
   return DL_OK;
 }
 
@@ -512,16 +651,21 @@ static dl_status build_mega(dl_plan* p) {
 // its NoOp terminator last.  Returns DL_ERR_PLAN_INVALID with a message
 // otherwise.
 static dl_status validate_queues(const Instr* queues, int workers, int qlen, int n_events) {
+  // per event: the total of its signals and the latest op that signals it
   std::vector<unsigned long long> total(static_cast<size_t>(n_events), 0);
+  std::vector<long long> last_producer(static_cast<size_t>(n_events), -1);
   const size_t n = static_cast<size_t>(workers) * qlen;
   for (size_t i = 0; i < n; ++i) {
     const Instr& in = queues[i];
     if (in.op_row == 0xffffffffu) continue;
-    if (in.n_signal > 2) return fail(DL_ERR_PLAN_INVALID, "too many waits/signals");
+    if (in.n_wait > kMaxWaits || in.n_signal > kMaxSignals)
+      return fail(DL_ERR_PLAN_INVALID, "too many waits/signals");
     for (uint32_t s = 0; s < in.n_signal; ++s) {
-      if (in.signal_event[s] >= static_cast<uint32_t>(n_events))
+      const uint32_t e = instr_signal_event(in, s);
+      if (e >= static_cast<uint32_t>(n_events))
         return fail(DL_ERR_PLAN_INVALID, "signal of an unknown event");
-      total[in.signal_event[s]] += in.signal_inc[s];
+      total[e] += instr_signal_inc(in, s);
+      last_producer[e] = std::max<long long>(last_producer[e], in.op_row);
     }
   }
   for (int w = 0; w < workers; ++w) {
@@ -537,12 +681,15 @@ static dl_status validate_queues(const Instr* queues, int workers, int qlen, int
       if (static_cast<long long>(in.op_row) <= prev)
         return fail(DL_ERR_PLAN_INVALID, "queue not in global op order");
       prev = in.op_row;
-      if (in.n_wait > 4 || in.n_signal > 2) return fail(DL_ERR_PLAN_INVALID, "too many waits/signals");
       for (uint32_t k = 0; k < in.n_wait; ++k) {
         const uint32_t e = in.wait_event[k];
-        if (e >= in.op_row)
+        if (e >= static_cast<uint32_t>(n_events))
+          return fail(DL_ERR_PLAN_INVALID, "wait on an unknown event");
+        // every instruction that signals e must come earlier in the global
+        // order; then the earliest unfinished instruction can always run
+        if (last_producer[e] >= static_cast<long long>(in.op_row))
           return fail(DL_ERR_PLAN_INVALID, "wait on an event of a later op (deadlock)");
-        if (e >= static_cast<uint32_t>(n_events) || in.wait_value[k] > total[e])
+        if (in.wait_value[k] > total[e])
           return fail(DL_ERR_PLAN_INVALID, "wait threshold above the event's total signals");
       }
     }
@@ -588,6 +735,66 @@ static cudaError_t launch_mega(dl_plan* p, cudaStream_t s) {
   KernelCtx ctx = make_ctx(p, -1);
   void* args[] = {&m, &ctx};
   return cudaLaunchKernelExC(&lc, mega_kernel(), args);
+}
+
+// The megakernel with every worker's queue a single NoOp: the framework's
+// own cost (launch of the persistent grid, barrier and TMEM set-up, the
+// queue read, the counters' reset by the last worker, teardown).
+extern "C" dl_status dl_plan_bench_empty_megakernel(dl_plan* p, int iters, double* us_per_launch,
+                                                    void* stream) {
+  if (!p || !us_per_launch || iters < 1) return fail(DL_ERR_INVALID_ARG, "NULL plan or output");
+  if (!p->d_queues) return fail(DL_ERR_INVALID_ARG, "no megakernel plan");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!p->d_noop_queues) {
+    std::vector<Instr> noop(static_cast<size_t>(p->workers));
+    for (Instr& in : noop) {
+      std::memset(&in, 0, sizeof(in));
+      in.op_row = 0xffffffffu;
+    }
+    CK(cudaMalloc(&p->d_noop_queues, noop.size() * sizeof(Instr)));
+    CK(cudaMemcpy(p->d_noop_queues, noop.data(), noop.size() * sizeof(Instr),
+                  cudaMemcpyHostToDevice));
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(p->workers);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = p->mega_smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  MegaArgs m;
+  std::memset(&m, 0, sizeof(m));
+  m.ops = p->d_ops;
+  m.queues = p->d_noop_queues;
+  m.qlen = 1;
+  m.workers = p->workers;
+  m.events = p->d_events;
+  m.finish_cnt = p->d_finish;
+  m.num_events = p->n_events;
+  m.budget_ns = p->budget_ns;
+  m.trace = nullptr;
+  m.ns = p->mega_ns;
+  m.slot_bytes = p->mega_slot;
+  m.priv_off = p->mega_priv_off;
+  KernelCtx ctx = make_ctx(p, -1);
+  void* args[] = {&m, &ctx};
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  CK(cudaLaunchKernelExC(&lc, mega_kernel(), args));   // warm-up
+  CK(cudaEventRecord(e0, s));
+  for (int i = 0; i < iters; ++i) CK(cudaLaunchKernelExC(&lc, mega_kernel(), args));
+  CK(cudaEventRecord(e1, s));
+  CK(cudaEventSynchronize(e1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *us_per_launch = 1e3 * ms / iters;
+  return DL_OK;
 }
 
 // ------------------------------------------------------------- creation
@@ -726,6 +933,11 @@ static dl_status build_plan(dl_plan* p) {
 
   const size_t MH2 = static_cast<size_t>(M) * H * 2;
   if (const char* e = std::getenv("DL_ATTN")) p->attn_tc = std::strcmp(e, "mma_sync") != 0;
+  if (const char* e = std::getenv("DL_MEGA_HEAD_EVENTS")) p->head_events = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_ATTN_SPLIT_SOFTMAX")) p->split_sm = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_DAG_PROGRAMMATIC_EDGES")) p->dag_prog_edges = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_GEMM_STAGES")) p->gemm_stages_max = std::max(2, std::min(kMaxStages, std::atoi(e)));
+  if (const char* e = std::getenv("DL_ATTN_STAGES")) p->attn_stages_max = std::max(2, std::min(kMaxStages, std::atoi(e)));
   for (int l = 0; l < p->L; ++l) {
     const dl_layer_weights& lw = p->layers[l];
     const bool last = (l == p->L - 1);
@@ -1151,6 +1363,11 @@ extern "C" dl_status dl_plan_debug_buffer(dl_plan* p, int which, void** ptr, siz
     case 10: *ptr = p->act; *bytes = Mr * I * eb; break;
     case 11: *ptr = p->acts; *bytes = M * (I / 128) * 4; break;
     case 12: *ptr = p->y; *bytes = M * H * 2; break;
+    case 16:
+      if (!p->full) return fail(DL_ERR_INVALID_ARG, "debug buffer 16 (final norm) needs a full-step plan");
+      *ptr = p->hfin;
+      *bytes = M * H * 2;
+      break;
     default: return fail(DL_ERR_INVALID_ARG, "unknown debug buffer");
   }
   return DL_OK;

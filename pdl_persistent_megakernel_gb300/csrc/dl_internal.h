@@ -169,6 +169,8 @@ struct AttnArgs {
   int NB;                     // 64-key blocks per pair (from max_context)
   int G;                      // CTAs
   int stages;
+  int max_ctx;                // positions must lie in [0, max_ctx) (else DERR_BOUNDS)
+  int split_sm;               // tcgen05 engine: split softmax up to 32 query rows
   float scale_log2;           // log2(e) / sqrt(d)
   float* ws;                  // partials [G][2][QRp][d] + lse [G][2][QRp]
   unsigned* pair_cnt;         // [R * Hkv]
@@ -197,9 +199,20 @@ struct Instr {
   uint32_t wait_value[4];     // wait until event >= value
   uint32_t signal_event[2];
   uint32_t signal_inc[2];
-  uint32_t pad[16];
+  uint32_t signal_event_hi[2];  // signals 2 and 3 (n_signal <= 4)
+  uint32_t signal_inc_hi[2];
+  uint32_t pad[12];
 };
 static_assert(sizeof(Instr) == 128, "instruction is 128 bytes");
+
+constexpr uint32_t kMaxWaits = 4, kMaxSignals = 4;
+
+__host__ __device__ inline uint32_t instr_signal_event(const Instr& in, uint32_t s) {
+  return s < 2 ? in.signal_event[s] : in.signal_event_hi[s - 2];
+}
+__host__ __device__ inline uint32_t instr_signal_inc(const Instr& in, uint32_t s) {
+  return s < 2 ? in.signal_inc[s] : in.signal_inc_hi[s - 2];
+}
 
 struct MegaArgs {
   const OpArgs* ops;

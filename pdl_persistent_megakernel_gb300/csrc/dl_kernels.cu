@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mega(MegaArgs m, KernelCtx ctx)
         if (!ab) {
           fence_proxy_async_global();
           __threadfence();
-          for (uint32_t s = 0; s < ins.n_signal && s < 2; ++s)
-            red_release_gpu_add(m.events + ins.signal_event[s], ins.signal_inc[s]);
+          for (uint32_t s = 0; s < ins.n_signal && s < kMaxSignals; ++s)
+            red_release_gpu_add(m.events + instr_signal_event(ins, s), instr_signal_inc(ins, s));
         }
         stop = ab ? 1 : 0;
         if (m.trace)

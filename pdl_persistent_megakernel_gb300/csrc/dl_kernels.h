@@ -19,6 +19,10 @@ int attn_smem_bytes(int QRp, int stages);
 // CTAs of a split-KV attention over `pairs` (request, kv head) streams of
 // `nb` 64-key blocks on `sms` SMs (dl_host.cu).
 int attn_ctas(int pairs, int nb, int sms);
+// Pipeline stages of the mma.sync attention kernel for a query-row padding
+// (dl_host.cu): one rule for the plans and the allocation-free entry point,
+// so the kernel's shared-memory attribute is the same whichever sets it.
+int attn_mma_stages(int QRp);
 int norm_smem_bytes();
 cudaError_t launch_test_kv_write(const void* src, void* kv, const int* bt, const int* pos,
                                  int layer, int M, int T, int Hkv, int d, int P,

@@ -9,8 +9,10 @@
 // binding table with the cache's TMA descriptor, the device status word,
 // the per-(request, kv head) arrival counters and the fp32 split-KV
 // partials) from one file-scope __device__ array whose size is fixed at
-// build time.  The kernel it launches is the attention kernel every plan
-// uses; only the origin of its scratch differs.
+// build time.  It launches the split-KV attention kernel on the mma.sync
+// engine (the one the megakernel runs, and the standalone schedules under
+// DL_ATTN=mma_sync) with the plans' work split and pipeline depth; only the
+// origin of its scratch differs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -44,7 +46,6 @@ constexpr size_t kCounterOff = 512;
 constexpr int kMaxPairs = 4096;
 constexpr size_t kPartialOff = kCounterOff + kMaxPairs * sizeof(unsigned);  // 16896
 constexpr int kMaxDevices = 64;
-constexpr int kStageTarget = 210 * 1024;  // shared-memory budget the plans use
 constexpr unsigned long long kBudgetNs = 1000000000ull;
 
 static_assert(sizeof(Binding) <= kStatusOff - kBindingOff, "binding slot");
@@ -64,13 +65,6 @@ struct DeviceSetup {
 std::mutex g_mu;
 DeviceSetup g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
-
-// Pipeline depth of the attention kernel for a query-row padding; the same
-// rule the plans apply, so the kernel's shared-memory attribute is the same
-// whichever caller sets it.
-int attn_stages(int QRp) {
-  return std::max(2, std::min(4, (kStageTarget - attn_smem_bytes(QRp, 0)) / (4 * kAttnKeys * 128)));
-}
 
 dl_status err(dl_status s, const char* what, cudaError_t e = cudaSuccess) {
   char buf[256];
@@ -98,7 +92,7 @@ dl_status setup_current_device(DeviceSetup** out) {
     if (e != cudaSuccess) return err(DL_ERR_CUDA, "cudaDeviceGetAttribute", e);
     for (int QRp : {16, 32, 64}) {
       e = cudaFuncSetAttribute(attn_kernel(QRp), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               attn_smem_bytes(QRp, attn_stages(QRp)));
+                               attn_smem_bytes(QRp, attn_mma_stages(QRp)));
       if (e != cudaSuccess) return err(DL_ERR_CUDA, "cudaFuncSetAttribute", e);
     }
     if (!g_enc) {
@@ -178,11 +172,12 @@ extern "C" dl_status dl_attention_noalloc(const dl_config* c, int layer, const v
   a.QR = QR;
   a.QRp = QR <= 16 ? 16 : (QR <= 32 ? 32 : 64);
   a.NB = (c->max_context + kAttnKeys - 1) / kAttnKeys;
+  a.max_ctx = c->max_context;
   const int sms = c->num_sms > 0 ? std::min(c->num_sms, d->sms) : d->sms;
   a.G = attn_ctas(pairs, a.NB, sms);
   if (static_cast<long long>(pairs) * a.NB * a.G >= (1LL << 32))
     return err(DL_ERR_UNSUPPORTED, "num_requests * n_kv_heads * blocks * CTAs >= 2^32");
-  a.stages = attn_stages(a.QRp);
+  a.stages = attn_mma_stages(a.QRp);
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.d)));
   const size_t need = kPartialOff + static_cast<size_t>(a.G) * 2 * a.QRp * 129 * sizeof(float);
   if (need > kScratchBytes) {

@@ -1317,10 +1317,12 @@ __host__ __device__ inline AttnSmem attn_tc_smem_layout(int QRp, int stages) {
   L.stage_off = (4 * QRp * 128 + 1023) & ~1023;
   L.o_off = L.stage_off + stages * L.stage_bytes;
   L.xs_off = L.o_off;                               // (no score exchange)
-  L.stat_off = L.o_off + QRp * kOP * 4;             // lse, positions, max, sum [QRp]
-  L.bar_off = (L.stat_off + 4 * QRp * 4 + 15) & ~15;
-  L.tbar_off = L.bar_off + 2 * kMaxStages * 8;      // s_full[2] s_free[2] p_full[2] pv_done[2]
-  L.misc_off = L.tbar_off + 8 * 8;
+  // lse, positions, max, sum [QRp]; the split softmax's four partial sums
+  L.stat_off = L.o_off + QRp * kOP * 4;
+  L.bar_off = (L.stat_off + 8 * QRp * 4 + 15) & ~15;
+  // s_full[2] s_free[2] p_full[2] pv_done[2] s_ready[2] s2_free[2]
+  L.tbar_off = L.bar_off + 2 * kMaxStages * 8;
+  L.misc_off = L.tbar_off + 12 * 8;
   L.total = L.misc_off + 64 + 32 * 4 * 4 + 64 * 4 + kMaxContrib * 4 + kMaxContrib * 4;
   return L;
 }
@@ -1544,6 +1546,12 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_full + 4;
   uint64_t* pv_done = s_full + 6;
+  uint64_t* s_ready = s_full + 8;                              // split softmax
+  uint64_t* s2_free = s_full + 10;
+  float* row_lk = row_l1 + QRp;       // [4][QRp] the exp warps' partial sums
+  // staged S of the split softmax, [2][QRp][68] fp32: 64 scores, the
+  // exponent offset -max and the block's rescale factor; it shares its
+  // memory with Ob, which is written only after a pair run's last block
   int* flag = reinterpret_cast<int*>(smem + L.misc_off);
   int* ctb = flag + 16 + 32 * 4 + 64;
   const int U = a.R * a.Hkv * a.NB;
@@ -1552,8 +1560,15 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
   const int ct = tid - 32;
   const int nq = QRp > 32 ? 2 : 1;                   // TMEM lane quarters in use
   const int quarter = warp & 3;
+  // Up to 32 query rows (TMEM lanes 0-31, which only the warps of SM
+  // sub-partition 0 can read) the softmax is split: warp 4 reads S, takes
+  // the row maxima and stages S in shared memory; four exp warps, one per
+  // sub-partition (8, 5, 6, 7), exponentiate 16 keys each.  With 64 rows
+  // two warps per lane quarter alternate blocks.
+  const bool split = QRp <= 32 && a.split_sm;
+  const int ek = !split ? -1 : warp == 8 ? 0 : warp == 5 ? 1 : warp == 6 ? 2 : warp == 7 ? 3 : -1;
   // softmax role: quarter 0 -> warps 4 (k = 0), 8 (k = 1); quarter 1 -> warps 1, 5
-  const bool is_sm = (quarter < nq) && (warp == 4 || warp == 8 || warp == 1 || warp == 5);
+  const bool is_sm = !split && (quarter < nq) && (warp == 4 || warp == 8 || warp == 1 || warp == 5);
   const int kk_sm = (warp >= 5) ? 1 : 0;             // which of the pair
   const int row = quarter * 32 + lane;
   if (ct == 0) {
@@ -1645,8 +1660,12 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
             // keys kk*16 .. +15: two 8-key groups (1024 B apart); the d
             // halves (64 elements each) are 8 KiB apart
             const uint64_t bdd = umma_desc_sw128_mn(vb + kk * 2048, kAttnKeys * 128, 1024);
-            // O[g & 1] starts at the run's first block of its parity
-            umma_bf16(t_o + (g & 1) * 128, ad, bdd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+            // split: one O for the run; else O[g & 1] starts at the run's
+            // first block of its parity
+            if (split)
+              umma_bf16(t_o, ad, bdd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            else
+              umma_bf16(t_o + (g & 1) * 128, ad, bdd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
           }
           umma_commit(pipe_empty(P, pipe_q(P, g)));
           umma_commit(&pv_done[g & 1]);
@@ -1655,6 +1674,195 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
         if (dead && last >= 0) mbar_drain(&pv_done[last & 1], (last >> 1) & 1, ctx.budget_ns);
       }
       dead = __shfl_sync(0xffffffffu, dead ? 1 : 0, 0) != 0;
+    } else if (split && warp == 4) {
+      // ------------------------------------ split softmax: S reader (rows)
+      float* Sst = Ob;
+      const int lim = row < QRp ? row_pos[row] : -1;    // rows past QRp: all masked
+      const int lim0 = row_pos[0];                       // the pair's first query position
+      const float scl = a.scale_log2;
+      float m_run = -INFINITY;
+      for (int j = 0; j < n && !dead; ++j) {
+        const int g = i + j;
+        const int k0 = (blk_a + j) * kAttnKeys;
+        const int nk = min(kAttnKeys, ctxr - k0);
+        if (!warp_wait(&s_full[g & 1], (g >> 1) & 1, ctx, 83)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        float sv[kAttnKeys];
+#pragma unroll
+        for (int c4 = 0; c4 < kAttnKeys / 16; ++c4)
+          tmem_ld16(t_s + t_lane + (g & 1) * kAttnKeys + c4 * 16, sv + c4 * 16);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[g & 1]);
+        // the block's row maximum (four independent chains); masked keys
+        // become -inf, so their probabilities are exactly 0
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (nk == kAttnKeys && k0 + kAttnKeys - 1 <= lim0) {
+#pragma unroll
+          for (int e = 0; e < kAttnKeys; ++e) mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kAttnKeys; ++e) {
+            sv[e] = (e < nk && k0 + e <= lim) ? sv[e] : -INFINITY;
+            mq[e & 3] = fmaxf(mq[e & 3], sv[e]);
+          }
+        }
+        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        mx = row < QRp ? mx * scl : -INFINITY;
+        const bool grow = mx > m_run + 8.f;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mx);
+          m_run = mx;
+        }
+        // O holds blocks i .. g - 1 of the run: rescale it once PV_{g-1} is
+        // done (the exp warps' P_g, and so PV_g, come after this block's
+        // staging below)
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const int gp = g - 1;
+          if (!warp_wait(&pv_done[gp & 1], (gp >> 1) & 1, ctx, 88)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 8; ++c16) {
+            float ov[16];
+            tmem_ld16(t_o + t_lane + c16 * 16, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+            tmem_st16(t_o + t_lane + c16 * 16, ov);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        // staging buffer g & 1 was last read for block g - 2
+        if (g >= 2 && !warp_wait(&s2_free[g & 1], ((g >> 1) - 1) & 1, ctx, 89)) {
+          dead = true;
+          break;
+        }
+        if (row < QRp) {
+          float4* st = reinterpret_cast<float4*>(Sst + ((g & 1) * QRp + row) * 68);
+#pragma unroll
+          for (int e4 = 0; e4 < kAttnKeys / 4; ++e4)
+            st[e4] = make_float4(sv[4 * e4], sv[4 * e4 + 1], sv[4 * e4 + 2], sv[4 * e4 + 3]);
+          st[kAttnKeys / 4] = make_float4(m_run == -INFINITY ? 0.f : -m_run, alpha, 0.f, 0.f);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_ready[g & 1]);
+      }
+      // merge: the four partial sums, then O / l and the rows' lse
+      named_bar(5, 160);
+      float l = 0.f;
+      if (row < QRp) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) l += row_lk[k * QRp + row];
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      bool ok = n > 0 && !dead;
+      if (ok) {
+        const int gl = i + n - 1;      // the last PV into O
+        ok = warp_wait(&pv_done[gl & 1], (gl >> 1) & 1, ctx, 86);
+        if (!ok) dead = true;
+      }
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c16 = 0; c16 < 8; ++c16) {
+          float o[16];
+          tmem_ld16(t_o + t_lane + c16 * 16, o);
+          tmem_wait_ld();
+          if (row < QRp) {
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4)
+              *reinterpret_cast<float4*>(Ob + row * kOP + c16 * 16 + e4 * 4) =
+                  make_float4(o[e4 * 4] * inv, o[e4 * 4 + 1] * inv, o[e4 * 4 + 2] * inv,
+                              o[e4 * 4 + 3] * inv);
+          }
+        }
+        tc_fence_before();
+      } else if (row < QRp) {
+        for (int e4 = 0; e4 < 32; ++e4)
+          *reinterpret_cast<float4*>(Ob + row * kOP + e4 * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (row < QRp) row_lse[row] = l > 0.f ? m_run + log2f(l) : -INFINITY;
+    } else if (ek >= 0) {
+      // ------------------------- split softmax: exp warp ek, keys 16 ek ..
+      const float* Sst = Ob;
+      const float scl = a.scale_log2;
+      const int lrow = lane;                              // query row (< 32)
+      float l_k = 0.f;
+      for (int j = 0; j < n && !dead; ++j) {
+        const int g = i + j;
+        const int k0 = (blk_a + j) * kAttnKeys;
+        const int nk = min(kAttnKeys, ctxr - k0);
+        if (!warp_wait(&s_ready[g & 1], (g >> 1) & 1, ctx, 90)) {
+          dead = true;
+          break;
+        }
+        float sv[16];
+        float nmb = 0.f, alpha = 1.f;
+        if (lrow < QRp) {
+          const float4* st = reinterpret_cast<const float4*>(Sst + ((g & 1) * QRp + lrow) * 68);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 v = st[ek * 4 + q4];
+            sv[4 * q4] = v.x;
+            sv[4 * q4 + 1] = v.y;
+            sv[4 * q4 + 2] = v.z;
+            sv[4 * q4 + 3] = v.w;
+          }
+          const float4 ma = st[kAttnKeys / 4];
+          nmb = ma.x;
+          alpha = ma.y;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s2_free[g & 1]);
+        // P buffer g & 1 was last read by PV_{g-2}
+        if (g >= 2 && !warp_wait(&pv_done[g & 1], ((g >> 1) - 1) & 1, ctx, 91)) {
+          dead = true;
+          break;
+        }
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float p0 = ex2_approx(fmaf(sv[e], scl, nmb));
+          const float p1 = ex2_approx(fmaf(sv[e + 1], scl, nmb));
+          s4[(e >> 1) & 3] += p0 + p1;
+          pk[e >> 1] = pack_bf16(p0, p1);
+        }
+        l_k = l_k * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+        if (nk < kAttnKeys && ek == 0) {
+          // V rows past the context were not loaded (or are stale)
+          uint8_t* vst = attn_v(P, g);
+          for (int e = lane; e < (kAttnKeys - nk) * 16; e += 32) {
+            const int key = nk + (e >> 4), hf = (e >> 3) & 1, c8 = e & 7;
+            *reinterpret_cast<uint4*>(vst + hf * kAttnKeys * 128 + key * 128 + c8 * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (lrow < QRp) {
+          uint8_t* prow = ps + (g & 1) * QRp * 128 + lrow * 128;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c8 = 2 * ek + h2;
+            *reinterpret_cast<uint4*>(prow + ((c8 ^ (lrow & 7)) << 4)) =
+                make_uint4(pk[4 * h2], pk[4 * h2 + 1], pk[4 * h2 + 2], pk[4 * h2 + 3]);
+          }
+        }
+        fence_proxy_async_shared();   // P and the zeroed V rows feed the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+      }
+      if (lrow < QRp) row_lk[ek * QRp + lrow] = l_k;
+      named_bar(5, 160);
     } else if (is_sm) {
       // --------------------------------------------------- softmax warps
       const int lim = row < QRp ? row_pos[row] : -1;    // rows past QRp: all masked
@@ -2222,15 +2430,21 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     }
     if (kTC) {
       uint64_t* tb = reinterpret_cast<uint64_t*>(smem + L.tbar_off);
+      // split softmax (up to 32 query rows): one warp reads S, four write P
+      const bool split = QRp <= 32 && a.split_sm;
       const uint32_t nsm = QRp > 32 ? 2u : 1u;
-      mbar_init(&tb[0], 1);      // s_full: QK^T commit
+      mbar_init(&tb[0], 1);                  // s_full: QK^T commit
       mbar_init(&tb[1], 1);
-      mbar_init(&tb[2], nsm);    // s_free: softmax warps read S
-      mbar_init(&tb[3], nsm);
-      mbar_init(&tb[4], nsm);    // p_full: softmax warps wrote P
-      mbar_init(&tb[5], nsm);
-      mbar_init(&tb[6], 1);      // pv_done: PV commit
+      mbar_init(&tb[2], split ? 1u : nsm);   // s_free: S read from TMEM
+      mbar_init(&tb[3], split ? 1u : nsm);
+      mbar_init(&tb[4], split ? 4u : nsm);   // p_full: P written
+      mbar_init(&tb[5], split ? 4u : nsm);
+      mbar_init(&tb[6], 1);                  // pv_done: PV commit
       mbar_init(&tb[7], 1);
+      mbar_init(&tb[8], 1);                  // s_ready: S staged (split)
+      mbar_init(&tb[9], 1);
+      mbar_init(&tb[10], 4);                 // s2_free: staged S read (split)
+      mbar_init(&tb[11], 4);
     }
     flag[0] = flag[1] = 0;
     flag[2] = 1;
@@ -2252,7 +2466,13 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     const int* pos = resolve<const int>(a.pos, bd);
     const int* bt = resolve<const int>(a.bt, bd);
     const int M = a.R * a.T;
-    for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
+    for (int m = lane; m < M; m += 32) {
+      // a position outside [0, max_context) is reported; the keys past the
+      // plan's blocks are never loaded, so the row is still safe to compute
+      const int p = pos[m];
+      if (p < 0 || p >= a.max_ctx) report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 33, p);
+      ppos[m] = p;
+    }
     __syncwarp();
     const uint64_t pol = policy_evict_first();
     const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box
@@ -2474,7 +2694,11 @@ __device__ __noinline__ bool mk_produce_attn(const AttnArgs& a_, int c, const De
   const int* pos = resolve<const int>(a.pos, bd);
   const int* bt = resolve<const int>(a.bt, bd);
   const int M = a.R * a.T;
-  for (int m = lane; m < M; m += 32) ppos[m] = pos[m];
+  for (int m = lane; m < M; m += 32) {
+    const int p = pos[m];
+    if (p < 0 || p >= a.max_ctx) report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 66, p);
+    ppos[m] = p;
+  }
   __syncwarp();
   const uint64_t pol = policy_evict_first();
   const int box = a.P < kAttnKeys ? a.P : kAttnKeys;   // rows per TMA box

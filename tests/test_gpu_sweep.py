@@ -38,7 +38,7 @@ def test_sweep_cell(batch, context, fp8):
     for mode in (dl.MODE_SERIAL, dl.MODE_MEGAKERNEL):
         what = f"{cfg.name}/{dl.MODE_NAMES[mode]}"
         out, kv = c.run(plan, mode)
-        c.check_kv(kv, what)
+        c.check_kv(kv, what, plan)
         if fp8:
             c.check_layer_out(out, what)
             continue

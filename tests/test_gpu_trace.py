@@ -69,14 +69,56 @@ def test_trace_stamps_ordered_and_units_complete(mode, monkeypatch):
         want = _units(cfg, name, grid)
         if want is not None:
             assert int(t[:, 5].sum()) == want, (name, int(t[:, 5].sum()), want)
-        # every share of op k starts its dependent reads after op k-1 ended
-        if k > 0 and mode != dl.MODE_SERIAL:
+        # every share of op k starts its dependent reads after op k-1 ended;
+        # in the megakernel an attention share waits only for the QKV tiles
+        # of its kv heads (per-head events): after the shares that finish them
+        if k > 0 and mode == dl.MODE_MEGAKERNEL and name == "attention":
+            _check_head_events(cfg, tr, k, ops)
+        elif k > 0 and mode != dl.MODE_SERIAL:
             assert deps.min() >= prev_end - 2000, name   # globaltimer granularity slack
         prev_end = int(end.max())
         assert (tr[k, grid:] == 0).all(), name
     # reading cleared the table
     assert not plan.trace().any()
     plan.close()
+
+
+def _sk_begin(U, G, c):
+    return (U * c) // G
+
+
+def _sk_owner(U, G, x):
+    """The share whose Stream-K range holds unit x."""
+    c = min(G - 1, (x * G) // U)
+    while c > 0 and _sk_begin(U, G, c) > x:
+        c -= 1
+    while c + 1 < G and _sk_begin(U, G, c + 1) <= x:
+        c += 1
+    return c
+
+
+def _check_head_events(cfg, tr, k, ops):
+    """Each attention share's dependent reads start after the QKV shares
+    that finish (own the first unit of) every tile of its pairs' kv heads:
+    the group's q heads, the k head and the v head."""
+    Hq, Hkv = cfg.n_q_heads, cfg.n_kv_heads
+    G = Hq // Hkv
+    kb = cfg.hidden // (128 if cfg.fp8 else 64)
+    nt = Hq + 2 * Hkv
+    gq, ga = ops[k - 1][1], ops[k][1]
+    uq = nt * kb
+    qend = tr[k - 1, :gq, 4].astype(np.int64)
+    nb = -(-cfg.context // 64)
+    ua = cfg.num_requests * Hkv * nb
+    adeps = tr[k, :ga, 1].astype(np.int64)
+    for c in range(ga):
+        u0, u1 = _sk_begin(ua, ga, c), _sk_begin(ua, ga, c + 1)
+        if u1 <= u0:
+            continue
+        heads = {p % Hkv for p in range(u0 // nb, (u1 - 1) // nb + 1)}
+        tiles = [t for h in heads for t in list(range(h * G, h * G + G)) + [Hq + h, Hq + Hkv + h]]
+        owners = {_sk_owner(uq, gq, t * kb) for t in tiles}
+        assert adeps[c] >= max(qend[o] for o in owners) - 2000, ("attention share", c)
 
 
 def test_trace_off_is_reported():

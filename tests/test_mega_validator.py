@@ -15,14 +15,16 @@ OK, INVALID_ARG, PLAN_INVALID = 0, 1, 6
 
 def instr(op, cta=0, waits=(), signals=((None, 1),)):
     """One instruction as 32 uint32: op_row, cta, n_wait, n_signal,
-    wait_event[4], wait_value[4], signal_event[2], signal_inc[2], pad."""
+    wait_event[4], wait_value[4], signal_event[0:2], signal_inc[0:2],
+    signal_event[2:4], signal_inc[2:4], pad."""
     w = np.zeros(32, dtype=np.uint32)
     w[0], w[1] = op, cta
     w[2], w[3] = len(waits), len(signals)
     for k, (e, v) in enumerate(waits):
         w[4 + k], w[8 + k] = e, v
     for k, (e, inc) in enumerate(signals):
-        w[12 + k], w[14 + k] = (op if e is None else e), inc
+        base = 12 if k < 2 else 14
+        w[base + k], w[base + 2 + k] = (op if e is None else e), inc
     return w
 
 
@@ -123,7 +125,7 @@ def test_malformed_counts_and_events_are_rejected():
     bad[0, 1, 2] = 5                            # n_wait > 4
     assert validate(bad, 2) == PLAN_INVALID
     bad = q.copy()
-    bad[0, 0, 3] = 3                            # n_signal > 2
+    bad[0, 0, 3] = 5                            # n_signal > 4
     assert validate(bad, 2) == PLAN_INVALID
     bad = q.copy()
     bad[0, 0, 12] = 7                           # signal of an unknown event
@@ -135,3 +137,26 @@ def test_empty_description_is_an_argument_error():
     assert L.dl_test_validate_mega_queues(None, 1, 1, 1) == INVALID_ARG
     q = chain_queues(1, 1)
     assert validate(q, 0) == INVALID_ARG
+
+
+def test_per_head_events_signalled_by_an_earlier_op():
+    """Events that are not an op's own (the per-head events of a QKV
+    projection): a later op may wait on them once their signals, from any
+    instruction of earlier ops and in any of the four signal slots, reach
+    the threshold; waiting on one that the same or a later op signals is a
+    deadlock."""
+    workers = 2
+    # op 0 signals its own event and head events 2 and 3 (slots 2 and 3)
+    q = np.zeros((workers, 3, 32), dtype=np.uint32)
+    q[0, 0] = instr(0, 0, (), ((None, 1), (2, 1), (3, 2)))
+    q[1, 0] = instr(0, 1, (), ((None, 1), (2, 1), (3, 1), (4, 1)))
+    q[0, 1] = instr(1, 0, ((2, 2), (3, 3)))
+    q[1, 1] = instr(1, 1, ((4, 1),))
+    q[:, 2] = noop()
+    assert validate(q, 5) == OK
+    bad = q.copy()
+    bad[1, 1] = instr(1, 1, ((3, 4),))          # only 3 signalled
+    assert validate(bad, 5) == PLAN_INVALID
+    bad = q.copy()
+    bad[0, 1] = instr(1, 0, ((2, 2),), ((None, 1), (4, 1)))   # op 1 signals 4 ...
+    assert validate(bad, 5) == PLAN_INVALID     # ... which op 1 waits on
