@@ -134,6 +134,37 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class L2Flush:
+    """What runs between timed steps (outside the events).
+    flush: a 256 MiB write.  It evicts everything, but leaves L2 full of
+      dirty lines, which the timed step then writes back to HBM as its own
+      reads evict them (up to the 129 MB of L2 of extra write traffic).
+    clean: the same write, then a read of another 256 MiB buffer, so that the
+      timed step starts from an L2 holding clean, unrelated lines: nothing of
+      the step's inputs, nothing to write back.
+    stream: nothing (one step reads more bytes than L2 holds)."""
+
+    def __init__(self, mode: str, device):
+        import torch
+        self.mode = mode
+        self.w = self.r = None
+        if mode in ("flush", "clean"):
+            self.w = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        if mode == "clean":
+            self.r = torch.zeros(64 << 20, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        if self.w is not None:
+            self.w.zero_()
+        if self.r is not None:
+            self.r.sum()
+
+    def describe(self) -> str:
+        return {"flush": "256 MiB write between timed steps",
+                "clean": "256 MiB write, then a 256 MiB read of another buffer, between timed steps",
+                "stream": "no flush: each step reads more than L2 holds"}[self.mode]
+
+
 def build_workload(name: str, device, cpu_weights: bool):
     from pdl_persistent_megakernel_gb300 import synth
     cfg = synth.CONFIGS[name]
@@ -566,9 +597,11 @@ def main():
     ap.add_argument("--micro", action="store_true",
                     help="microbenchmarks: tcgen05.mma cost, acquire-poll round trip, empty "
                          "megakernel, trace build overhead")
-    ap.add_argument("--l2", default="flush", choices=["flush", "stream"],
-                    help="flush: a 256 MiB write before every step; stream: steps back to "
-                         "back (each step reads more bytes than the 129 MB L2 holds)")
+    ap.add_argument("--l2", default="flush", choices=["flush", "clean", "stream"],
+                    help="flush: a 256 MiB write before every step; clean: that write, then a "
+                         "256 MiB read of another buffer (no dirty line left for the step to "
+                         "write back); stream: steps back to back (each step reads more "
+                         "bytes than the 129 MB L2 holds)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
@@ -614,7 +647,9 @@ def main():
     bt, pos = inp["block_table"].to(device), inp["positions"].to(device)
     out = (torch.empty((cfg.M,), dtype=torch.int32, device=device) if cfg.vocab
            else torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device))
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    l2 = L2Flush(args.l2, device)
+    # per-kernel timings always start from an evicted L2
+    l2k = l2 if args.l2 != "stream" else L2Flush("clean", device)
     algo = bytes_model.algorithmic_bytes(cfg)["total"]
     peak, peak_kind = measured_peaks()
 
@@ -626,15 +661,13 @@ def main():
     def timed_steps(mode, k, w_):
         with torch.cuda.stream(stream):
             for _ in range(w_):
-                if args.l2 == "flush":
-                    flush.zero_()
+                l2()
                 plan.step(x, res, kv, bt, pos, out, mode, stream)
             barrier()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(k)]
             for a, b in evs:
-                if args.l2 == "flush":
-                    flush.zero_()
+                l2()
                 a.record(stream)
                 plan.step(x, res, kv, bt, pos, out, mode, stream)
                 b.record(stream)
@@ -665,7 +698,7 @@ def main():
         for i, (nm, grid, smem) in enumerate(ops):
             evs = []
             for _ in range(max(3, args.steps)):
-                flush.zero_()
+                l2k()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 plan.launch_op(i, stream)
@@ -710,8 +743,7 @@ def main():
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         evs = []
         for _ in range(args.steps):
-            if args.l2 == "flush":
-                flush.zero_()
+            l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             plan.step_host(xh, rh, kv, bth, posh, outh, emode, stream)
@@ -752,8 +784,7 @@ def main():
                        "tokens_per_request": cfg.tokens_per_request, "context": cfg.context,
                        "page_size": cfg.page_size,
                        "weights": "fp8_e4m3_b128" if cfg.fp8 else "bf16",
-                       "algorithmic_bytes": algo, "l2": ("256 MiB write between timed steps" if args.l2 == "flush" else
-                              "no flush: each step reads more than L2 holds"),
+                       "algorithmic_bytes": algo, "l2": l2.describe(),
                        "replicas": ws},
             "us_per_layer": r["us"] / cfg.n_layers,
             "frac_of_8TBs": r["frac_of_8TBs"],

@@ -298,6 +298,7 @@ struct GemmShared {
   uint64_t* tempty;
   uint64_t* tready;  // [2] finished tile buffer b written (4 epilogue warps)
   uint64_t* tfree;   // [2] tile buffer b finished and free (2 fix-up warps)
+
   int* flag;      // [4]
   int* ctb;       // [kMaxContrib] contributor list of a fix-up
   int* flag2;     // the epilogue warps' own control area (last tile)
@@ -930,6 +931,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
           trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
         }
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
+        const bool fp8 = a.fp8 != 0;
         const int nslots = (nunits + P.ups - 1) / P.ups;
         uint32_t last_tq = 0;
         bool any_tq = false;
@@ -948,18 +950,23 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
               break;
             }
             tc_fence_after();
-            const uint32_t sb = smem_u32(gemm_x(P, i));
+            // descriptors built once per operand and advanced by constants
+            // (the start-address field counts 16-byte units: +32 bytes of K
+            // = +2); a single thread issues every MMA, and per-MMA address
+            // arithmetic between them is what bounds its issue rate
+            const uint64_t bd0 = umma_desc_sw128(smem_u32(gemm_x(P, i)));
+            const uint32_t dbase = TR.base + b * TR.stride;
             for (int p = 0; p < npair; ++p) {
-              const uint32_t d = TR.base + b * TR.stride + p * kMp;
-              const uint32_t sa = smem_u32(gemm_w(P, i, p));
+              const uint32_t d = dbase + p * kMp;
+              const uint64_t ad0 = umma_desc_sw128(smem_u32(gemm_w(P, i, p)));
+              if (fp8) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = umma_desc_sw128(sa + k * 32);
-                const uint64_t bd = umma_desc_sw128(sb + k * 32);
-                if (a.fp8)
-                  umma_e4m3(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-                else
-                  umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                for (int k = 0; k < 4; ++k)
+                  umma_e4m3(d, ad0 + 2 * k, bd0 + 2 * k, idesc, k > 0 ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  umma_bf16(d, ad0 + 2 * k, bd0 + 2 * k, idesc, k > 0 ? 1u : 0u);
               }
             }
             umma_commit(&sh.tfull[b]);
@@ -1581,6 +1588,7 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
   const uint16_t* qg = static_cast<const uint16_t*>(a.q);
   const uint32_t qs_u32 = smem_u32(qs), ps_u32 = smem_u32(ps);
   const uint32_t idesc_s = umma_idesc(kAttnKeys, true);
+  const uint64_t qd0 = umma_desc_sw128(qs_u32), qd1 = qd0 + QRp * 128 / 16;   // Q d-halves
   const uint32_t idesc_o = umma_idesc(128, true) | (1u << 16);   // B (V) MN-major
   const uint32_t t_o = tmem, t_s = tmem + 256;
   const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -1613,11 +1621,17 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
     for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
     fence_proxy_async_shared();    // Q, written by threads, is read by the tensor core
     named_bar(1, 256);
-    if (warp == 2) {
+    if (warp == 2 || (split && warp == 1)) {
       // --------------------------------------------------- QK^T issuer
-      if (lane == 0 && !dead && n > 0) {
+      // One thread issues a tcgen05.mma every ~70 ns at best, so with the
+      // split softmax (warp 1 otherwise idle) two threads issue QK^T, warp 2
+      // the run's even blocks and warp 1 the odd ones: a block and the one
+      // two later share an S buffer and an issuer.
+      const int jstep = split ? 2 : 1;
+      const int jfirst = warp == 1 ? 1 : 0;
+      if (lane == 0 && !dead && n > jfirst) {
         int last = -1;
-        for (int j = 0; j < n; ++j) {
+        for (int j = jfirst; j < n; j += jstep) {
           const int g = i + j;
           const uint32_t q = pipe_q(P, g);
           if (!mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 80) ||
@@ -1627,13 +1641,15 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
           }
           if (g == 0) trace_stamp(ctx, c, TR_FIRST);
           tc_fence_after();
-          const uint32_t kb = smem_u32(attn_k(P, g));
+          // descriptors advanced by constants (16-byte units): the d half
+          // is QRp * 128 (Q) or 64 * 128 (K) bytes on, each K step 32
+          const uint64_t kd0 = umma_desc_sw128(smem_u32(attn_k(P, g)));
+          const uint32_t ts = t_s + (g & 1) * kAttnKeys;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = umma_desc_sw128(qs_u32 + (kk >> 2) * QRp * 128 + (kk & 3) * 32);
-            const uint64_t bdd = umma_desc_sw128(kb + (kk >> 2) * kAttnKeys * 128 + (kk & 3) * 32);
-            umma_bf16(t_s + (g & 1) * kAttnKeys, ad, bdd, idesc_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(ts, (kk < 4 ? qd0 : qd1) + 2 * (kk & 3),
+                      kd0 + (kk >> 2) * (kAttnKeys * 128 / 16) + 2 * (kk & 3), idesc_s,
+                      kk > 0 ? 1u : 0u);
           umma_commit(&s_full[g & 1]);
           last = g;
         }
@@ -1652,21 +1668,19 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
             break;
           }
           tc_fence_after();
-          const uint32_t vb = smem_u32(attn_v(P, g));
-          const uint32_t pb = ps_u32 + (g & 1) * QRp * 128;
+          // keys kk*16 .. +15: two 8-key groups (1024 B apart); the d halves
+          // (64 elements each) are 8 KiB apart; descriptors advanced by
+          // constants (16-byte units)
+          const uint64_t pd0 = umma_desc_sw128(ps_u32 + (g & 1) * QRp * 128);
+          const uint64_t vd0 = umma_desc_sw128_mn(smem_u32(attn_v(P, g)), kAttnKeys * 128, 1024);
+          // split: one O for the run; else O[g & 1] starts at the run's first
+          // block of its parity
+          const uint32_t to = split ? t_o : t_o + (g & 1) * 128;
+          const bool acc0 = split ? j > 0 : j > 1;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = umma_desc_sw128(pb + kk * 32);
-            // keys kk*16 .. +15: two 8-key groups (1024 B apart); the d
-            // halves (64 elements each) are 8 KiB apart
-            const uint64_t bdd = umma_desc_sw128_mn(vb + kk * 2048, kAttnKeys * 128, 1024);
-            // split: one O for the run; else O[g & 1] starts at the run's
-            // first block of its parity
-            if (split)
-              umma_bf16(t_o, ad, bdd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            else
-              umma_bf16(t_o + (g & 1) * 128, ad, bdd, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(to, pd0 + 2 * kk, vd0 + kk * (2048 / 16), idesc_o,
+                      (acc0 || kk > 0) ? 1u : 0u);
           umma_commit(pipe_empty(P, pipe_q(P, g)));
           umma_commit(&pv_done[g & 1]);
           last = g;
