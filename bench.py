@@ -301,12 +301,36 @@ def run_sweep(args):
                             [a.elapsed_time(b) * 1e3 for a, b in evs])
                 plan.status()
                 plan.close()
+                # the megakernel again with every attention share waiting on
+                # the whole QKV projection (no per-head events)
+                os.environ["DL_MEGA_HEAD_EVENTS"] = "0"
+                plan = dl.Plan(cfg, wd, modes_mask=1 << dl.MODE_MEGAKERNEL)
+                os.environ.pop("DL_MEGA_HEAD_EVENTS", None)
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup):
+                        plan.step(inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"],
+                                  inp["positions"], out, dl.MODE_MEGAKERNEL, stream)
+                    evs = []
+                    for _ in range(args.steps):
+                        flush()
+                        a, b = (torch.cuda.Event(enable_timing=True),
+                                torch.cuda.Event(enable_timing=True))
+                        a.record(stream)
+                        plan.step(inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"],
+                                  inp["positions"], out, dl.MODE_MEGAKERNEL, stream)
+                        b.record(stream)
+                        evs.append((a, b))
+                    torch.cuda.synchronize(device)
+                op_wait_us = statistics.median([a.elapsed_time(b) * 1e3 for a, b in evs])
+                plan.status()
+                plan.close()
                 best = min(res, key=res.get)
                 cell = {"batch": batch, "context": ctx, "dtype": "fp8_e4m3" if fp8 else "bf16",
                         "us": {k: round(v, 2) for k, v in res.items()}, "best": best,
                         "best_GBs": round(algo / (res[best] * 1e-6) / 1e9, 1),
                         "frac_of_8TBs": round(algo / (res[best] * 1e-6) / 1e9 / HBM_NOMINAL_GBS, 3),
                         "mega_over_pdl": round(res["megakernel"] / res["graph_linear_pdl"], 3),
+                        "megakernel_op_wait_us": round(op_wait_us, 2),
                         "algorithmic_bytes": algo}
                 cells.append(cell)
                 print(json.dumps(cell), file=sys.stderr, flush=True)
