@@ -136,6 +136,15 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def l2_bytes(device) -> int:
+    """The device's L2 size (129 MB, GB300's, where torch reports none)."""
+    import torch
+    dev = torch.device(device)
+    if dev.type != "cuda":
+        return int(129e6)
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
+
+
 class L2Flush:
     """What runs between timed steps (outside the events).
     flush: a 256 MiB write.  It evicts everything, but leaves L2 full of
@@ -144,27 +153,42 @@ class L2Flush:
     clean: the same write, then a read of another 256 MiB buffer, so that the
       timed step starts from an L2 holding clean, unrelated lines: nothing of
       the step's inputs, nothing to write back.
-    stream: nothing (one step reads more bytes than L2 holds)."""
+    stream: nothing.  Valid only when one step reads at least twice the
+      bytes L2 holds, so that nothing a step reads survives to the next.
+    auto: stream for such workloads (`step_bytes` >= 2 x L2), clean for the
+      others.
+    The buffers are allocated at the first call."""
 
-    def __init__(self, mode: str, device):
-        import torch
+    def __init__(self, mode: str, device, step_bytes: float = None):
+        if mode == "auto":
+            big = step_bytes is not None and step_bytes >= 2 * l2_bytes(device)
+            mode = "stream" if big else "clean"
         self.mode = mode
+        self.device = device
         self.w = self.r = None
-        if mode in ("flush", "clean"):
-            self.w = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-        if mode == "clean":
-            self.r = torch.zeros(64 << 20, dtype=torch.int32, device=device)
 
     def __call__(self):
-        if self.w is not None:
-            self.w.zero_()
+        import torch
+        if self.mode == "stream":
+            return
+        if self.w is None:
+            self.w = torch.empty(256 << 20, dtype=torch.uint8, device=self.device)
+            if self.mode == "clean":
+                self.r = torch.zeros(64 << 20, dtype=torch.int32, device=self.device)
+        self.w.zero_()
         if self.r is not None:
             self.r.sum()
+
+    @staticmethod
+    def describe_all() -> str:
+        return "stream = steps back to back (a step reads >= 2 x L2); clean = 256 MiB " \
+               "write, then a 256 MiB read of another buffer, between timed steps"
 
     def describe(self) -> str:
         return {"flush": "256 MiB write between timed steps",
                 "clean": "256 MiB write, then a 256 MiB read of another buffer, between timed steps",
-                "stream": "no flush: each step reads more than L2 holds"}[self.mode]
+                "stream": "no flush: steps back to back, each reading at least twice the "
+                          "bytes L2 holds"}[self.mode]
 
 
 def build_workload(name: str, device, cpu_weights: bool):
@@ -266,7 +290,6 @@ def run_sweep(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
-    flush = L2Flush(args.l2, device)
     modes = [dl.MODE_SERIAL, dl.MODE_GRAPH_LINEAR_PDL, dl.MODE_MEGAKERNEL]
     cells = []
     for fp8 in (False, True):
@@ -280,6 +303,7 @@ def run_sweep(args):
                 plan = dl.Plan(cfg, wd, modes_mask=sum(1 << m for m in modes))
                 out = torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device)
                 algo = bytes_model.algorithmic_bytes(cfg)["total"]
+                flush = L2Flush(args.l2, device, algo)
                 res = {}
                 with torch.cuda.stream(stream):
                     for m in modes:
@@ -331,14 +355,15 @@ def run_sweep(args):
                         "frac_of_8TBs": round(algo / (res[best] * 1e-6) / 1e9 / HBM_NOMINAL_GBS, 3),
                         "mega_over_pdl": round(res["megakernel"] / res["graph_linear_pdl"], 3),
                         "megakernel_op_wait_us": round(op_wait_us, 2),
-                        "algorithmic_bytes": algo}
+                        "algorithmic_bytes": algo, "l2": flush.mode}
                 cells.append(cell)
                 print(json.dumps(cell), file=sys.stderr, flush=True)
                 del inp, out
                 torch.cuda.empty_cache()
     print(json.dumps({"metric": "crossover sweep: decode-layer us per schedule and best GB/s",
                       "cells": cells, "steps": args.steps, "warmup": args.warmup,
-                      "l2": "256 MiB write between timed steps", "data": "synthetic"}),
+                      "l2": "per cell (" + args.l2 + "): " + L2Flush.describe_all(),
+                      "data": "synthetic"}),
           flush=True)
 
 
@@ -429,7 +454,8 @@ def run_trace(args):
         out = torch.zeros((cfg.M,), dtype=torch.int32, device=device)
     else:
         out = torch.zeros((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device)
-    flush = L2Flush(args.l2, device)
+    from pdl_persistent_megakernel_gb300 import bytes_model
+    flush = L2Flush(args.l2, device, bytes_model.algorithmic_bytes(cfg)["total"])
     args_ = (inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"], inp["positions"], out)
     for mode in modes:
         for _ in range(max(3, args.warmup)):
@@ -475,7 +501,8 @@ def run_micro(args):
     inp = {k: v.to(device) for k, v in inp.items()}
     out = torch.zeros((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device) \
         if not cfg.vocab else torch.zeros((cfg.M,), dtype=torch.int32, device=device)
-    flush = L2Flush(args.l2, device)
+    from pdl_persistent_megakernel_gb300 import bytes_model
+    flush = L2Flush(args.l2, device, bytes_model.algorithmic_bytes(cfg)["total"])
     args_ = (inp["x"], inp["residual"], inp["kv_pages"], inp["block_table"], inp["positions"], out)
     modes = (dl.MODE_GRAPH_LINEAR_PDL, dl.MODE_MEGAKERNEL)
     mask = sum(1 << m for m in modes)
@@ -599,7 +626,7 @@ def run_ablation(args):
         torch.cuda.empty_cache()
     print(json.dumps({"metric": "programmatic-launch ablation: norm -> QKV edge span (us)",
                       "cells": out_cells, "incremental": incremental, "steps": reps,
-                      "warmup": args.warmup, "l2": "256 MiB write before every replay",
+                      "warmup": args.warmup, "l2": flush.describe(),
                       "data": "synthetic"}), flush=True)
 
 
@@ -623,11 +650,11 @@ def main():
     ap.add_argument("--micro", action="store_true",
                     help="microbenchmarks: tcgen05.mma cost, acquire-poll round trip, empty "
                          "megakernel, trace build overhead")
-    ap.add_argument("--l2", default="stream", choices=["flush", "clean", "stream"],
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "clean", "stream"],
                     help="flush: a 256 MiB write before every step; clean: that write, then a "
                          "256 MiB read of another buffer (no dirty line left for the step to "
-                         "write back); stream: steps back to back (each step reads more "
-                         "bytes than the 129 MB L2 holds)")
+                         "write back); stream: steps back to back; auto (default): stream "
+                         "when one step reads at least twice the L2 size, else clean")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
@@ -673,10 +700,10 @@ def main():
     bt, pos = inp["block_table"].to(device), inp["positions"].to(device)
     out = (torch.empty((cfg.M,), dtype=torch.int32, device=device) if cfg.vocab
            else torch.empty((2, cfg.M, cfg.hidden), dtype=torch.bfloat16, device=device))
-    l2 = L2Flush(args.l2, device)
-    # per-kernel timings always start from an evicted L2
-    l2k = l2 if args.l2 != "stream" else L2Flush("clean", device)
     algo = bytes_model.algorithmic_bytes(cfg)["total"]
+    l2 = L2Flush(args.l2, device, algo)
+    # per-kernel timings always start from an evicted L2
+    l2k = l2 if l2.mode != "stream" else L2Flush("clean", device)
     peak, peak_kind = measured_peaks()
 
     def barrier():
@@ -718,7 +745,7 @@ def main():
     # the best schedule again from an evicted L2 (when the steps ran back to
     # back): written, then another buffer read, before every step
     evicted = None
-    if args.l2 == "stream":
+    if l2.mode == "stream":
         l2_saved = l2
         l2 = L2Flush("clean", device)
         ms = timed_steps(name_to_mode[best], args.steps, args.warmup)

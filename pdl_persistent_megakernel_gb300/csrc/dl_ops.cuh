@@ -937,6 +937,14 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         bool any_tq = false;
         for (int j = w; j < nslots; j += 2) {
           const uint32_t q = P.seq0 + static_cast<uint32_t>(j);
+          // With an odd number of slots a stage's consecutive uses belong to
+          // different issuers, and nothing else keeps this issuer from
+          // running a whole ring ahead of the other (the TMEM ring only
+          // does when it is no deeper than the slot ring): the parity wait
+          // on slot q would then match the stage's earlier phase, still
+          // the other issuer's slot q - ns.  So first wait until that
+          // earlier use has been consumed (its commit frees the stage).
+          if (q >= P.ns && !mbar_wait(pipe_empty(P, q - P.ns), pipe_par(P, q - P.ns), ctx, 12)) break;
           if (!mbar_wait(pipe_full(P, q), pipe_par(P, q), ctx, 14)) break;
           const int i0 = j * P.ups, i1 = min(nunits, i0 + P.ups);
           bool ok = true;
