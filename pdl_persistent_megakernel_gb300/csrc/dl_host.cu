@@ -128,6 +128,9 @@ struct dl_plan {
   // megakernel: attention shares wait on per-head QKV tile events
   // (DL_MEGA_HEAD_EVENTS=0: on the whole projection)
   bool head_events = true;
+  // a projection whose output only feeds the next norm leaves its Stream-K
+  // fix-up to that norm (EPI_PARTIALS)
+  bool defer_fixup = true;
   unsigned long long budget_ns = 1000000000ull;
 
   std::vector<void*> allocs;
@@ -151,6 +154,10 @@ struct dl_plan {
   std::vector<CUtensorMap> h_maps;
 
   std::vector<LaunchOp> lin, dag;
+  // the megakernel's ops: the linear list with every Stream-K fix-up in its
+  // projection (its norm instructions run on M workers, where reading the
+  // projection's partials measured slower than the fix-up on all of them)
+  std::vector<LaunchOp> mega;
 
   // megakernel
   OpArgs* d_ops = nullptr;
@@ -244,7 +251,7 @@ static LaunchOp make_norm(dl_plan* p, DPtr x, DPtr res, DPtr rout, const void* w
   a.H = p->H;
   a.rows_per_cta = 1;
   a.eps = p->cfg.eps;
-  op.kernel = norm_kernel();
+  op.kernel = norm_kernel(p->H);
   op.grid = p->M;
   op.smem = norm_smem_bytes();
   op.name = name;
@@ -307,6 +314,51 @@ static LaunchOp make_gemm(dl_plan* p, const GemmSpec& s, unsigned* cnt) {
   op.smem = gemm_smem_bytes(npair, a.Mp, a.stages, a.KB, a.fp8, s.epi, a.M, a.share_max);
   op.name = s.name;
   return op;
+}
+
+// Deferred Stream-K fix-up: a bf16-output projection directly followed by a
+// norm that reads exactly that output (the O projection before the second
+// norm, the down projection before the next layer's first norm or the final
+// norm) skips its fix-up and epilogue: each CTA writes the partial of every
+// tile its range touches and leaves, and the norm forms each element as the
+// CTA-ordered sum of the tile's partials (the order of the fix-up, so the
+// result is the same to the bit) before its residual add.  The projection's
+// tail -- waiting for the other contributors, reading their partials, the
+// epilogue -- leaves the critical path; the norm reads the partials in the
+// round trip in which it read the projection's output.  Taken only when
+// every CTA's range touches at most two tiles (its two partial slots) and no
+// tile has more than kMaxPartContrib contributors.
+static unsigned host_sk_begin(unsigned U, int G, int c);
+static void defer_fixups(std::vector<LaunchOp>& ops) {
+  for (size_t i = 0; i + 1 < ops.size(); ++i) {
+    LaunchOp& g = ops[i];
+    LaunchOp& n = ops[i + 1];
+    if (g.args.kind != OP_GEMM || n.args.kind != OP_NORM || g.branch != 0 || n.branch != 0) continue;
+    GemmArgs& a = g.args.gemm;
+    NormArgs& na = n.args.norm;
+    if (a.epi != EPI_STORE_BF16 || a.pair || a.t_base != 0 || a.NT * 128 != na.H ||
+        a.out.slot >= 0 || a.out.p != na.x.p || a.out.offset != na.x.offset || a.ldo != na.H ||
+        na.x.slot >= 0 || na.H > 64 * 128)
+      continue;
+    const unsigned U = static_cast<unsigned>(a.NT) * static_cast<unsigned>(a.KB);
+    bool ok = true;
+    std::vector<int> contrib(static_cast<size_t>(a.NT), 0);
+    for (int c = 0; c < a.G && ok; ++c) {
+      const unsigned u0 = host_sk_begin(U, a.G, c), u1 = host_sk_begin(U, a.G, c + 1);
+      if (u1 <= u0) continue;
+      const int t0 = static_cast<int>(u0 / a.KB), t1 = static_cast<int>((u1 - 1) / a.KB);
+      if (t1 - t0 > 1) ok = false;
+      for (int t = t0; t <= t1 && ok; ++t)
+        if (++contrib[t] > kMaxPartContrib) ok = false;
+    }
+    if (!ok) continue;
+    a.epi = EPI_PARTIALS;
+    na.part = a.ws;
+    na.part_U = static_cast<int>(U);
+    na.part_G = a.G;
+    na.part_KB = a.KB;
+    na.part_mp = a.Mp;
+  }
 }
 
 // CTAs of the split-KV attention: a whole number of CTAs per (request, kv
@@ -528,7 +580,7 @@ static int host_sk_owner(unsigned U, int G, unsigned x) {
 }
 
 static dl_status build_mega(dl_plan* p) {
-  const std::vector<LaunchOp>& ops = p->lin;
+  const std::vector<LaunchOp>& ops = p->mega;
   const int nops = static_cast<int>(ops.size());
   p->workers = p->sms;
   std::vector<std::vector<Instr>> qs(p->workers);
@@ -934,6 +986,7 @@ static dl_status build_plan(dl_plan* p) {
   const size_t MH2 = static_cast<size_t>(M) * H * 2;
   if (const char* e = std::getenv("DL_ATTN")) p->attn_tc = std::strcmp(e, "mma_sync") != 0;
   if (const char* e = std::getenv("DL_MEGA_HEAD_EVENTS")) p->head_events = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_DEFER_FIXUP")) p->defer_fixup = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_ATTN_SPLIT_SOFTMAX")) p->split_sm = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_DAG_PROGRAMMATIC_EDGES")) p->dag_prog_edges = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_GEMM_STAGES")) p->gemm_stages_max = std::max(2, std::min(kMaxStages, std::atoi(e)));
@@ -1034,6 +1087,8 @@ static dl_status build_plan(dl_plan* p) {
     p->dag.push_back(lop);
   }
   if (cpos > p->n_counters) return fail(DL_ERR_CUDA, "counter pool overflow");
+  if (p->defer_fixup)
+    for (auto* list : {&p->lin, &p->dag}) defer_fixups(*list);
 
   // the kernels split units with 32-bit arithmetic: units x CTAs < 2^32
   for (const auto* list : {&p->lin, &p->dag})
@@ -1125,12 +1180,17 @@ static dl_status build_plan(dl_plan* p) {
 
   // megakernel
   if (c.modes_mask & (1u << DL_MODE_MEGAKERNEL)) {
+    p->mega = p->lin;
+    for (LaunchOp& op : p->mega) {
+      if (op.args.kind == OP_GEMM && op.args.gemm.epi == EPI_PARTIALS) op.args.gemm.epi = EPI_STORE_BF16;
+      if (op.args.kind == OP_NORM) op.args.norm.part = nullptr;
+    }
     if ((s = build_mega(p)) != DL_OK) return s;
     if ((s = validate_mega(p)) != DL_OK) return s;
     // the worker's ring of equal operand slots (32 KiB of weight tiles or
     // K/V plus the activation slices) and the largest private area
     int slot = 32768, priv = norm_smem_bytes();
-    for (const LaunchOp& op : p->lin) {
+    for (const LaunchOp& op : p->mega) {
       if (op.args.kind == OP_GEMM) {
         const GemmArgs& a = op.args.gemm;
         slot = std::max(slot, 32768 + (a.pair ? 1 : 2) * (((a.Mp * 128 + 1023) / 1024) * 1024));
@@ -1162,7 +1222,7 @@ static dl_status build_plan(dl_plan* p) {
                                                      p->mega_smem));
     if (per_sm < 1) return fail(DL_ERR_PLAN_INVALID, "megakernel worker does not fit on an SM");
     std::vector<OpArgs> h_ops;
-    for (const LaunchOp& op : p->lin) h_ops.push_back(op.args);
+    for (const LaunchOp& op : p->mega) h_ops.push_back(op.args);
     DA(p->d_ops, h_ops.size() * sizeof(OpArgs));
     CK(cudaMemcpy(p->d_ops, h_ops.data(), h_ops.size() * sizeof(OpArgs), cudaMemcpyHostToDevice));
     DA(p->d_queues, p->queues.size() * sizeof(Instr));

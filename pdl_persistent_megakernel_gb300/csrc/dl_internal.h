@@ -87,7 +87,13 @@ enum Epilogue : int {
   EPI_STORE_BF16 = 1, // out[m][n] = bf16(acc)
   EPI_SILU_MUL = 2,   // a = silu(bf16 g) * bf16 u (+ FP8 quant per 128)
   EPI_LOGITS = 3,     // fp32 logits + greedy argmax (lowest index on ties)
+  EPI_PARTIALS = 4,   // no fix-up: every CTA publishes its partial of each
+                      // tile it touches; the next op (a norm) sums them
 };
+
+// Most CTAs whose Stream-K ranges may share one tile of a projection whose
+// fix-up the following norm performs (EPI_PARTIALS).
+constexpr int kMaxPartContrib = 32;
 
 // L2 prefetch of the first weight tiles the next projection's share with a
 // given CTA index will stream (tmap == NULL: none).  Issued by the current
@@ -106,6 +112,12 @@ struct NormArgs {
   float* h_scale;     // FP8: [M, H/128]
   int fp8, M, H, rows_per_cta;
   float eps;
+  // The producing projection's Stream-K partials (EPI_PARTIALS), or NULL:
+  // x[m][n] = bf16(sum over the CTAs whose ranges hold tile n / 128, in CTA
+  // order, of their partial), written to x as well.  Partial slot s holds
+  // [part_mp][128] fp32 at part + s * part_mp * 128.
+  const float* part;
+  int part_U, part_G, part_KB, part_mp;
 };
 
 struct GemmArgs {

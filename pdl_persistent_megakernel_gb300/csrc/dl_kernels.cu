@@ -20,11 +20,12 @@ __device__ __forceinline__ int tmem_cols_pow2(int cols) {
 }
 
 // ------------------------------------------------------------ standalone
+template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_norm(NormArgs a, KernelCtx ctx) {
   extern __shared__ uint8_t smem_raw[];
   Dep dep{};
   dep.mode = 0;
-  norm_op(a, blockIdx.x, dep, ctx, align1024(smem_raw));
+  norm_op<NV>(a, blockIdx.x, dep, ctx, align1024(smem_raw));
 }
 
 template <int kMG, int kMp>
@@ -338,7 +339,12 @@ const void* gemm_kernel(int mma, int m_or_mp) {
   return reinterpret_cast<const void*>(&k_gemm<0, 64>);
 }
 
-const void* norm_kernel() { return reinterpret_cast<const void*>(&k_norm); }
+const void* norm_kernel(int H) {
+  const int nv = ((H >> 3) + 255) >> 8;
+  if (nv <= 1) return reinterpret_cast<const void*>(&k_norm<1>);
+  if (nv <= 2) return reinterpret_cast<const void*>(&k_norm<2>);
+  return reinterpret_cast<const void*>(&k_norm<4>);
+}
 const void* attn_tc_kernel() { return reinterpret_cast<const void*>(&k_attn_tc); }
 
 int attn_tc_smem_bytes(int QRp, int stages) {
@@ -365,7 +371,9 @@ int attn_smem_bytes(int QRp, int stages) {
   return attn_smem_layout(QRp, stages).total + 1024;
 }
 
-int norm_smem_bytes() { return 1024 + 256; }
+// the reduction scratch, the contributor table of a deferred fix-up (up to
+// 64 tiles of 128 columns) and the norm weight (H <= 8192 bf16)
+int norm_smem_bytes() { return 1024 + kNormWOff + 8192 * 2; }
 
 cudaError_t launch_test_kv_write(const void* src, void* kv, const int* bt, const int* pos,
                                  int layer, int M, int T, int Hkv, int d, int P,

@@ -8,7 +8,7 @@
 namespace dl {
 
 const void* gemm_kernel(int mma, int m_or_mp);
-const void* norm_kernel();
+const void* norm_kernel(int H);
 const void* attn_kernel(int QRp);
 const void* attn_tc_kernel();
 int attn_tc_smem_bytes(int QRp, int stages);

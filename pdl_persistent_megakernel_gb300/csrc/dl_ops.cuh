@@ -119,11 +119,84 @@ __device__ __forceinline__ void prefetch_next_share(const PrefetchSpec& pf, int 
   }
 }
 
+__device__ __forceinline__ int sk_contributors(int U, int G, int ts, int len, int* ctb);
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi);
+
 // =================================================================== NORM
 // Residual add + RMSNorm (+ per-token, per-128-group e4m3 quantisation):
 //   r = bf16(x + res);  h = r * rsqrt(mean(r^2) + eps) * w
 // One CTA handles rows [c * rows_per_cta, ...); 256 consumer threads, 16-byte
-// vectors, H <= 8192.
+// vectors, H <= 8192.  With the producing projection's Stream-K partials
+// (a.part), x is first formed here: the partials of the CTAs whose ranges
+// hold each tile, summed in CTA order (the order of the projection's own
+// fix-up) and rounded to bf16; x is written out as well.
+constexpr int kNormTabOff = 256;                    // contributor table [H/128][1 + kMaxPartContrib]
+constexpr int kNormWOff = kNormTabOff + 64 * (1 + kMaxPartContrib) * 4;   // norm weight, bf16 [H]
+
+// x of two of a thread's 8-column vectors (v0, v1; row m), each the bf16 of
+// the CTA-ordered sum of its tile's partials: every contributor of both
+// vectors, up to six per pass, is loaded before any is added (one round
+// trip for the usual five or six contributors of a tile).
+__device__ __forceinline__ void norm_partial_sum2(const NormArgs& a, const int* ptab, int m,
+                                                  int v0, int v1, bool act0, bool act1,
+                                                  uint4& x0, uint4& x1) {
+  constexpr int kB = 6;
+  const int* tb0 = ptab + (v0 >> 4) * (1 + kMaxPartContrib);
+  const int* tb1 = ptab + (v1 >> 4) * (1 + kMaxPartContrib);
+  const int n0 = act0 ? tb0[0] : 0, n1 = act1 ? tb1[0] : 0;
+  const size_t pstride = static_cast<size_t>(a.part_mp) * 128;
+  const size_t r0 = static_cast<size_t>(m) * 128 + ((v0 & 15) << 3);
+  const size_t r1 = static_cast<size_t>(m) * 128 + ((v1 & 15) << 3);
+  float4 s[2][2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int nn = max(n0, n1);
+  for (int k0 = 0; k0 < nn; k0 += kB) {
+    float4 l[2][kB][2];
+#pragma unroll
+    for (int kk = 0; kk < kB; ++kk) {
+      if (k0 + kk < n0) {
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part + static_cast<size_t>(tb0[1 + k0 + kk]) * pstride + r0);
+        l[0][kk][0] = __ldcg(src);
+        l[0][kk][1] = __ldcg(src + 1);
+      }
+      if (k0 + kk < n1) {
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part + static_cast<size_t>(tb1[1 + k0 + kk]) * pstride + r1);
+        l[1][kk][0] = __ldcg(src);
+        l[1][kk][1] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < kB; ++kk) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (k0 + kk < (i == 0 ? n0 : n1)) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (k0 + kk == 0) {
+              s[i][h] = l[i][kk][h];
+            } else {
+              s[i][h].x += l[i][kk][h].x;
+              s[i][h].y += l[i][kk][h].y;
+              s[i][h].z += l[i][kk][h].z;
+              s[i][h].w += l[i][kk][h].w;
+            }
+          }
+        }
+      }
+    }
+  }
+  x0 = make_uint4(pack_bf16(s[0][0].x, s[0][0].y), pack_bf16(s[0][0].z, s[0][0].w),
+                  pack_bf16(s[0][1].x, s[0][1].y), pack_bf16(s[0][1].z, s[0][1].w));
+  x1 = make_uint4(pack_bf16(s[1][0].x, s[1][0].y), pack_bf16(s[1][0].z, s[1][0].w),
+                  pack_bf16(s[1][1].x, s[1][1].y), pack_bf16(s[1][1].z, s[1][1].w));
+}
+
+// NV = 16-byte vectors per thread and row: 1 (H <= 2048), 2 (H <= 4096) or
+// 4 (H <= 8192); the registers a thread holds scale with it.
+template <int NV, bool kPart = true>
 __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
                         const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x;
@@ -135,14 +208,22 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   if (ct == 0) trace_stamp(ctx, c, TR_START);
   float* red = reinterpret_cast<float*>(smem);     // [2][8]
   int* sflag = reinterpret_cast<int*>(smem + 128);
+  int* ptab = reinterpret_cast<int*>(smem + kNormTabOff);
   const int H = a.H, nvec = H >> 3;
-  // the norm weight does not depend on the previous op: load it first
+  // the contributor lists are plain range arithmetic: built before the wait
+  if (kPart && a.part) {
+    for (int t = ct; t < (H >> 7); t += 256)
+      ptab[t * (1 + kMaxPartContrib)] =
+          sk_contributors(a.part_U, a.part_G, t * a.part_KB, a.part_KB, ptab + t * (1 + kMaxPartContrib) + 1);
+    named_bar(1, 256);
+  }
+  // the norm weight does not depend on the previous op: staged in shared
+  // memory (each thread its own vectors) before the wait
   const uint16_t* w = static_cast<const uint16_t*>(a.w);
-  uint4 wv[4];
+  uint4* wsm = reinterpret_cast<uint4*>(smem + kNormWOff);
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    wv[j] = (ct + j * 256 < nvec) ? __ldg(reinterpret_cast<const uint4*>(w + (ct + j * 256) * 8))
-                                  : make_uint4(0, 0, 0, 0);
+  for (int j = 0; j < NV; ++j)
+    if (ct + j * 256 < nvec) wsm[ct + j * 256] = __ldg(reinterpret_cast<const uint4*>(w + (ct + j * 256) * 8));
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag)) return;
   if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
   const Binding* bd = ctx.binding;
@@ -151,19 +232,43 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   uint16_t* rout = resolve<uint16_t>(a.r_out, bd);
   const int m0 = c * a.rows_per_cta;
   const int m1 = min(a.M, m0 + a.rows_per_cta);
+  const uint64_t pol_keep = policy_evict_last();
   for (int m = m0; m < m1; ++m) {
+    // every load of the row goes out before any store (a store to the
+    // residual or x buffer could alias a later load): one round trip
+    uint4 xv[NV], rv[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = ct + j * 256;
+      rv[j] = make_uint4(0, 0, 0, 0);
+      xv[j] = rv[j];
+      if (v < nvec) {
+        const size_t off = static_cast<size_t>(m) * H + v * 8;
+        rv[j] = __ldcg(reinterpret_cast<const uint4*>(res + off));
+        if (!(kPart && a.part)) xv[j] = __ldcg(reinterpret_cast<const uint4*>(x + off));
+      }
+    }
+    if (kPart && a.part) {
+#pragma unroll
+      for (int j = 0; j < NV; j += 2) {
+        const int v0 = ct + j * 256, v1 = v0 + 256;
+        uint4 spare;
+        if (v0 < nvec)
+          norm_partial_sum2(a, ptab, m, v0, v1, true, j + 1 < NV && v1 < nvec, xv[j],
+                            j + 1 < NV ? xv[(j + 1) % NV] : spare);
+      }
+    }
     // r = bf16(x + res), kept as packed bf16 (exact)
-    uint32_t rp[4][4];
+    uint32_t rp[NV][4];
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NV; ++j) {
       const int v = ct + j * 256;
       if (v < nvec) {
         const size_t off = static_cast<size_t>(m) * H + v * 8;
-        const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(x + off));
-        const uint4 rv = __ldcg(reinterpret_cast<const uint4*>(res + off));
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t rs[4] = {rv.x, rv.y, rv.z, rv.w};
+        if (kPart && a.part) *reinterpret_cast<uint4*>(const_cast<uint16_t*>(x) + off) = xv[j];
+        const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float a0 = bfround(bf16_lo(xs[e]) + bf16_lo(rs[e]));
@@ -172,7 +277,10 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
           rp[j][e] = static_cast<uint32_t>(f2bf(a0)) |
                      (static_cast<uint32_t>(f2bf(a1)) << 16);
         }
-        *reinterpret_cast<uint4*>(rout + off) = make_uint4(rp[j][0], rp[j][1], rp[j][2], rp[j][3]);
+        // the new residual is read again by the next norm, after the
+        // projections and the attention have streamed their operands
+        // (evict-first) through L2: kept there with evict-last priority
+        st_global_v4_hint(rout + off, make_uint4(rp[j][0], rp[j][1], rp[j][2], rp[j][3]), pol_keep);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) rp[j][e] = 0u;
@@ -186,12 +294,13 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     for (int i = 0; i < 8; ++i) tot += red[(m & 1) * 8 + i];
     const float inv = rsqrtf(tot / static_cast<float>(H) + a.eps);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NV; ++j) {
       const int v = ct + j * 256;
       const bool act = v < nvec;
       float h[8];
       if (act) {
-        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+        const uint4 wj = wsm[v];
+        const uint32_t ws[4] = {wj.x, wj.y, wj.z, wj.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           h[2 * e] = bf16_lo(rp[j][e]) * inv * bf16_lo(ws[e]);
@@ -275,7 +384,7 @@ __host__ __device__ inline GemmSmem gemm_smem_layout(int npair, int Mp, int stag
   L.epi_off = ((L.sw_off + (fp8 ? 2 * share * 4 : 0)) + 15) & ~15;   // sw [2][share]
   L.bar_off = L.epi_off + (epi == EPI_QKV_ROPE ? M * (8 + 512) + 256 * 4 + 16 : 0);
   L.bar_off = (L.bar_off + 15) & ~15;
-  L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 4) * 8;
+  L.misc_off = L.bar_off + (2 * kMaxStages + 2 * kMaxTmemBufs + 5) * 8;
   // two control areas (flags + contributor list): the fix-up warps' and the
   // epilogue warps' (which finish the last tile themselves)
   L.total = L.misc_off + 2 * (256 + kMaxContrib * 4);
@@ -298,6 +407,7 @@ struct GemmShared {
   uint64_t* tempty;
   uint64_t* tready;  // [2] finished tile buffer b written (4 epilogue warps)
   uint64_t* tfree;   // [2] tile buffer b finished and free (2 fix-up warps)
+  uint64_t* tprep;   // QKV epilogue operands staged (fix-up warps), or NULL
 
   int* flag;      // [4]
   int* ctb;       // [kMaxContrib] contributor list of a fix-up
@@ -308,10 +418,52 @@ struct GemmShared {
 // dst (the first partial) plus `nc` fp32 partials (float4 granular, nel4
 // float4s each) listed in ctb as workspace slot indices, in list order, into
 // dst.  Each thread owns up to 8 float4s per pass and loads them for two
-// contributors at a time, so a pass costs about nc / 2 L2 round trips.
+// contributors at a time, so a pass costs about nc / 2 L2 round trips.  When
+// a thread owns at most 4 float4s and there are more than two partials, it
+// loads four contributors at a time instead (one round trip up to four).
+template <bool kWide>
 __device__ __forceinline__ void ordered_sum4(float4* dst, const float* ws, size_t part,
                                              const int* ctb, int nc, int nel4, int nthr,
                                              int ct) {
+  if (kWide && nc > 2 && nel4 <= 4 * nthr) {
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e4 = ct + q * nthr;
+      acc[q] = e4 < nel4 ? dst[e4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int j = 0; j < nc; j += 4) {
+      float4 v[4][4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float4* src = reinterpret_cast<const float4*>(
+            ws + static_cast<size_t>(ctb[j + jj < nc ? j + jj : j]) * part);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e4 = ct + q * nthr;
+          v[jj][q] = (j + jj < nc && e4 < nel4) ? __ldcg(src + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (j + jj < nc) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[q].x += v[jj][q].x;
+            acc[q].y += v[jj][q].y;
+            acc[q].z += v[jj][q].z;
+            acc[q].w += v[jj][q].w;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e4 = ct + q * nthr;
+      if (e4 < nel4) dst[e4] = acc[q];
+    }
+    return;
+  }
   constexpr int kQ = 8;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int q0 = 0; q0 * nthr < nel4; q0 += kQ) {
@@ -583,12 +735,28 @@ __device__ void epi_logits(const GemmArgs& a, int tg, int tl, const float* tout,
 
 // Finish tile tl (local index; global tg = t_base + tl): Stream-K fix-up,
 // then the epilogue.  tout holds this CTA's sum over its k-blocks.
+// kWide: the four-contributor sum (the megakernel keeps the two-wide one,
+// whose registers its engine functions can spare)
+template <bool kWide>
 __device__ void gemm_finish_tile(const GemmArgs& a, int c, int u0, int tl,
                                  bool full_tile, int npair, int nthr, int ct,
                                  int bar, const KernelCtx& ctx,
                                  const GemmShared& sh) {
   float* tout = sh.tout;
   const int nel = npair * a.Mp * 128;
+  if (a.epi == EPI_PARTIALS) {
+    // no fix-up here: the partial goes to slot 0 when this CTA's range
+    // begins inside the tile, slot 1 when the tile begins inside it (the
+    // slot numbering of sk_contributors); the next op sums the slots
+    const int slot = u0 >= tl * a.KB ? 0 : 1;
+    float4* mine = reinterpret_cast<float4*>(a.ws + static_cast<size_t>(c * 2 + slot) * nel);
+    for (int e4 = ct; e4 < a.M * 32 * npair; e4 += nthr) {
+      const int pp = e4 / (a.M * 32), r4 = e4 - pp * a.M * 32;
+      mine[pp * a.Mp * 32 + r4] = reinterpret_cast<const float4*>(tout)[pp * a.Mp * 32 + r4];
+    }
+    named_bar(bar, nthr);  // tout is reused by the next tile
+    return;
+  }
   if (!full_tile) {
     const int U = a.NT * a.KB;
     const int ts = tl * a.KB;
@@ -616,7 +784,7 @@ __device__ void gemm_finish_tile(const GemmArgs& a, int c, int u0, int tl,
     __threadfence();
     // this CTA's partial (first in CTA order) plus the others' in CTA order:
     // the sum does not depend on which CTA finished when
-    ordered_sum4(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb + 1,
+    ordered_sum4<kWide>(reinterpret_cast<float4*>(tout), a.ws, static_cast<size_t>(nel), sh.ctb + 1,
                  sh.flag[3] - 1, nel / 4, nthr, ct);
     if (ct == 0) trace_stamp(ctx, c, TR_REDUCE);
     named_bar(bar, nthr);
@@ -804,7 +972,7 @@ struct TmemRing {
 //
 // gemm_consume_t is the consumer side (warps 1-8); gemm_op_t wraps it with
 // the standalone kernel's own stages and producer.
-template <int kMG, int kMp>
+template <int kMG, int kMp, bool kWide = true>
 __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
                                const KernelCtx& ctx, const GemmShared& sh,
                                const Pipe& P, const TmemRing& TR) {
@@ -912,7 +1080,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       }
       if (ct == 0 && i == nunits) trace_stamp(ctx, c, TR_LOOP_END);
       if (named_bar_or(1, 256, dead)) return;
-      gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 256, ct, 1, ctx, sh);
+      gemm_finish_tile<kWide>(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 256, ct, 1, ctx, sh);
     }
     if (ct == 0) trace_stamp(ctx, c, TR_END);
   } else {
@@ -923,13 +1091,15 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     // its units and, after a slot's last unit, the slot's release; the
     // epilogue takes the accumulators in unit order.
     if (warp == 1 || warp == 2) {
+      // the share's start: stamped before the dependency wait, like the
+      // other engines' (the wait returns at the dependency release)
+      if (warp == 1 && lane == 0) {
+        trace_stamp(ctx, c, TR_START);
+        trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
+      }
       idle_wait(dep);
       const int w = warp - 1;
       if (lane == 0) {
-        if (w == 0) {
-          trace_stamp(ctx, c, TR_START);
-          trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(nunits));
-        }
         const uint32_t idesc = umma_idesc(kMp, !a.fp8);
         const bool fp8 = a.fp8 != 0;
         const int nslots = (nunits + P.ups - 1) / P.ups;
@@ -997,9 +1167,16 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     const int tile_floats = npair * a.Mp * 128;
     if (warp == 3 || warp == 4) {
       // fix-up warps: the Stream-K fix-up and epilogue of each finished
-      // tile, while the epilogue warps already accumulate the next one
-      idle_wait(dep);
+      // tile, while the epilogue warps already accumulate the next one.
+      // They also stage the QKV epilogue's operands (dependent reads of
+      // step inputs, several round trips), off the epilogue warps' path to
+      // the first unit; the epilogue warps take them before the last tile.
       const int ft = tid - 96;
+      if (a.epi == EPI_QKV_ROPE && sh.tprep) {
+        qkv_epi_prepare(a, 64, ft, 3, ctx, sh);
+        if (ft == 0) mbar_arrive(sh.tprep);
+      }
+      idle_wait(dep);
       int i = 0;
       uint32_t rq = TR.rseq0;
       while (i < nunits) {
@@ -1012,7 +1189,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
         if (aborted(ctx.status)) return;
         GemmShared shb = sh;
         shb.tout = sh.tout + b * tile_floats;
-        gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 64, ft, 3, ctx, shb);
+        gemm_finish_tile<kWide>(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 64, ft, 3, ctx, shb);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.tfree[b]);
         i += run;
@@ -1028,7 +1205,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     const int et = tid - 160;
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    if (a.epi == EPI_QKV_ROPE) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
+    if (a.epi == EPI_QKV_ROPE && !sh.tprep) qkv_epi_prepare(a, 128, et, 2, ctx, sh);
     if (a.fp8) stage_w_scales(a, sh, u0, nunits, 128, et);
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
     if (et == 0) trace_stamp(ctx, c, TR_DEPS);
@@ -1115,12 +1292,13 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
       if (i == nunits) {
         // the last tile: finished here, 128 threads, own control area (the
         // fix-up warps may still be on the previous one)
-        named_bar(2, 128);
+        if (a.epi == EPI_QKV_ROPE && sh.tprep && !warp_wait(sh.tprep, 0, ctx, 24)) dead = true;
+        if (named_bar_or(2, 128, dead)) return;
         GemmShared shl = sh;
         shl.tout = tout;
         shl.flag = sh.flag2;
         shl.ctb = sh.ctb2;
-        gemm_finish_tile(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, shl);
+        gemm_finish_tile<kWide>(a, c, u0, tl, kb0 == 0 && run == a.KB, npair, 128, et, 2, ctx, shl);
         break;
       }
       __syncwarp();
@@ -1152,6 +1330,7 @@ __device__ __forceinline__ GemmShared gemm_shared(const GemmArgs& a, uint8_t* sm
   sh.tempty = sh.tfull + kMaxTmemBufs;
   sh.tready = sh.tempty + kMaxTmemBufs;
   sh.tfree = sh.tready + 2;
+  sh.tprep = sh.tfree + 2;
   sh.flag = reinterpret_cast<int*>(smem + L.misc_off);
   sh.ctb = reinterpret_cast<int*>(smem + L.misc_off + 256);
   sh.flag2 = reinterpret_cast<int*>(smem + L.misc_off + 256 + kMaxContrib * 4);
@@ -1188,6 +1367,7 @@ __device__ void gemm_op_t(const GemmArgs& a, int c, const Dep& dep,
       mbar_init(&sh.tready[b], 4);
       mbar_init(&sh.tfree[b], 2);
     }
+    mbar_init(sh.tprep, 1);
     sh.flag[0] = sh.flag[1] = sh.flag[3] = 0;
     sh.flag[2] = 1;
     fence_barrier_init();
@@ -1590,9 +1770,17 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
     trace_stamp(ctx, c, TR_START);
     trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(u1 - u0));
   }
+  // the positions are step inputs, not the previous kernel's output: staged
+  // before the dependency wait, which then leaves one dependent round trip
+  // (the queries) before the first QK^T
+  int* pos = ctb + kMaxContrib;             // [R T] token positions
+  {
+    const int* gpos = resolve<const int>(a.pos, bd);
+    for (int m = ct; m < a.R * a.T; m += 256) pos[m] = gpos[m];
+  }
+  named_bar(1, 256);
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 34, &flag[2])) return -1;
   if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
-  const int* pos = resolve<const int>(a.pos, bd);
   const uint16_t* qg = static_cast<const uint16_t*>(a.q);
   const uint32_t qs_u32 = smem_u32(qs), ps_u32 = smem_u32(ps);
   const uint32_t idesc_s = umma_idesc(kAttnKeys, true);
@@ -1613,18 +1801,28 @@ __device__ int attn_consume_tc(const AttnArgs& a, int c, const Dep& dep, const K
     const int nvb = (ctxr + kAttnKeys - 1) / kAttnKeys;
     const int n = max(0, min(blk_b, nvb) - blk_a);    // valid blocks of this run
     // this pair's query rows: [d-half][row][128 B], 16-byte chunk c8 of a
-    // row at (c8 ^ (row & 7)) (128-byte swizzle); rows QR..QRp-1 zero
-#pragma unroll 4
-    for (int e = ct; e < QRp * 16; e += 256) {
-      const int rr = e >> 4, ch = e & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (rr < a.QR) {
-        const int t = rr / G, g = rr % G;
-        const size_t src = (static_cast<size_t>(r * a.T + t) * a.Hq + h * G + g) * 128 + ch * 8;
-        v = __ldcg(reinterpret_cast<const uint4*>(qg + src));
+    // row at (c8 ^ (row & 7)) (128-byte swizzle); rows QR..QRp-1 zero.
+    // All of a thread's loads go out before its stores (one round trip).
+    {
+      uint4 qv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = ct + k * 256, rr = e >> 4, ch = e & 15;
+        qv[k] = make_uint4(0, 0, 0, 0);
+        if (e < QRp * 16 && rr < a.QR) {
+          const int t = rr / G, g = rr % G;
+          const size_t src = (static_cast<size_t>(r * a.T + t) * a.Hq + h * G + g) * 128 + ch * 8;
+          qv[k] = __ldcg(reinterpret_cast<const uint4*>(qg + src));
+        }
       }
-      const int hf = ch >> 3, c8 = ch & 7;
-      *reinterpret_cast<uint4*>(qs + hf * QRp * 128 + rr * 128 + ((c8 ^ (rr & 7)) << 4)) = v;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = ct + k * 256, rr = e >> 4, ch = e & 15;
+        if (e < QRp * 16) {
+          const int hf = ch >> 3, c8 = ch & 7;
+          *reinterpret_cast<uint4*>(qs + hf * QRp * 128 + rr * 128 + ((c8 ^ (rr & 7)) << 4)) = qv[k];
+        }
+      }
     }
     for (int rr = ct; rr < QRp; rr += 256) row_pos[rr] = rr < a.QR ? pos[r * a.T + rr / G] : -1;
     fence_proxy_async_shared();    // Q, written by threads, is read by the tensor core
@@ -2815,7 +3013,7 @@ __device__ __noinline__ void mk_gemm_v(const GemmArgs& a_, int c, const Dep& dep
   const GemmShared sh = sh_;
   const Pipe P = P_;
   const TmemRing TR = TR_;
-  gemm_consume_t<kMG, kMp>(a, c, dep, ctx, sh, P, TR);
+  gemm_consume_t<kMG, kMp, false>(a, c, dep, ctx, sh, P, TR);
 }
 
 template <int kNMT>
@@ -2833,7 +3031,9 @@ __device__ __noinline__ void mk_norm(const NormArgs& a_, int c, const Dep& dep_,
   const NormArgs a = a_;
   const Dep dep = dep_;
   const KernelCtx ctx = ctx_;
-  norm_op(a, c, dep, ctx, priv);
+  // one engine for every H (the megakernel's code stays small), without
+  // the deferred fix-up's partial sums (its projections finish their tiles)
+  norm_op<4, false>(a, c, dep, ctx, priv);
 }
 
 __device__ void mk_gemm(const GemmArgs& a, int c, const Dep& dep, const KernelCtx& ctx,
@@ -2843,6 +3043,7 @@ __device__ void mk_gemm(const GemmArgs& a, int c, const Dep& dep, const KernelCt
   sh.tempty = tbars + 4;       // [4]
   sh.tready = tbars + 8;       // [2]
   sh.tfree = tbars + 10;       // [2]
+  sh.tprep = nullptr;          // the epilogue warps stage the QKV operands
   if (!a.mma) {
     if (a.M <= 1)
       mk_gemm_v<1, 0>(a, c, dep, ctx, sh, P, TR);

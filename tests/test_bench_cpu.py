@@ -132,14 +132,14 @@ def test_single_thread_sample_is_bounded():
 
 def test_l2_auto_streams_only_workloads_twice_the_l2():
     """--l2 auto runs steps back to back only when one step reads at least
-    twice the L2 size (the Q8 FP8 layer at M = 16, ctx 8192: 260.7 MB); a
+    1.5 times the L2 size (the Q8 FP8 layer at M = 16, ctx 8192: 260.7 MB); a
     smaller step (the Q0.6B layer at batch 1: 35.7 MB) gets the clean flush.
     Nothing is allocated before the first call."""
     import bench
     from pdl_persistent_megakernel_gb300 import bytes_model, synth
     big = bytes_model.algorithmic_bytes(synth.CONFIGS["q8_layer_m16_ctx8192_fp8"])["total"]
     small = bytes_model.algorithmic_bytes(synth.CONFIGS["q06_layer_b1_ctx1024"])["total"]
-    assert big >= 2 * 129e6 > small
+    assert big >= 1.5 * 132.2e6 > small
     f = bench.L2Flush("auto", "cpu", big)
     assert f.mode == "stream" and f.w is None
     f()
@@ -148,4 +148,4 @@ def test_l2_auto_streams_only_workloads_twice_the_l2():
     assert g.mode == "clean" and g.w is None
     assert bench.L2Flush("auto", "cpu").mode == "clean"
     assert bench.L2Flush("flush", "cpu", big).mode == "flush"
-    assert "twice" in f.describe() and "read of another buffer" in g.describe()
+    assert "1.5 times" in f.describe() and "read of another buffer" in g.describe()
