@@ -82,6 +82,7 @@ struct LaunchOp {
   int grid = 0;
   int smem = 0;
   int branch = 0;  // 0 main chain, 1 side branch (DAG lists)
+  int cluster = 1; // thread-block cluster size along x (the split norm)
   std::string name;
 };
 
@@ -131,6 +132,8 @@ struct dl_plan {
   // a projection whose output only feeds the next norm leaves its Stream-K
   // fix-up to that norm (EPI_PARTIALS)
   bool defer_fixup = true;
+  // add + RMSNorm rows split over clusters of up to this many CTAs (1, 2, 4)
+  int norm_split = 4;
   unsigned long long budget_ns = 1000000000ull;
 
   std::vector<void*> allocs;
@@ -251,8 +254,18 @@ static LaunchOp make_norm(dl_plan* p, DPtr x, DPtr res, DPtr rout, const void* w
   a.H = p->H;
   a.rows_per_cta = 1;
   a.eps = p->cfg.eps;
-  op.kernel = norm_kernel(p->H);
-  op.grid = p->M;
+  // a row over a cluster of 4 (or 2) CTAs: a part is a whole number of
+  // 128-column quantisation groups and tiles, and all rows' clusters fit in
+  // one wave (the megakernel runs one share per worker)
+  int split = 1;
+  for (int k : {4, 2})
+    if (split == 1 && k <= p->norm_split && p->H % (k * 128) == 0 && p->H / k <= 2048 &&
+        p->M * k <= p->sms)
+      split = k;
+  op.kernel = norm_kernel(p->H, split);
+  op.grid = p->M * split;
+  op.cluster = split;
+  a.split = split;
   op.smem = norm_smem_bytes();
   op.name = name;
   return op;
@@ -463,17 +476,24 @@ static cudaError_t launch_op(const dl_plan* p, const LaunchOp& op, cudaStream_t 
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = op.smem;
   lc.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   lc.attrs = attr;
   lc.numAttrs = 1;
   if (prog_event) {
-    attr[1].id = cudaLaunchAttributeProgrammaticEvent;
-    attr[1].val.programmaticEvent.event = prog_event;
-    attr[1].val.programmaticEvent.flags = 0;
-    attr[1].val.programmaticEvent.triggerAtBlockStart = 0;
-    lc.numAttrs = 2;
+    attr[lc.numAttrs].id = cudaLaunchAttributeProgrammaticEvent;
+    attr[lc.numAttrs].val.programmaticEvent.event = prog_event;
+    attr[lc.numAttrs].val.programmaticEvent.flags = 0;
+    attr[lc.numAttrs].val.programmaticEvent.triggerAtBlockStart = 0;
+    ++lc.numAttrs;
+  }
+  if (op.cluster > 1) {
+    attr[lc.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[lc.numAttrs].val.clusterDim.x = static_cast<unsigned>(op.cluster);
+    attr[lc.numAttrs].val.clusterDim.y = 1;
+    attr[lc.numAttrs].val.clusterDim.z = 1;
+    ++lc.numAttrs;
   }
   KernelCtx ctx = make_ctx(p, op_id);
   switch (op.args.kind) {
@@ -987,6 +1007,7 @@ static dl_status build_plan(dl_plan* p) {
   if (const char* e = std::getenv("DL_ATTN")) p->attn_tc = std::strcmp(e, "mma_sync") != 0;
   if (const char* e = std::getenv("DL_MEGA_HEAD_EVENTS")) p->head_events = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_DEFER_FIXUP")) p->defer_fixup = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_NORM_SPLIT")) p->norm_split = std::max(1, std::min(4, std::atoi(e)));
   if (const char* e = std::getenv("DL_ATTN_SPLIT_SOFTMAX")) p->split_sm = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_DAG_PROGRAMMATIC_EDGES")) p->dag_prog_edges = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_GEMM_STAGES")) p->gemm_stages_max = std::max(2, std::min(kMaxStages, std::atoi(e)));
@@ -1183,7 +1204,7 @@ static dl_status build_plan(dl_plan* p) {
     p->mega = p->lin;
     for (LaunchOp& op : p->mega) {
       if (op.args.kind == OP_GEMM && op.args.gemm.epi == EPI_PARTIALS) op.args.gemm.epi = EPI_STORE_BF16;
-      if (op.args.kind == OP_NORM) op.args.norm.part = nullptr;
+      if (op.args.kind == OP_NORM) op.args.norm.part = nullptr;   // (split rows: see NormArgs)
     }
     if ((s = build_mega(p)) != DL_OK) return s;
     if ((s = validate_mega(p)) != DL_OK) return s;

@@ -118,6 +118,10 @@ struct NormArgs {
   // [part_mp][128] fp32 at part + s * part_mp * 128.
   const float* part;
   int part_U, part_G, part_KB, part_mp;
+  // CTAs (shares) per row: a cluster of `split` CTAs each norms a part of
+  // the row; in the megakernel share c % split == 0 norms the whole row
+  // c / split and the others only pass the dependency
+  int split;
 };
 
 struct GemmArgs {

@@ -20,12 +20,13 @@ __device__ __forceinline__ int tmem_cols_pow2(int cols) {
 }
 
 // ------------------------------------------------------------ standalone
-template <int NV>
+// kS > 1: launched in clusters of kS CTAs, one row per cluster
+template <int NV, int kS>
 __global__ void __launch_bounds__(kThreads, 1) k_norm(NormArgs a, KernelCtx ctx) {
   extern __shared__ uint8_t smem_raw[];
   Dep dep{};
   dep.mode = 0;
-  norm_op<NV>(a, blockIdx.x, dep, ctx, align1024(smem_raw));
+  norm_op<NV, true, kS>(a, blockIdx.x, dep, ctx, align1024(smem_raw));
 }
 
 template <int kMG, int kMp>
@@ -339,11 +340,14 @@ const void* gemm_kernel(int mma, int m_or_mp) {
   return reinterpret_cast<const void*>(&k_gemm<0, 64>);
 }
 
-const void* norm_kernel(int H) {
-  const int nv = ((H >> 3) + 255) >> 8;
-  if (nv <= 1) return reinterpret_cast<const void*>(&k_norm<1>);
-  if (nv <= 2) return reinterpret_cast<const void*>(&k_norm<2>);
-  return reinterpret_cast<const void*>(&k_norm<4>);
+const void* norm_kernel(int H, int split) {
+  const int nv = ((H >> 3) / split + 255) >> 8;
+  if (split == 4) return nv <= 1 ? reinterpret_cast<const void*>(&k_norm<1, 4>) : nullptr;
+  if (split == 2) return nv <= 1 ? reinterpret_cast<const void*>(&k_norm<1, 2>) : nullptr;
+  if (split != 1) return nullptr;
+  if (nv <= 1) return reinterpret_cast<const void*>(&k_norm<1, 1>);
+  if (nv <= 2) return reinterpret_cast<const void*>(&k_norm<2, 1>);
+  return reinterpret_cast<const void*>(&k_norm<4, 1>);
 }
 const void* attn_tc_kernel() { return reinterpret_cast<const void*>(&k_attn_tc); }
 

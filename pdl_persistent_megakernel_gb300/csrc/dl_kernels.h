@@ -8,7 +8,9 @@
 namespace dl {
 
 const void* gemm_kernel(int mma, int m_or_mp);
-const void* norm_kernel(int H);
+// The add + RMSNorm kernel for rows of H columns, each row split over a
+// cluster of `split` CTAs (1, 2 or 4); NULL for an unsupported pair.
+const void* norm_kernel(int H, int split);
 const void* attn_kernel(int QRp);
 const void* attn_tc_kernel();
 int attn_tc_smem_bytes(int QRp, int stages);

@@ -194,25 +194,49 @@ __device__ __forceinline__ void norm_partial_sum2(const NormArgs& a, const int* 
                   pack_bf16(s[1][1].x, s[1][1].y), pack_bf16(s[1][1].z, s[1][1].w));
 }
 
-// NV = 16-byte vectors per thread and row: 1 (H <= 2048), 2 (H <= 4096) or
-// 4 (H <= 8192); the registers a thread holds scale with it.
-template <int NV, bool kPart = true>
+// NV = 16-byte vectors per thread and row part: 1 (up to 2048 columns), 2
+// (4096) or 4 (8192); the registers a thread holds scale with it.
+// kS > 1: a row is split over a cluster of kS CTAs (CTA c: row c / kS,
+// columns of part c % kS = its cluster rank), which add their sums of
+// squares through distributed shared memory.  The partial sums of a
+// deferred fix-up then spread over kS SMs: one SM keeps only so many loads
+// in flight, and a whole row's partials (about 100 KB at H = 4096) took it
+// several microseconds.
+template <int NV, bool kPart = true, int kS = 1>
 __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
                         const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x;
+  float* csum = reinterpret_cast<float*>(smem + 160);   // this CTA's sum of squares
   if (tid < 32) {
     idle_wait(dep);
+    if constexpr (kS > 1) {
+      cluster_sync_all();   // the consumers' two cluster barriers
+      cluster_sync_all();
+    }
     return;
   }
   const int ct = tid - 32, lane = tid & 31, wc = ct >> 5;
   if (ct == 0) trace_stamp(ctx, c, TR_START);
+  const int split = a.split > 1 ? a.split : 1;
+  if (kS == 1 && c % split != 0) {
+    // megakernel, a split row: the share of part 0 norms it whole
+    if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, reinterpret_cast<int*>(smem + 128))) return;
+    if (ct == 0) {
+      trace_stamp(ctx, c, TR_DEPS);
+      trace_put(ctx, c, TR_UNITS, 0ull);
+      trace_stamp(ctx, c, TR_END);
+    }
+    return;
+  }
   float* red = reinterpret_cast<float*>(smem);     // [2][8]
   int* sflag = reinterpret_cast<int*>(smem + 128);
   int* ptab = reinterpret_cast<int*>(smem + kNormTabOff);
-  const int H = a.H, nvec = H >> 3;
+  const int H = a.H;
+  // this CTA's vectors of 8 columns: [vb, vb + nvec)
+  const int nvec = (H >> 3) / kS, vb = (kS > 1 ? c % kS : 0) * nvec;
   // the contributor lists are plain range arithmetic: built before the wait
   if (kPart && a.part) {
-    for (int t = ct; t < (H >> 7); t += 256)
+    for (int t = (vb >> 4) + ct; t < ((vb + nvec) >> 4); t += 256)
       ptab[t * (1 + kMaxPartContrib)] =
           sk_contributors(a.part_U, a.part_G, t * a.part_KB, a.part_KB, ptab + t * (1 + kMaxPartContrib) + 1);
     named_bar(1, 256);
@@ -223,14 +247,15 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   uint4* wsm = reinterpret_cast<uint4*>(smem + kNormWOff);
 #pragma unroll
   for (int j = 0; j < NV; ++j)
-    if (ct + j * 256 < nvec) wsm[ct + j * 256] = __ldg(reinterpret_cast<const uint4*>(w + (ct + j * 256) * 8));
+    if (ct + j * 256 < nvec)
+      wsm[vb + ct + j * 256] = __ldg(reinterpret_cast<const uint4*>(w + (vb + ct + j * 256) * 8));
   if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag)) return;
   if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
   const Binding* bd = ctx.binding;
   const uint16_t* x = resolve<const uint16_t>(a.x, bd);
   const uint16_t* res = resolve<const uint16_t>(a.res, bd);
   uint16_t* rout = resolve<uint16_t>(a.r_out, bd);
-  const int m0 = c * a.rows_per_cta;
+  const int m0 = (c / split) * a.rows_per_cta;
   const int m1 = min(a.M, m0 + a.rows_per_cta);
   const uint64_t pol_keep = policy_evict_last();
   for (int m = m0; m < m1; ++m) {
@@ -239,10 +264,10 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     uint4 xv[NV], rv[NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int v = ct + j * 256;
+      const int vl = ct + j * 256, v = vb + vl;
       rv[j] = make_uint4(0, 0, 0, 0);
       xv[j] = rv[j];
-      if (v < nvec) {
+      if (vl < nvec) {
         const size_t off = static_cast<size_t>(m) * H + v * 8;
         rv[j] = __ldcg(reinterpret_cast<const uint4*>(res + off));
         if (!(kPart && a.part)) xv[j] = __ldcg(reinterpret_cast<const uint4*>(x + off));
@@ -251,10 +276,10 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     if (kPart && a.part) {
 #pragma unroll
       for (int j = 0; j < NV; j += 2) {
-        const int v0 = ct + j * 256, v1 = v0 + 256;
+        const int vl0 = ct + j * 256, v0 = vb + vl0, v1 = v0 + 256;
         uint4 spare;
-        if (v0 < nvec)
-          norm_partial_sum2(a, ptab, m, v0, v1, true, j + 1 < NV && v1 < nvec, xv[j],
+        if (vl0 < nvec)
+          norm_partial_sum2(a, ptab, m, v0, v1, true, j + 1 < NV && vl0 + 256 < nvec, xv[j],
                             j + 1 < NV ? xv[(j + 1) % NV] : spare);
       }
     }
@@ -263,8 +288,8 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int v = ct + j * 256;
-      if (v < nvec) {
+      const int vl = ct + j * 256, v = vb + vl;
+      if (vl < nvec) {
         const size_t off = static_cast<size_t>(m) * H + v * 8;
         if (kPart && a.part) *reinterpret_cast<uint4*>(const_cast<uint16_t*>(x) + off) = xv[j];
         const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
@@ -292,11 +317,24 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) tot += red[(m & 1) * 8 + i];
+    if constexpr (kS > 1) {
+      // the row's sum of squares: the cluster's parts, in rank order
+      if (ct == 0) *csum = tot;
+      cluster_sync_all();
+      if (aborted(ctx.status)) {
+        cluster_sync_all();
+        return;
+      }
+      tot = 0.f;
+#pragma unroll
+      for (int r = 0; r < kS; ++r) tot += ld_dsmem_f32(cluster_map(smem_u32(csum), static_cast<uint32_t>(r)));
+      cluster_sync_all();   // no CTA leaves while another still reads its part
+    }
     const float inv = rsqrtf(tot / static_cast<float>(H) + a.eps);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      const int v = ct + j * 256;
-      const bool act = v < nvec;
+      const int vl = ct + j * 256, v = vb + vl;
+      const bool act = vl < nvec;
       float h[8];
       if (act) {
         const uint4 wj = wsm[v];
@@ -343,7 +381,7 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     }
   }
   if (ct == 0) {
-    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(m1 > m0 ? m1 - m0 : 0));
+    trace_put(ctx, c, TR_UNITS, static_cast<unsigned long long>(c % split == 0 && m1 > m0 ? m1 - m0 : 0));
     trace_stamp(ctx, c, TR_END);
   }
 }
