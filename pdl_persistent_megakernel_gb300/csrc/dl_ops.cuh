@@ -879,15 +879,37 @@ __device__ __forceinline__ void unpack_e4m3x16(const uint4& v, float* f) {
 // Activation scales [M][KB] -> shared [KB][Mp] (zero for padding tokens):
 // an epilogue reads the Mp scales of one k-block as contiguous vectors.
 __device__ __forceinline__ void stage_x_scales(const GemmArgs& a, const GemmShared& sh,
-                                               int nthr, int ct, int bar) {
+                                               int nthr, int ct, int bar, int u0, int nunits) {
   const int M = a.M, KB = a.KB, Mp = a.Mp;
-  for (int e = ct; e < M * KB; e += nthr) {
-    const int m = e / KB, kb = e - m * KB;
-    sh.sx[kb * Mp + m] = __ldcg(a.x_scale + e);
-  }
-  for (int e = ct; e < (Mp - M) * KB; e += nthr) {
-    const int m = M + e / KB, kb = e % KB;
-    sh.sx[kb * Mp + m] = 0.f;
+  if (nunits >= KB) {
+    for (int e = ct; e < M * KB; e += nthr) {
+      const int m = e / KB, kb = e - m * KB;
+      sh.sx[kb * Mp + m] = __ldcg(a.x_scale + e);
+    }
+    for (int e = ct; e < (Mp - M) * KB; e += nthr) {
+      const int m = M + e / KB, kb = e % KB;
+      sh.sx[kb * Mp + m] = 0.f;
+    }
+  } else {
+    // only the k-blocks of this share's units (a share shorter than a tile
+    // touches at most nunits of them), every load of a pass before its
+    // stores: the staging sits between the dependency release and the
+    // first unit's promotion (down projection: 96 k-blocks, about 20 used)
+    for (int e0 = ct; e0 < nunits * Mp; e0 += 4 * nthr) {
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q * nthr;
+        const int i = e / Mp, m = e - i * Mp;
+        v[q] = (e < nunits * Mp && m < M) ? __ldcg(a.x_scale + m * KB + (u0 + i) % KB) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q * nthr;
+        const int i = e / Mp, m = e - i * Mp;
+        if (e < nunits * Mp) sh.sx[((u0 + i) % KB) * Mp + m] = v[q];
+      }
+    }
   }
   named_bar(bar, nthr);
 }
@@ -1034,7 +1056,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     if (a.fp8) stage_w_scales(a, sh, u0, nunits, 256, ct);
     if (!group_wait(dep, ctx, 1, 256, ct == 0, 12, &sh.flag[2])) return;
     if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
-    if (a.fp8) stage_x_scales(a, sh, 256, ct, 1);
+    if (a.fp8) stage_x_scales(a, sh, 256, ct, 1, u0, nunits);
     const int c8 = ct & 7, r0 = ct >> 3;
     bool dead = false;
     int i = 0;
@@ -1247,7 +1269,7 @@ __device__ void gemm_consume_t(const GemmArgs& a, int c, const Dep& dep,
     if (a.fp8) stage_w_scales(a, sh, u0, nunits, 128, et);
     if (!group_wait(dep, ctx, 2, 128, et == 0, 16, &sh.flag[2])) return;
     if (et == 0) trace_stamp(ctx, c, TR_DEPS);
-    if (a.fp8) stage_x_scales(a, sh, 128, et, 2);
+    if (a.fp8) stage_x_scales(a, sh, 128, et, 2, u0, nunits);
     // loop invariants in registers (the arguments may sit in memory that
     // every asm memory clobber below would make the compiler read again)
     const bool fp8 = a.fp8 != 0;
