@@ -186,6 +186,7 @@ struct AttnArgs {
   int G;                      // CTAs
   int stages;
   int max_ctx;                // positions must lie in [0, max_ctx) (else DERR_BOUNDS)
+  int pre_stages;             // > 0: K/V blocks loaded before the dependency wait, at most
   int split_sm;               // tcgen05 engine: split softmax up to 32 query rows
   float scale_log2;           // log2(e) / sqrt(d)
   float* ws;                  // partials [G][2][QRp][d] + lse [G][2][QRp]

@@ -2790,7 +2790,7 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
           }
           uint8_t* st = stage0 + s * L.stage_bytes;
           const int nk = min(kAttnKeys, ctxr - k0);
-          if (!deps_ok && k0 + nk > ppos[r * a.T]) {
+          if (!deps_ok && (k0 + nk > ppos[r * a.T] || (a.pre_stages > 0 && i >= a.pre_stages))) {
             deps_ok = true;
             if (dep.mode == 0) {
               gdc_wait();
