@@ -194,11 +194,45 @@ __device__ __forceinline__ void norm_partial_sum2(const NormArgs& a, const int* 
                   pack_bf16(s[1][1].x, s[1][1].y), pack_bf16(s[1][1].z, s[1][1].w));
 }
 
+// The row's sum of squares over a cluster of kS CTAs: thread ct 0 pushes
+// this CTA's part `v` into slot [rank] of every cluster CTA (st.async,
+// completing as transaction bytes on that CTA's exchange barrier), then
+// every thread waits for its own barrier and adds the kS slots in rank
+// order.  One round trip, against two cluster barriers and a remote load.
+// Every CTA of the cluster calls this once per launch (an aborted one with
+// v = 0), and none exits before the peers' pushes into it have landed, so
+// the wait ignores the abort flag; it is bounded by the budget all the same.
+template <int kS>
+__device__ __forceinline__ float cluster_row_sum(float v, float* xsum, uint64_t* xbar, int ct,
+                                                 int rank, const KernelCtx& ctx) {
+  cluster_wait();   // every exchange barrier of the cluster is initialised
+  if (ct == 0) {
+    mbar_arrive_expect_tx(xbar, kS * 4);
+    const uint32_t slot = smem_u32(xsum + rank), bar = smem_u32(xbar);
+#pragma unroll
+    for (int r = 0; r < kS; ++r)
+      st_async_f32(cluster_map(slot, static_cast<uint32_t>(r)), v,
+                   cluster_map(bar, static_cast<uint32_t>(r)));
+  }
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait<true>(xbar, 0)) {
+    if (globaltimer() - t0 > ctx.budget_ns) {
+      if (ct == 0) report_error(ctx.status, DERR_TIMEOUT, ctx.op_id, blockIdx.x, 40, 0);
+      break;
+    }
+  }
+  float tot = 0.f;
+#pragma unroll
+  for (int r = 0; r < kS; ++r) tot += xsum[r];
+  return tot;
+}
+
 // NV = 16-byte vectors per thread and row part: 1 (up to 2048 columns), 2
 // (4096) or 4 (8192); the registers a thread holds scale with it.
 // kS > 1: a row is split over a cluster of kS CTAs (CTA c: row c / kS,
 // columns of part c % kS = its cluster rank), which add their sums of
-// squares through distributed shared memory.  The partial sums of a
+// squares through distributed shared memory (cluster_row_sum; one row per
+// CTA, the launch shape the host gives a split norm).  The partial sums of a
 // deferred fix-up then spread over kS SMs: one SM keeps only so many loads
 // in flight, and a whole row's partials (about 100 KB at H = 4096) took it
 // several microseconds.
@@ -206,13 +240,20 @@ template <int NV, bool kPart = true, int kS = 1>
 __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
                         const KernelCtx& ctx, uint8_t* smem) {
   const int tid = threadIdx.x;
-  float* csum = reinterpret_cast<float*>(smem + 160);   // this CTA's sum of squares
-  if (tid < 32) {
-    idle_wait(dep);
-    if constexpr (kS > 1) {
-      cluster_sync_all();   // the consumers' two cluster barriers
-      cluster_sync_all();
+  float* xsum = reinterpret_cast<float*>(smem + 160);      // [kS] the cluster's sums of squares
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + 192);   // their exchange barrier
+  if constexpr (kS > 1) {
+    // the exchange barrier is initialised before this CTA's threads arrive
+    // on the cluster barrier, which every peer waits on before its push
+    if (tid == 32) {
+      mbar_init(xbar, 1);
+      fence_barrier_init();
     }
+    cluster_arrive();
+  }
+  if (tid < 32) {
+    if constexpr (kS > 1) cluster_wait();
+    idle_wait(dep);
     return;
   }
   const int ct = tid - 32, lane = tid & 31, wc = ct >> 5;
@@ -249,14 +290,21 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
   for (int j = 0; j < NV; ++j)
     if (ct + j * 256 < nvec)
       wsm[vb + ct + j * 256] = __ldg(reinterpret_cast<const uint4*>(w + (vb + ct + j * 256) * 8));
-  if (!group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag)) return;
+  bool live = group_wait(dep, ctx, 1, 256, ct == 0, 1, sflag);
+  // under griddepcontrol each thread read the abort flag itself: one
+  // verdict for the CTA, so that no thread is left at a barrier
+  if (dep.mode == 0) live = !named_bar_or(1, 256, !live);
+  if (!live) {
+    if constexpr (kS > 1) cluster_row_sum<kS>(0.f, xsum, xbar, ct, c % kS, ctx);
+    return;
+  }
   if (ct == 0) trace_stamp(ctx, c, TR_DEPS);
   const Binding* bd = ctx.binding;
   const uint16_t* x = resolve<const uint16_t>(a.x, bd);
   const uint16_t* res = resolve<const uint16_t>(a.res, bd);
   uint16_t* rout = resolve<uint16_t>(a.r_out, bd);
   const int m0 = (c / split) * a.rows_per_cta;
-  const int m1 = min(a.M, m0 + a.rows_per_cta);
+  const int m1 = min(a.M, m0 + (kS > 1 ? 1 : a.rows_per_cta));
   const uint64_t pol_keep = policy_evict_last();
   for (int m = m0; m < m1; ++m) {
     // every load of the row goes out before any store (a store to the
@@ -317,19 +365,8 @@ __device__ void norm_op(const NormArgs& a, int c, const Dep& dep,
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) tot += red[(m & 1) * 8 + i];
-    if constexpr (kS > 1) {
-      // the row's sum of squares: the cluster's parts, in rank order
-      if (ct == 0) *csum = tot;
-      cluster_sync_all();
-      if (aborted(ctx.status)) {
-        cluster_sync_all();
-        return;
-      }
-      tot = 0.f;
-#pragma unroll
-      for (int r = 0; r < kS; ++r) tot += ld_dsmem_f32(cluster_map(smem_u32(csum), static_cast<uint32_t>(r)));
-      cluster_sync_all();   // no CTA leaves while another still reads its part
-    }
+    // the row's sum of squares: the cluster's parts, in rank order
+    if constexpr (kS > 1) tot = cluster_row_sum<kS>(tot, xsum, xbar, ct, c % kS, ctx);
     const float inv = rsqrtf(tot / static_cast<float>(H) + a.eps);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
