@@ -138,6 +138,8 @@ struct dl_plan {
   // M = 16, context 8192: the early loads compete with the QKV projection
   // still streaming its weights.
   int attn_pre_stages = 3;
+  // the tcgen05 attention loads a 64-key block as one 4-D TMA box
+  bool attn_kv4 = true;
   // add + RMSNorm rows split over clusters of up to this many CTAs (1, 2, 4)
   int norm_split = 4;
   unsigned long long budget_ns = 1000000000ull;
@@ -422,6 +424,7 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.NB = (p->cfg.max_context + kAttnKeys - 1) / kAttnKeys;
   a.max_ctx = p->cfg.max_context;
   a.pre_stages = p->attn_pre_stages;
+  a.kv4 = p->attn_tc && p->attn_kv4 && p->P % kAttnKeys == 0 && p->d == 128 ? 1 : 0;
   a.split_sm = p->split_sm ? 1 : 0;
   a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms);
   // stages of 32 KiB: the tcgen05 engine holds a block from its arrival to
@@ -1014,6 +1017,7 @@ static dl_status build_plan(dl_plan* p) {
   if (const char* e = std::getenv("DL_ATTN")) p->attn_tc = std::strcmp(e, "mma_sync") != 0;
   if (const char* e = std::getenv("DL_MEGA_HEAD_EVENTS")) p->head_events = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_DEFER_FIXUP")) p->defer_fixup = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_ATTN_KV4")) p->attn_kv4 = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_ATTN_PRE_STAGES")) p->attn_pre_stages = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("DL_NORM_SPLIT")) p->norm_split = std::max(1, std::min(4, std::atoi(e)));
   if (const char* e = std::getenv("DL_ATTN_SPLIT_SOFTMAX")) p->split_sm = std::atoi(e) != 0;
@@ -1305,6 +1309,19 @@ static dl_status bind(dl_plan* p, Binding& b, cudaStream_t s) {
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return fail(DL_ERR_INVALID_ARG, "kv_pages cannot be described by a TMA descriptor");
+  if (p->attn_tc && p->attn_kv4 && p->P % kAttnKeys == 0 && p->d == 128) {
+    // [K/V][d-half][rows][64 elements]: strides one row, 128 bytes, and
+    // kv_heads * page_size rows (V of a slot lies that far after its K)
+    const uint64_t row_b = static_cast<uint64_t>(p->d) * 2;
+    cuuint64_t dims4[4] = {64, rows, 2, 2};
+    cuuint64_t strides4[3] = {row_b, 128, static_cast<cuuint64_t>(p->Hkv) * p->P * row_b};
+    cuuint32_t boxd4[4] = {64, static_cast<cuuint32_t>(kAttnKeys), 2, 2};
+    cuuint32_t estr4[4] = {1, 1, 1, 1};
+    if (g_encode(&b.kv_map4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, b.p[SLOT_KV], dims4, strides4,
+                 boxd4, estr4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return fail(DL_ERR_INVALID_ARG, "kv_pages cannot be described by a 4-D TMA descriptor");
+  }
   CK(launch_bind(p->d_binding, b, s));
   p->last = b;
   p->have_last = true;

@@ -47,6 +47,12 @@ struct alignas(128) Binding {
   // (rows = layers * pages * 2 * kv_heads * page_size), 128-byte swizzle,
   // boxes of 64 head-dim elements by min(page_size, 64) rows.
   CUtensorMap kv_map;
+  // The same cache as [K/V][d-half][rows][64] (strides: kv_heads *
+  // page_size rows, 128 bytes, one row), one box = a whole 64-key block:
+  // K low, K high, V low, V high halves of 64 rows each, the stage layout of
+  // the tcgen05 attention.  Set when page_size is a multiple of 64 and
+  // head_dim = 128 (AttnArgs::kv4); zero otherwise.
+  CUtensorMap kv_map4;
 };
 
 // A pointer operand: a fixed plan-owned address, or (slot >= 0) a binding
@@ -187,6 +193,7 @@ struct AttnArgs {
   int stages;
   int max_ctx;                // positions must lie in [0, max_ctx) (else DERR_BOUNDS)
   int pre_stages;             // > 0: K/V blocks loaded before the dependency wait, at most
+  int kv4;                    // 1: a block is one TMA box of Binding::kv_map4
   int split_sm;               // tcgen05 engine: split softmax up to 32 query rows
   float scale_log2;           // log2(e) / sqrt(d)
   float* ws;                  // partials [G][2][QRp][d] + lse [G][2][QRp]

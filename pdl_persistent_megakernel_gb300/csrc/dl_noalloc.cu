@@ -35,16 +35,16 @@ using namespace dl;
 
 namespace {
 
-// 8 MiB: a 256-byte binding slot, a 256-byte status slot, up to 4096
+// 8 MiB: a 512-byte binding slot, a 256-byte status slot, up to 4096
 // arrival counters, then the partials (G CTAs x 2 slots x QRp rows x 129
 // floats: 128 output dims + the row's log-sum-exp).  At 152 CTAs that holds
 // every query-row padding up to 32; 64-row groups need num_sms <= 126.
 constexpr size_t kScratchBytes = 8u << 20;
 constexpr size_t kBindingOff = 0;
-constexpr size_t kStatusOff = 256;
-constexpr size_t kCounterOff = 512;
+constexpr size_t kStatusOff = 512;
+constexpr size_t kCounterOff = 768;
 constexpr int kMaxPairs = 4096;
-constexpr size_t kPartialOff = kCounterOff + kMaxPairs * sizeof(unsigned);  // 16896
+constexpr size_t kPartialOff = kCounterOff + kMaxPairs * sizeof(unsigned);  // 17152
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kBudgetNs = 1000000000ull;
 

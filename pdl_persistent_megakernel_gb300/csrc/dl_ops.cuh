@@ -2776,9 +2776,14 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
     // and block table are step inputs.  Lane 0 waits at the first block that
     // holds a new key.
     bool ok = true, deps_ok = false;
+    const CUtensorMap* kvm4 = &bd->kv_map4;
     if (lane == 0) {
       fence_tmap_acquire(kvm);
       prefetch_tmap(kvm);
+      if (a.kv4) {
+        fence_tmap_acquire(kvm4);
+        prefetch_tmap(kvm4);
+      }
     }
     const int* pos = resolve<const int>(a.pos, bd);
     const int* bt = resolve<const int>(a.bt, bd);
@@ -2839,6 +2844,19 @@ __device__ void attn_op_t(const AttnArgs& a, int c, const Dep& dep,
           }
           const int nbox = (nk + box - 1) / box;     // boxes that hold valid keys
           mbar_arrive_expect_tx(&full[s], nbox * box * 128 * 4);
+          if (a.kv4) {
+            // the whole block in one box: a page holds all 64 keys (one
+            // instruction where four took the issuing thread about 0.9 us)
+            int page = pgbuf[j * 4];
+            if (page < 0 || page >= a.num_pages) {
+              report_error(ctx.status, DERR_BOUNDS, ctx.op_id, blockIdx.x, 32, k0 / a.P);
+              page = 0;
+            }
+            const int rk = static_cast<int>(kv_row(a.layer, a.num_pages, a.Hkv, a.P, page, 0, h, k0 % a.P));
+            tma_load_4d(st, kvm4, &full[s], 0, rk, 0, 0, pol);
+            ++i;
+            continue;
+          }
           for (int q = 0; q < nbox; ++q) {
             const int key = k0 + q * box;
             int page = pgbuf[j * 4 + q];

@@ -188,7 +188,7 @@ def test_noalloc_rejects_oversized_scratch_then_runs():
     blocks = -(-cfg.context // 64)
     pairs = cfg.num_requests * cfg.n_kv_heads
     G = min(sms, pairs * blocks, 62 * pairs)
-    need = 16896 + G * 2 * 64 * 129 * 4
+    need = 17152 + G * 2 * 64 * 129 * 4
     if need > SCRATCH_BYTES:
         inp = {k: v.to(DEV) for k, v in synth.make_inputs(cfg).items()}
         QD = cfg.n_q_heads * cfg.head_dim
