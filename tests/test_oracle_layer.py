@@ -4,7 +4,8 @@ The parts are pinned in test_oracle_ops.py.  Here special cases reduce the
 layer to closed forms (zero projections, identity projections) so that a
 wiring mistake -- a wrong tensor fed forward, a wrong residual, a transposed
 operand, a missed cache write -- fails a check.  A float64 torch restatement
-of the layer on a random tiny case is an extra cross-check; beyond these the
+of the layer on random tiny cases, bf16 and FP8 (the FP8 one quantising with
+torch's own e4m3 cast), is a further cross-check; beyond these the
 full-layer numbers are "parity unpinned" (no page prints a worked layer).
 """
 import math
@@ -170,8 +171,24 @@ def test_rejects_non_consecutive_positions():
         oracle.decode_step(cfg, {"layers": [synth.make_layer_weights(cfg, 0)]}, inputs)
 
 
-def _torch_layer(cfg, w, inputs):
-    """float64 torch restatement of the layer (extra cross-check)."""
+def _quant_groups(v32):
+    """Per-token e4m3 quantisation in groups of 128 (fp32 scale = amax / 448,
+    code = e4m3(x / scale) in fp32), with torch's own float8_e4m3fn cast.
+    Returns the codes (uint8), the scales and the dequantised float64."""
+    M, K = v32.shape
+    g = v32.reshape(M, K // 128, 128)
+    amax = g.abs().amax(-1)
+    s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (g / s[..., None]).to(torch.float8_e4m3fn)
+    deq = (codes.double() * s.double()[..., None]).reshape(M, K)
+    return codes.view(torch.uint8).reshape(M, K), s, deq
+
+
+def _torch_layer(cfg, w, inputs, sites=None):
+    """float64 torch restatement of the layer (extra cross-check).  With
+    cfg.fp8 every projection input is quantised from fp32 (_quant_groups)
+    and the weights are e4m3 codes times their 128x128 block scales; the
+    codes and scales of the four quantisation sites go into `sites`."""
     bf = lambda t: t.to(torch.bfloat16).double()
     d, G, P = cfg.head_dim, cfg.n_q_heads // cfg.n_kv_heads, cfg.page_size
     x, res = inputs["x"].double(), inputs["residual"].double()
@@ -180,9 +197,19 @@ def _torch_layer(cfg, w, inputs):
     def rms(v, wt):
         return v / torch.sqrt((v * v).mean(-1, keepdim=True) + cfg.eps) * wt.double()
 
+    def proj(a, name, site):
+        """a: the unrounded float64 input of the projection."""
+        if not cfg.fp8:
+            return bf(a) @ w[name].double().T
+        codes, scales, deq = _quant_groups(a.float())
+        if sites is not None:
+            sites[site] = (codes, scales)
+        wd = w[name].view(torch.float8_e4m3fn).double() * torch.kron(
+            w[name + "_scale"].double(), torch.ones(128, 128, dtype=torch.float64))
+        return deq @ wd.T
+
     r1 = bf(x + res)
-    h1 = bf(rms(r1, w["ln1_w"]))
-    qkv = bf(h1 @ w["w_qkv"].double().T)
+    qkv = bf(proj(rms(r1, w["ln1_w"]), "w_qkv", "h1"))
     M = cfg.M
     heads = qkv.view(M, -1, d)
     Hq, Hkv = cfg.n_q_heads, cfg.n_kv_heads
@@ -213,14 +240,12 @@ def _torch_layer(cfg, w, inputs):
             K = torch.stack([cache[0, a, 0, hq // G, s] for a, s in zip(idx, sl)]).double()
             V = torch.stack([cache[0, a, 1, hq // G, s] for a, s in zip(idx, sl)]).double()
             attn[m, hq] = torch.softmax(q[m, hq] @ K.T / math.sqrt(d), 0) @ V
-    attn = bf(attn.view(M, -1))
-    o2 = bf(attn @ w["w_o"].double().T)
+    o2 = bf(proj(attn.view(M, -1), "w_o", "attn"))
     r2 = bf(o2 + r1)
-    h2 = bf(rms(r2, w["ln2_w"]))
-    gu = bf(h2 @ w["w_gate_up"].double().T)
+    gu = bf(proj(rms(r2, w["ln2_w"]), "w_gate_up", "h2"))
     I = cfg.inter
-    a = bf(torch.nn.functional.silu(gu[:, :I]) * gu[:, I:])
-    y = bf(a @ w["w_down"].double().T)
+    a = torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]
+    y = bf(proj(a, "w_down", "act"))
     return y, r2
 
 
@@ -236,3 +261,35 @@ def test_random_layer_matches_float64_torch_restatement():
         # identical up to a rare bf16 rounding flip of an intermediate
         assert diff.max() <= 2 ** -6 * (1 + np.abs(want.numpy()).max())
         assert (diff == 0).mean() > 0.95
+
+
+@pytest.mark.parametrize("shape", [
+    dict(hidden=256, inter=384, n_q_heads=4, n_kv_heads=2),
+    dict(hidden=512, inter=768, n_q_heads=4, n_kv_heads=1, seed=5),
+])
+def test_fp8_layer_matches_float64_torch_restatement(shape):
+    """The FP8 layer against its float64 torch restatement: the codes and
+    scales at each quantisation site (h1, attention output, h2, SiLU·mul)
+    and the layer outputs agree element for element, up to a rare rounding
+    flip of an intermediate.  One k-block scale misplaced in the oracle's
+    weights (planted here through its input) leaves most outputs different,
+    so the agreement pins where each scale and quantisation enters."""
+    cfg = TINY.replace(fp8=True, **shape)
+    w = synth.make_layer_weights(cfg, 0)       # e4m3 codes + block scales
+    inputs = synth.make_inputs(cfg)
+    r = oracle.decode_step(cfg, {"layers": [w]}, inputs, trace=True)
+    sites = {}
+    y, r2 = _torch_layer(cfg, w, inputs, sites)
+    for name, (codes, scales) in sites.items():
+        assert (r[name + "_codes"] == codes.numpy()).mean() > 0.999, name
+        assert (r[name + "_scales"] == scales.numpy()).mean() > 0.99, name
+    for got, want in ((r["out"][0], y), (r["out"][1], r2)):
+        diff = np.abs(f64(got) - want.numpy())
+        assert diff.max() <= 2 ** -6 * (1 + np.abs(want.numpy()).max())
+        assert (diff == 0).mean() > 0.99
+    bad = dict(w)
+    sc = w["w_down_scale"].clone()
+    sc[:, [0, 1]] = sc[:, [1, 0]]
+    bad["w_down_scale"] = sc
+    rb = oracle.decode_step(cfg, {"layers": [bad]}, inputs)
+    assert (f64(rb["out"][0]) == y.numpy()).mean() < 0.5
