@@ -140,6 +140,8 @@ struct dl_plan {
   int attn_pre_stages = 3;
   // the tcgen05 attention loads a 64-key block as one 4-D TMA box
   bool attn_kv4 = true;
+  // 64-key blocks each attention CTA takes at least (when its pair has them)
+  int attn_min_blocks = 4;
   // add + RMSNorm rows split over clusters of up to this many CTAs (1, 2, 4)
   int norm_split = 4;
   unsigned long long budget_ns = 1000000000ull;
@@ -386,10 +388,14 @@ static void defer_fixups(std::vector<LaunchOp>& ops) {
 // head) pair when the pairs are fewer than the SMs, so that no CTA's range
 // straddles two pairs (a straddling CTA merges and publishes mid-range and
 // holds up both pairs' combines); at most 62 per pair (the combine's weights
-// sit in two lanes of a warp); never more than the units.
-int dl::attn_ctas(int pairs, int nb, int sms) {
+// sit in two lanes of a warp); never more than the units.  min_blocks > 1
+// gives each CTA at least that many 64-key blocks of its pair (fewer
+// contributors for the pair's combine).
+int dl::attn_ctas(int pairs, int nb, int sms, int min_blocks) {
   const long long U = static_cast<long long>(pairs) * nb;
-  long long g = pairs <= sms ? static_cast<long long>(pairs) * std::min(62, sms / pairs) : sms;
+  const int per = std::min(std::min(62, sms / std::max(1, pairs)),
+                           std::max(1, (nb + min_blocks - 1) / std::max(1, min_blocks)));
+  long long g = pairs <= sms ? static_cast<long long>(pairs) * per : sms;
   return static_cast<int>(std::max(1LL, std::min(g, U)));
 }
 
@@ -426,7 +432,7 @@ static LaunchOp make_attn(dl_plan* p, int layer, unsigned* cnt) {
   a.pre_stages = p->attn_pre_stages;
   a.kv4 = p->attn_tc && p->attn_kv4 && p->P % kAttnKeys == 0 && p->d == 128 ? 1 : 0;
   a.split_sm = p->split_sm ? 1 : 0;
-  a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms);
+  a.G = attn_ctas(a.R * a.Hkv, a.NB, p->sms, p->attn_min_blocks);
   // stages of 32 KiB: the tcgen05 engine holds a block from its arrival to
   // its PV commit, so it takes as many as fit (up to 6)
   a.stages = p->attn_tc
@@ -1018,6 +1024,7 @@ static dl_status build_plan(dl_plan* p) {
   if (const char* e = std::getenv("DL_MEGA_HEAD_EVENTS")) p->head_events = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_DEFER_FIXUP")) p->defer_fixup = std::atoi(e) != 0;
   if (const char* e = std::getenv("DL_ATTN_KV4")) p->attn_kv4 = std::atoi(e) != 0;
+  if (const char* e = std::getenv("DL_ATTN_MIN_BLOCKS")) p->attn_min_blocks = std::max(1, std::atoi(e));
   if (const char* e = std::getenv("DL_ATTN_PRE_STAGES")) p->attn_pre_stages = std::max(0, std::atoi(e));
   if (const char* e = std::getenv("DL_NORM_SPLIT")) p->norm_split = std::max(1, std::min(4, std::atoi(e)));
   if (const char* e = std::getenv("DL_ATTN_SPLIT_SOFTMAX")) p->split_sm = std::atoi(e) != 0;

@@ -20,7 +20,7 @@ int gemm_smem_bytes(int npair, int Mp, int stages, int KB, int fp8, int epi, int
 int attn_smem_bytes(int QRp, int stages);
 // CTAs of a split-KV attention over `pairs` (request, kv head) streams of
 // `nb` 64-key blocks on `sms` SMs (dl_host.cu).
-int attn_ctas(int pairs, int nb, int sms);
+int attn_ctas(int pairs, int nb, int sms, int min_blocks = 1);
 // Pipeline stages of the mma.sync attention kernel for a query-row padding
 // (dl_host.cu): one rule for the plans and the allocation-free entry point,
 // so the kernel's shared-memory attribute is the same whichever sets it.
