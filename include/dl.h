@@ -264,7 +264,8 @@ void dl_plan_destroy(dl_plan* plan);
  *                num_pages), after which the output is unspecified).
  * Limits: the partials take G x 2 x QRp x 516 bytes of the 8 MiB.  QRp is
  * tokens_per_request x group size rounded up to 16, 32 or 64.  G is the
- * plans' CTA count: with pairs = num_requests x n_kv_heads, blocks =
+ * CTA count of the split (the plans' rule without their minimum of four
+ * blocks a CTA): with pairs = num_requests x n_kv_heads, blocks =
  * ceil(max_context / 64) and S = num_sms (0: every SM), G = min(pairs x
  * min(62, S / pairs), pairs x blocks) when pairs <= S, else min(S, pairs x
  * blocks); it is at most S.  num_requests x n_kv_heads <= 4096.  Larger

@@ -150,7 +150,9 @@ extern "C" dl_status dl_attention_noalloc(const dl_config* c, int layer, const v
   dl_status st = setup_current_device(&d);
   if (st != DL_OK) return st;
 
-  // ---- launch shape: the plans' split (same CTA count, same stages)
+  // ---- launch shape: the plans' split rule without their minimum of four
+  // blocks a CTA (the documented scratch limit is stated for this count),
+  // the plans' stage rule
   AttnArgs a;
   std::memset(&a, 0, sizeof(a));
   a.kv = DPtr{nullptr, SLOT_KV, 0, 0};
